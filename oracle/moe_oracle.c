@@ -1,0 +1,252 @@
+/*
+ * CPU oracle for the Grok-1 top-2-of-8 Mixture-of-Experts feed-forward layer.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+ * of the package entry file and the CPU-baseline leg of the benchmark may load
+ * or run this file.  It shares no code, header, table or helper with the CUDA
+ * library; the two meet only through the arrays of the seeded input generator.
+ *
+ * What it computes, written as plain loops in the order the sources give it:
+ *
+ *   xn   = RMSNorm_pre(x)                      pre-MoE RMSNorm
+ *   l_e  = <xn, G_e> (+ b_e)                   router logits, e = 0..7
+ *   p    = softmax(l)                          router probabilities
+ *   i0, i1 = top_k(p, 2)                       ties go to the lower index
+ *   o_r  = W1_e (GELU(W_e xn) * (Wv_e xn))     GeGLU expert FFN, e = i_r
+ *   m    = p_i0 o_0 + p_i1 o_1                 probability-weighted combine
+ *   y    = x + RMSNorm_post(m)                 post-MoE RMSNorm, residual add
+ *
+ * Sources (page title, section):
+ *  - "Jah-yee/grok" README, architecture diagram: MoE FFN with 8 experts and
+ *    top-2 routing, expert form GELU(x W) (*) (x Wv) followed by an output
+ *    projection; RMSNorm; list item "Gated GELU".
+ *  - "Unveiling Grok-1" (oneruby-dev), section "Expert Routing Details": the
+ *    router applies softmax to the gate logits and takes jax.lax.top_k(k=2) of
+ *    the softmax outputs, returning those gates unrenormalised; the gating
+ *    noise is for training only.  Section "How MoE Works in Practice": each
+ *    expert output is multiplied by its gate weight and the results summed.
+ *    Section "Why JAX Instead of PyTorch" (block listing): normalised input to
+ *    the MoE sublayer, then x + sublayer output.
+ *  - "TevunahAi/Grok-1-BF16" model card, "Grok-1 Specific Behaviors": four
+ *    norms per layer, pre-MoE and post-MoE among them; "Weight Verification":
+ *    expert tensors linear / linear_v [32768, 6144] and linear_1 [6144, 32768]
+ *    in PyTorch [out, in] order, gate [8, 6144], norm scales [6144];
+ *    "Conversion Details": int8 weights times bf16 scales with grouped scale
+ *    broadcasting, scale shapes (1,N), (8,N), (8,1,N), (8,8,N), transposed from
+ *    JAX [in, out] to PyTorch [out, in].
+ *
+ * Readings where the sources are silent (each also listed in the design notes):
+ *  - GELU is the tanh approximation 0.5 u (1 + tanh(sqrt(2/pi)(u + 0.044715 u^3))).
+ *  - RMSNorm(v) = v / sqrt(mean(v^2) + eps) * scale, scale applied as is.
+ *  - The router sees the unrounded pre-norm output; ties in top-2 go to the
+ *    lower expert index; no capacity limit, no token dropping.
+ *  - The top-2 decision is taken on the probabilities rounded to fp32 (the
+ *    precision the GPU kernel decides in); every value is otherwise computed in
+ *    fp64 and the combine weights are the fp64 probabilities.
+ *  - Grouped scale rule for a weight viewed in JAX order [E, K_in, N] with scale
+ *    shape (E_s, G, N): w[e,k,n] = q[e,k,n] * s[E_s > 1 ? e : 0, k / (K_in/G), n].
+ *    The int8 x bf16 product is exact in fp32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_W_BF16 0
+#define ORACLE_W_INT8 1
+
+static inline float bf16_bits_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* One expert-stacked weight tensor, stored [E, N, K] (PyTorch [out, in]). */
+typedef struct {
+  int32_t dtype;          /* ORACLE_W_BF16 or ORACLE_W_INT8 */
+  const void* q;          /* bf16 bits (uint16) or int8, [E, N, K] */
+  const uint16_t* scale;  /* int8 only: bf16 bits, logical shape (scale_E, scale_G, N) */
+  int32_t scale_E;        /* 1 (shared by experts) or E */
+  int32_t scale_G;        /* number of groups along K_in; 1 = one scale per output channel */
+  int64_t N, K;
+} oracle_weight_t;
+
+/* Dequantised weight element w[e, n, k] ("Conversion Details": int8 x bf16 scale,
+ * grouped broadcasting).  The fp32 product of an 8-bit integer and an 8-bit-
+ * mantissa bf16 is exact. */
+static inline double weight_at(const oracle_weight_t* W, int64_t e, int64_t n, int64_t k) {
+  int64_t off = (e * W->N + n) * W->K + k;
+  if (W->dtype == ORACLE_W_BF16) return (double)bf16_bits_to_float(((const uint16_t*)W->q)[off]);
+  int64_t es = (W->scale_E > 1) ? e : 0;
+  int64_t g = k / (W->K / W->scale_G);
+  float s = bf16_bits_to_float(W->scale[(es * W->scale_G + g) * W->N + n]);
+  float v = (float)((const int8_t*)W->q)[off] * s;
+  return (double)v;
+}
+
+/* Full dequantisation of one weight tensor to fp32 [E, N, K] (for checks). */
+void oracle_dequant(int32_t dtype, const void* q, const uint16_t* scale, int32_t scale_E, int32_t scale_G,
+                    int64_t E, int64_t N, int64_t K, float* out) {
+  oracle_weight_t W = {dtype, q, scale, scale_E, scale_G, N, K};
+  for (int64_t e = 0; e < E; ++e)
+    for (int64_t n = 0; n < N; ++n)
+      for (int64_t k = 0; k < K; ++k) out[(e * N + n) * K + k] = (float)weight_at(&W, e, n, k);
+}
+
+/* GELU, tanh approximation ("Jah-yee/grok" README: gated GELU; the tanh form is
+ * the reading taken where the page names only "GELU"). */
+double oracle_gelu_tanh(double u) {
+  const double c = 0.79788456080286535588; /* sqrt(2/pi) */
+  return 0.5 * u * (1.0 + tanh(c * (u + 0.044715 * u * u * u)));
+}
+
+/* RMSNorm: out_j = v_j / sqrt(mean_i v_i^2 + eps) * s_j. */
+void oracle_rmsnorm(int64_t n, const double* v, const double* s, double eps, double* out) {
+  double ss = 0.0;
+  for (int64_t j = 0; j < n; ++j) ss += v[j] * v[j];
+  double r = 1.0 / sqrt(ss / (double)n + eps);
+  for (int64_t j = 0; j < n; ++j) out[j] = v[j] * r * s[j];
+}
+
+/* Router for one token: pre-norm, logits, softmax, top-2 ("Expert Routing
+ * Details": softmax(gate(x)), then top_k(k=2) of the softmax outputs). */
+static void route_one(int64_t d, int64_t E, const uint16_t* x_row, const float* gate, const float* bias,
+                      const float* s_pre, double eps, double* xn, double* p, int32_t* idx2, double* w2) {
+  double ss = 0.0;
+  for (int64_t j = 0; j < d; ++j) {
+    double xj = (double)bf16_bits_to_float(x_row[j]);
+    ss += xj * xj;
+  }
+  double r = 1.0 / sqrt(ss / (double)d + eps);
+  for (int64_t j = 0; j < d; ++j) xn[j] = (double)bf16_bits_to_float(x_row[j]) * r * (double)s_pre[j];
+
+  double l[64]; /* E <= 64 */
+  for (int64_t e = 0; e < E; ++e) {
+    double acc = 0.0;
+    for (int64_t j = 0; j < d; ++j) acc += xn[j] * (double)gate[e * d + j];
+    l[e] = acc + (bias ? (double)bias[e] : 0.0);
+  }
+  double mx = l[0];
+  for (int64_t e = 1; e < E; ++e)
+    if (l[e] > mx) mx = l[e];
+  double Z = 0.0;
+  for (int64_t e = 0; e < E; ++e) {
+    p[e] = exp(l[e] - mx);
+    Z += p[e];
+  }
+  for (int64_t e = 0; e < E; ++e) p[e] /= Z;
+
+  /* top-2 on the fp32-rounded probabilities, ties to the lower index */
+  int32_t i0 = 0;
+  for (int64_t e = 1; e < E; ++e)
+    if ((float)p[e] > (float)p[i0]) i0 = (int32_t)e;
+  int32_t i1 = (i0 == 0) ? 1 : 0;
+  for (int64_t e = 0; e < E; ++e)
+    if (e != i0 && (float)p[e] > (float)p[i1]) i1 = (int32_t)e;
+  idx2[0] = i0;
+  idx2[1] = i1;
+  w2[0] = p[i0];
+  w2[1] = p[i1];
+}
+
+/* Router over all T tokens.  xn_out [T, d] may be NULL. */
+void oracle_route(int64_t T, int64_t d, int64_t E, const uint16_t* x, const float* gate, const float* bias,
+                  const float* s_pre, double eps, double* xn_out, double* p_out, int32_t* idx_out, double* w_out) {
+#pragma omp parallel
+  {
+    double* xn_local = (double*)malloc((size_t)d * sizeof(double));
+#pragma omp for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+      double* xn = xn_out ? xn_out + t * d : xn_local;
+      route_one(d, E, x + t * d, gate, bias, s_pre, eps, xn, p_out + t * E, idx_out + 2 * t, w_out + 2 * t);
+    }
+    free(xn_local);
+  }
+}
+
+/* One GeGLU expert on one token ("Jah-yee/grok" README: GELU(x W) (*) (x Wv),
+ * then the output projection; shapes from the model card's weight listing).
+ *   h_n = sum_k W[e,n,k] xn_k,  v_n = sum_k Wv[e,n,k] xn_k,  a_n = GELU(h_n) v_n,
+ *   o_j = sum_n W1[e,j,n] a_n.
+ * h, v, a are [F] and o is [d]; h, v may be NULL. */
+static void expert_ffn(int64_t d, int64_t F, int64_t e, const double* xn, const oracle_weight_t* W,
+                       const oracle_weight_t* Wv, const oracle_weight_t* W1, double* h, double* v, double* a,
+                       double* o) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < F; ++n) {
+    double hn = 0.0, vn = 0.0;
+    for (int64_t k = 0; k < d; ++k) {
+      hn += weight_at(W, e, n, k) * xn[k];
+      vn += weight_at(Wv, e, n, k) * xn[k];
+    }
+    if (h) h[n] = hn;
+    if (v) v[n] = vn;
+    a[n] = oracle_gelu_tanh(hn) * vn;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < d; ++j) {
+    double oj = 0.0;
+    for (int64_t n = 0; n < F; ++n) oj += weight_at(W1, e, j, n) * a[n];
+    o[j] = oj;
+  }
+}
+
+static void fill_weights(int32_t dtype, int64_t d, int64_t F, const void* w, const void* wv, const void* w1,
+                         const uint16_t* sw, const uint16_t* swv, const uint16_t* sw1, int32_t scale_E,
+                         int32_t scale_G_up, int32_t scale_G_down, oracle_weight_t* W, oracle_weight_t* Wv,
+                         oracle_weight_t* W1) {
+  oracle_weight_t a = {dtype, w, sw, scale_E, scale_G_up, F, d};
+  oracle_weight_t b = {dtype, wv, swv, scale_E, scale_G_up, F, d};
+  oracle_weight_t c = {dtype, w1, sw1, scale_E, scale_G_down, d, F};
+  *W = a;
+  *Wv = b;
+  *W1 = c;
+}
+
+/* One expert's FFN intermediates for one pre-normed token vector xn [d]. */
+void oracle_expert_ffn(int64_t d, int64_t F, int64_t e, const double* xn, int32_t dtype, const void* w,
+                       const void* wv, const void* w1, const uint16_t* sw, const uint16_t* swv,
+                       const uint16_t* sw1, int32_t scale_E, int32_t scale_G_up, int32_t scale_G_down, double* h,
+                       double* v, double* a, double* o) {
+  oracle_weight_t W, Wv, W1;
+  fill_weights(dtype, d, F, w, wv, w1, sw, swv, sw1, scale_E, scale_G_up, scale_G_down, &W, &Wv, &W1);
+  expert_ffn(d, F, e, xn, &W, &Wv, &W1, h, v, a, o);
+}
+
+/* The whole layer for a list of tokens (any subset of the T rows of x).
+ * Outputs, per listed token i: y [n, d] = x + RMSNorm_post(m), m [n, d] (may be
+ * NULL), idx [n, 2], w [n, 2] (combine weights), p [n, E] (probabilities).
+ * scratch must hold 2 * F + 3 * d doubles. */
+void oracle_moe_tokens(int64_t n_tok, const int64_t* tok, int64_t d, int64_t F, int64_t E, const uint16_t* x,
+                       const float* gate, const float* bias, const float* s_pre, const float* s_post, double eps,
+                       int32_t dtype, const void* w, const void* wv, const void* w1, const uint16_t* sw,
+                       const uint16_t* swv, const uint16_t* sw1, int32_t scale_E, int32_t scale_G_up,
+                       int32_t scale_G_down, double* y, double* m_out, int32_t* idx, double* wts, double* p,
+                       double* scratch) {
+  oracle_weight_t W, Wv, W1;
+  fill_weights(dtype, d, F, w, wv, w1, sw, swv, sw1, scale_E, scale_G_up, scale_G_down, &W, &Wv, &W1);
+  double* a = scratch;       /* [F] */
+  double* xn = a + F;        /* [d] */
+  double* o = xn + d;        /* [d] */
+  double* m = o + d;         /* [d] */
+  for (int64_t i = 0; i < n_tok; ++i) {
+    int64_t t = tok[i];
+    const uint16_t* x_row = x + t * d;
+    route_one(d, E, x_row, gate, bias, s_pre, eps, xn, p + i * E, idx + 2 * i, wts + 2 * i);
+    for (int64_t j = 0; j < d; ++j) m[j] = 0.0;
+    for (int r = 0; r < 2; ++r) {
+      int64_t e = idx[2 * i + r];
+      expert_ffn(d, F, e, xn, &W, &Wv, &W1, NULL, NULL, a, o);
+      for (int64_t j = 0; j < d; ++j) m[j] += wts[2 * i + r] * o[j];
+    }
+    if (m_out)
+      for (int64_t j = 0; j < d; ++j) m_out[i * d + j] = m[j];
+    /* y = x + RMSNorm_post(m) */
+    double ss = 0.0;
+    for (int64_t j = 0; j < d; ++j) ss += m[j] * m[j];
+    double rr = 1.0 / sqrt(ss / (double)d + eps);
+    for (int64_t j = 0; j < d; ++j)
+      y[i * d + j] = (double)bf16_bits_to_float(x_row[j]) + m[j] * rr * (double)s_post[j];
+  }
+}
