@@ -1,0 +1,196 @@
+/*
+ * moe_layer.h - C ABI of the Grok-1 top-2-of-8 Mixture-of-Experts feed-forward
+ * layer on NVIDIA B300 (sm_103a).
+ *
+ * The layer, per token t (hidden state x_t of d_model values):
+ *
+ *   xn    = RMSNorm_pre(x_t)                 = x_t / sqrt(mean(x_t^2) + eps) * s_pre
+ *   p     = softmax(G xn + b)                  G [E, d] router gate, b optional
+ *   i0,i1 = the two largest p, ties to the lower index; weights p_i0, p_i1 (not
+ *           renormalised)
+ *   o_r   = W1_e (GELU_tanh(W_e xn) * (Wv_e xn)),  e = i_r
+ *   y_t   = x_t + RMSNorm_post(p_i0 o_0 + p_i1 o_1)
+ *
+ * Sources (page title, section): "Jah-yee/grok" README, architecture diagram
+ * (8 experts, top-2, GELU(x W) (*) (x Wv) then the output projection, RMSNorm);
+ * "Unveiling Grok-1" (oneruby-dev), "Expert Routing Details" (softmax of the
+ * gate logits, then top_k(k=2) of the softmax outputs) and "How MoE Works in
+ * Practice" (gate-weighted sum of the expert outputs); "TevunahAi/Grok-1-BF16"
+ * model card, "Grok-1 Specific Behaviors" (pre-MoE and post-MoE norms),
+ * "Weight Verification" (tensor shapes, PyTorch [out, in] order) and
+ * "Conversion Details" (int8 weights with bf16 scales).
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are CUDA global-memory addresses on the device that was
+ *    current when the handle was created; host pointers are ordinary CPU memory.
+ *    Each argument's comment says which.  All must be 16-byte aligned.
+ *  - A stream argument is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).
+ *  - Argument errors are returned synchronously, before anything is enqueued.
+ *    Errors found on the device (a bounded wait that ran out, an index check of
+ *    MOE_FLAG_DEVICE_CHECKS) are latched in the handle and reported by
+ *    moe_layer_sync_status().  No kernel of this library traps or spins without
+ *    a limit.
+ *  - moe_last_error_message() gives a one-line description of the last error
+ *    returned on the calling thread.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, T out of range, bad config value */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape or dtype this build does not implement */
+  MOE_ERR_OOM = 3,          /* workspace allocation failed in moe_layer_create */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed */
+  MOE_ERR_DEVICE_CHECK = 5, /* a device-side index check failed (MOE_FLAG_DEVICE_CHECKS) */
+  MOE_ERR_TIMEOUT = 6       /* a bounded device wait ran out; the kernel returned early */
+} moe_status_t;
+
+typedef enum { MOE_WEIGHT_BF16 = 0, MOE_WEIGHT_INT8 = 1 } moe_weight_dtype_t;
+
+/* Bits of moe_config_t.flags */
+#define MOE_FLAG_DEVICE_CHECKS 0x1u /* kernels validate routing indices and row maps */
+#define MOE_FLAG_FORCE_TC 0x2u      /* always use the tensor-core grouped GEMM path */
+#define MOE_FLAG_FORCE_GEMV 0x4u    /* always use the weight-streaming decode path */
+
+typedef struct {
+  int32_t d_model;      /* d: multiple of 128 (Grok-1: 6144) */
+  int32_t d_ffn;        /* F: multiple of 128 (Grok-1: 32768) */
+  int32_t num_experts;  /* E: must be 8 */
+  int32_t top_k;        /* must be 2 */
+  int32_t max_tokens;   /* largest T any forward call will pass (>= 1); sizes the workspace */
+  float eps;            /* RMSNorm epsilon (Grok-1 configs: 1e-5) */
+  int32_t weight_dtype; /* moe_weight_dtype_t */
+  uint32_t flags;       /* MOE_FLAG_* */
+} moe_config_t;
+
+/*
+ * Layer parameters.  DEVICE pointers, BORROWED: the caller keeps them alive and
+ * unchanged for the life of the handle (the library keeps TMA descriptors that
+ * point into them).  Layouts are row-major, PyTorch [out, in] order for the
+ * expert matrices ("TevunahAi/Grok-1-BF16", "Weight Verification").
+ */
+typedef struct {
+  const float* gate;            /* [E, d] fp32 router gate (moe_block.gate.weight) */
+  const float* gate_bias;       /* [E] fp32 added to the logits, or NULL for none */
+  const void* w;                /* [E, F, d] bf16 or int8: GELU branch ("linear") */
+  const void* wv;               /* [E, F, d] bf16 or int8: linear branch ("linear_v") */
+  const void* w1;               /* [E, d, F] bf16 or int8: down projection ("linear_1") */
+  const uint16_t* w_scale;      /* int8 only: bf16 bits [E, F], one scale per expert and output
+                                   channel (the logical (8, 1, N) scale shape); NULL for bf16 */
+  const uint16_t* wv_scale;     /* int8 only: bf16 bits [E, F] */
+  const uint16_t* w1_scale;     /* int8 only: bf16 bits [E, d] */
+  const float* pre_norm_scale;  /* [d] fp32 (pre_moe_norm.scale) */
+  const float* post_norm_scale; /* [d] fp32 (post_moe_norm.scale) */
+} moe_weights_t;
+
+typedef struct moe_layer moe_layer_t;
+
+/*
+ * Validate cfg, take the borrowed weight pointers, build the TMA descriptors and
+ * allocate the workspace for cfg->max_tokens tokens on the current device.
+ * Launches no kernel.  On success *out receives the handle (owned by the caller,
+ * freed by moe_layer_destroy).  Errors: MOE_ERR_INVALID_ARG (null / misaligned
+ * pointer, max_tokens < 1, eps <= 0), MOE_ERR_UNSUPPORTED (E != 8, top_k != 2,
+ * d or F not a multiple of 128, d > 16384, int8 without scales, device not
+ * sm_103 / sm_100 class), MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weights, moe_layer_t** out);
+
+/*
+ * The layer on T tokens, asynchronous on `stream`.
+ *   hidden        DEVICE [T, d] bf16, read only
+ *   out           DEVICE [T, d] bf16, written; may equal `hidden` (in place)
+ *   T             0 <= T <= max_tokens; T == 0 enqueues nothing
+ *   topk_idx      DEVICE [T, 2] int32 or NULL: chosen experts in rank order
+ *   topk_prob     DEVICE [T, 2] fp32 or NULL: their softmax probabilities
+ *   expert_counts DEVICE [E] int32 or NULL: tokens routed to each expert
+ * The host never waits on the device and reads nothing back, so the call may be
+ * captured in a CUDA graph.  Calls on one handle must not overlap on the device
+ * (they share the workspace): issue them on one stream, or order the streams.
+ */
+moe_status_t moe_layer_forward(moe_layer_t* layer, const void* hidden, void* out, int32_t T, void* stream,
+                               int32_t* topk_idx, float* topk_prob, int32_t* expert_counts);
+
+/*
+ * Same layer, HOST buffers: copies hidden_host to the device, runs the layer
+ * and copies the results back, then waits for `stream`.  Synchronous.
+ *   hidden_host   HOST [T, d] bf16 (pinned memory gives full copy bandwidth)
+ *   out_host      HOST [T, d] bf16
+ *   topk_idx_host HOST [T, 2] int32 or NULL; topk_prob_host HOST [T, 2] fp32 or
+ *   NULL; expert_counts_host HOST [E] int32 or NULL.
+ * Uses a device staging area of the handle (allocated on first use).  Returns
+ * device-side errors directly (it synchronises).
+ */
+moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* hidden_host, void* out_host, int32_t T,
+                                    void* stream, int32_t* topk_idx_host, float* topk_prob_host,
+                                    int32_t* expert_counts_host);
+
+/* Wait for `stream`, then return (and clear) the first device-side error any
+ * earlier forward on this handle latched: MOE_OK, MOE_ERR_TIMEOUT,
+ * MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */
+moe_status_t moe_layer_sync_status(moe_layer_t* layer, void* stream);
+
+/* Free the workspace and the handle.  Waits for the device first.  NULL is a no-op. */
+moe_status_t moe_layer_destroy(moe_layer_t* layer);
+
+/* Static string naming a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* One-line detail of the last error returned on this thread ("" if none). */
+const char* moe_last_error_message(void);
+
+/* ----------------------------------------------------------- measurement */
+
+/* Kernels of one forward, in launch order (indices of the profiling arrays). */
+typedef enum {
+  MOE_K_ROUTER = 0,   /* pre-norm + router logits + softmax + top-2 */
+  MOE_K_PERMUTE = 1,  /* per-expert counts, padded offsets, stable slot order */
+  MOE_K_GATHER = 2,   /* copy of normed rows into expert-contiguous order */
+  MOE_K_UP = 3,       /* expert up-projections W, Wv with the GeGLU epilogue */
+  MOE_K_DOWN = 4,     /* expert down-projection W1, scaled by the combine weight */
+  MOE_K_COMBINE = 5,  /* combine of the two expert rows + post-norm + residual */
+  MOE_K_COUNT = 6
+} moe_kernel_id_t;
+
+/* Turn per-kernel CUDA-event timing of later forwards on (1) or off (0).
+ * Events are recorded on the forward's stream around each kernel. */
+moe_status_t moe_layer_set_profiling(moe_layer_t* layer, int32_t enable);
+
+/* Waits for the recorded events and returns, per kernel id, the summed device
+ * time in ms (ms_total[MOE_K_COUNT]) and the number of timed launches
+ * (launches[MOE_K_COUNT]) since the last reset.  Either array may be NULL.
+ * reset != 0 clears the sums afterwards. */
+moe_status_t moe_layer_profile_read(moe_layer_t* layer, double* ms_total, int64_t* launches, int32_t reset);
+
+/* Kernel launches enqueued by this handle since creation (all kernels). */
+int64_t moe_layer_launch_count(const moe_layer_t* layer);
+
+/* Workspace introspection (DEVICE pointers into the handle's workspace, valid
+ * until destroy; contents are those of the last forward once it completed). */
+typedef struct {
+  void* xn;             /* [max_tokens, d] bf16: pre-norm output */
+  int32_t* counts;      /* [E] tokens per expert */
+  int32_t* row_offset;  /* [E + 1] first permuted row of each expert (multiples of 128) */
+  int32_t* row_of_slot; /* [max_tokens, 2] permuted row of (token, rank) */
+  void* xn_perm;        /* [rows_cap, d] bf16: normed rows in expert order */
+  void* act;            /* [rows_cap, F] bf16: GELU(h) * v per permuted row */
+  float* y_rows;        /* [rows_cap, d] fp32: p * (W1 act) per permuted row */
+  int64_t rows_cap;     /* capacity in permuted rows */
+} moe_workspace_view_t;
+
+moe_status_t moe_layer_workspace(const moe_layer_t* layer, moe_workspace_view_t* view);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

@@ -1,0 +1,42 @@
+// Shared constants and small helpers of the MoE layer kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kNumExperts = 8;   // Grok-1: 8 experts ("Jah-yee/grok" README, architecture diagram)
+constexpr int kTopK = 2;         // top-2 routing
+constexpr int kRowTile = 128;    // rows of one expert tile; expert row blocks are padded to it
+
+// Device error word bits (latched in the handle, read by moe_layer_sync_status).
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrCheck = 2u;
+
+// Layout of the small scheduling block K2 writes and the GEMMs read:
+//   [0, E)        counts[e]       slots routed to expert e
+//   [E, 2E + 1)   row_offset[e]   first permuted row of expert e (multiple of kRowTile);
+//                                 row_offset[E] = total padded rows
+constexpr int kSchedInts = 2 * kNumExperts + 1;
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// GELU, tanh approximation: 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3))).
+__device__ __forceinline__ float gelu_tanh(float u) {
+  const float c = 0.7978845608028654f;
+  return 0.5f * u * (1.0f + tanhf(c * fmaf(0.044715f * u, u * u, u)));
+}
+
+}  // namespace moe

@@ -1,0 +1,72 @@
+// K5: combine of the two expert rows + post-MoE RMSNorm + residual add.
+//
+// Per token t ("Unveiling Grok-1", "How MoE Works in Practice": gate-weighted
+// sum of the chosen experts' outputs; "TevunahAi/Grok-1-BF16", "Grok-1 Specific
+// Behaviors": post-MoE norm; "Why JAX Instead of PyTorch" block listing:
+// x + sublayer output):
+//   m   = Y[row(t,0)] + Y[row(t,1)]       (Y rows already hold p * o, fp32)
+//   out = bf16(x + m / sqrt(mean(m^2) + eps) * s_post)
+// One CTA of 256 threads per token; m stays in registers between the two
+// passes (d <= 256 * 4 * kCombineVec), 16-byte loads and stores throughout.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kCombineThreads = 256;
+constexpr int kCombineVec = 16;  // float4 per thread kept in registers: d <= 16384
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const float* __restrict__ y_rows, const int32_t* __restrict__ row_of_slot, const __nv_bfloat16* x,
+    const float* __restrict__ s_post, float eps, int d, int rows_valid_cap, int checks, uint32_t* __restrict__ err,
+    __nv_bfloat16* out) {
+  __shared__ float red[kCombineThreads / 32];
+  const int t = blockIdx.x;
+  int r0 = row_of_slot[2 * t], r1 = row_of_slot[2 * t + 1];
+  if (checks && (r0 < 0 || r0 >= rows_valid_cap || r1 < 0 || r1 >= rows_valid_cap)) {
+    if (threadIdx.x == 0) atomicOr(err, kErrCheck);
+    r0 = r1 = 0;
+  }
+  const float4* y0 = reinterpret_cast<const float4*>(y_rows + (size_t)r0 * d);
+  const float4* y1 = reinterpret_cast<const float4*>(y_rows + (size_t)r1 * d);
+  const int nv = d >> 2;
+  float4 m[kCombineVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCombineVec; ++i) {
+    const int c = threadIdx.x + i * kCombineThreads;
+    if (c < nv) {
+      const float4 a = y0[c], b = y1[c];
+      m[i] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+      ss = fmaf(m[i].x, m[i].x, ss);
+      ss = fmaf(m[i].y, m[i].y, ss);
+      ss = fmaf(m[i].z, m[i].z, ss);
+      ss = fmaf(m[i].w, m[i].w, ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) tot += red[w];
+  const float rr = 1.0f / sqrtf(tot / (float)d + eps);
+
+  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d);
+  uint2* orow = reinterpret_cast<uint2*>(out + (size_t)t * d);
+#pragma unroll
+  for (int i = 0; i < kCombineVec; ++i) {
+    const int c = threadIdx.x + i * kCombineThreads;
+    if (c < nv) {
+      const float4 s = reinterpret_cast<const float4*>(s_post)[c];
+      const uint2 xv = xr[c];  // read before the (possibly aliasing) write below
+      uint2 o;
+      o.x = pack_bf16x2(bf16_lo(xv.x) + m[i].x * rr * s.x, bf16_hi(xv.x) + m[i].y * rr * s.y);
+      o.y = pack_bf16x2(bf16_lo(xv.y) + m[i].z * rr * s.z, bf16_hi(xv.y) + m[i].w * rr * s.w);
+      orow[c] = o;
+    }
+  }
+}
+
+}  // namespace moe

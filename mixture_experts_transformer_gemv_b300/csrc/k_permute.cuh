@@ -1,0 +1,132 @@
+// K2: per-expert grouping of the 2T (token, rank) slots, and the row gather.
+//
+// The sources route every token to two experts and sum the experts' outputs
+// ("Unveiling Grok-1", "How MoE Works in Practice"); they do not say how the
+// work is grouped.  Here the slots are grouped so each expert's rows are
+// contiguous and its expert FFN becomes a dense GEMM:
+//   counts[e]      = #slots with expert e
+//   row_offset[e]  = sum_{e' < e} ceil(counts[e'] / 128) * 128   (tiles never mix experts)
+//   rows of expert e, in slot order s = 2t + r (stable: token, then rank);
+//   padding rows (up to the next multiple of 128) get token -1 and weight 0.
+// A single CTA does the scan (it is a few microseconds even at T = 65536);
+// the gather of the normed rows into expert order runs on all SMs.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPermuteThreads = 1024;
+
+__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int32_t* __restrict__ sched,
+    int32_t* __restrict__ row_of_slot, int32_t* __restrict__ token_of_row, float* __restrict__ prob_of_row,
+    int32_t* __restrict__ user_counts, int rows_cap, int checks, uint32_t* __restrict__ err) {
+  __shared__ int32_t warp_tot[kPermuteThreads / 32][kNumExperts];
+  __shared__ int32_t s_counts[kNumExperts];
+  __shared__ int32_t s_off[kNumExperts + 1];
+  const int S = 2 * T;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (S + kPermuteThreads - 1) / kPermuteThreads;
+  const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+
+  int cnt[kNumExperts];
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) cnt[e] = 0;
+  for (int s = s0; s < s1; ++s) {
+    int e = idx[s];
+    if (checks && (e < 0 || e >= kNumExperts)) {
+      atomicOr(err, kErrCheck);
+      e = 0;
+    }
+#pragma unroll
+    for (int q = 0; q < kNumExperts; ++q) cnt[q] += (q == e);
+  }
+  // exclusive scan over threads, per expert: warp scan then scan of warp totals
+  int excl[kNumExperts];
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) {
+    int v = cnt[e];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    excl[e] = v - cnt[e];
+    if (lane == 31) warp_tot[warp][e] = v;
+  }
+  __syncthreads();
+  if (tid < kNumExperts) {
+    int run = 0;
+    for (int w = 0; w < kPermuteThreads / 32; ++w) {
+      int v = warp_tot[w][tid];
+      warp_tot[w][tid] = run;
+      run += v;
+    }
+    s_counts[tid] = run;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0;
+    for (int e = 0; e < kNumExperts; ++e) {
+      s_off[e] = off;
+      off += (s_counts[e] + kRowTile - 1) / kRowTile * kRowTile;
+    }
+    s_off[kNumExperts] = off;
+    if (checks && off > rows_cap) atomicOr(err, kErrCheck);
+  }
+  __syncthreads();
+  int pos[kNumExperts];
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) pos[e] = s_off[e] + warp_tot[warp][e] + excl[e];
+  for (int s = s0; s < s1; ++s) {
+    int e = idx[s];
+    if (checks && (e < 0 || e >= kNumExperts)) e = 0;
+    int row = 0;
+#pragma unroll
+    for (int q = 0; q < kNumExperts; ++q)
+      if (q == e) row = pos[q]++;
+    if (checks && row >= rows_cap) {
+      atomicOr(err, kErrCheck);
+      row_of_slot[s] = 0;
+      continue;
+    }
+    row_of_slot[s] = row;
+    token_of_row[row] = s >> 1;
+    prob_of_row[row] = prob[s];
+  }
+  // padding rows of every expert block
+  for (int e = 0; e < kNumExperts; ++e) {
+    const int r0 = s_off[e] + s_counts[e], r1 = min(s_off[e + 1], rows_cap);
+    for (int row = r0 + tid; row < r1; row += kPermuteThreads) {
+      token_of_row[row] = -1;
+      prob_of_row[row] = 0.f;
+    }
+  }
+  if (tid < kNumExperts) {
+    sched[tid] = s_counts[tid];
+    if (user_counts) user_counts[tid] = s_counts[tid];
+  }
+  if (tid <= kNumExperts) sched[kNumExperts + tid] = s_off[tid];
+}
+
+// xn_perm[row] = xn[token_of_row[row]] (zeros for padding rows); rows beyond
+// row_offset[E] are left alone.  Grid-stride over rows, 16-byte accesses.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ xn,
+                                                          const int32_t* __restrict__ token_of_row,
+                                                          const int32_t* __restrict__ sched, int d,
+                                                          __nv_bfloat16* __restrict__ xn_perm) {
+  const int rows = sched[2 * kNumExperts];
+  const int nchunk = d >> 3;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int tok = token_of_row[row];
+    uint4* dst = reinterpret_cast<uint4*>(xn_perm + (size_t)row * d);
+    if (tok >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(xn + (size_t)tok * d);
+      for (int c = threadIdx.x; c < nchunk; c += blockDim.x) dst[c] = src[c];
+    } else {
+      for (int c = threadIdx.x; c < nchunk; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+}  // namespace moe

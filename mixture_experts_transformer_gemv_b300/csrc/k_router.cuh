@@ -1,0 +1,187 @@
+// K1: pre-MoE RMSNorm + router logits + softmax + top-2, fused.
+//
+// Per token t ("TevunahAi/Grok-1-BF16" model card, "Grok-1 Specific Behaviors":
+// pre-MoE norm; "Unveiling Grok-1", "Expert Routing Details": softmax of the gate
+// logits, then top_k(k=2) of the softmax outputs):
+//   r      = 1 / sqrt(mean_j x_j^2 + eps)
+//   xn_j   = x_j * r * s_pre_j               (fp32; written out rounded to bf16)
+//   l_e    = sum_j xn_j G[e, j] + b_e        (from the fp32 xn, not the bf16 copy)
+//   p      = softmax(l)                      (max-subtracted, fp32)
+//   i0, i1 = two largest p, ties to the lower index; weights p_i0, p_i1
+//
+// One CTA of 256 threads handles kRouterTok tokens: every gate value it loads
+// feeds all of them (the gate is [8, d] fp32 and is read from L2 once per CTA,
+// not once per token).  x rows are read with 16-byte loads, twice (the second
+// pass hits L1/L2).
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRouterThreads = 256;
+constexpr int kRouterTok = 4;
+
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(
+    const __nv_bfloat16* __restrict__ x, int T, int d, const float* __restrict__ gate,
+    const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
+    __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
+    int32_t* __restrict__ user_idx, float* __restrict__ user_prob) {
+  __shared__ float red[kRouterThreads / 32][kRouterTok * kNumExperts];
+  __shared__ float rnorm[kRouterTok];
+  const int t0 = blockIdx.x * kRouterTok;
+  const int ntok = min(kRouterTok, T - t0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = d >> 3;  // 8 bf16 per 16-byte chunk
+
+  // ---- pass 1: sum of squares per token
+  float ss[kRouterTok];
+#pragma unroll
+  for (int i = 0; i < kRouterTok; ++i) ss[i] = 0.f;
+  for (int c = threadIdx.x; c < nchunk; c += kRouterThreads) {
+#pragma unroll
+    for (int i = 0; i < kRouterTok; ++i) {
+      if (i < ntok) {
+        uint4 v = ld_nc_v4(x + (size_t)(t0 + i) * d + c * 8);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
+          ss[i] = fmaf(a, a, ss[i]);
+          ss[i] = fmaf(b, b, ss[i]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kRouterTok; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+    if (lane == 0) red[warp][i] = ss[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < kRouterTok) {
+    float s = 0.f;
+    for (int w = 0; w < kRouterThreads / 32; ++w) s += red[w][threadIdx.x];
+    rnorm[threadIdx.x] = 1.0f / sqrtf(s / (float)d + eps);
+  }
+  __syncthreads();
+  float r[kRouterTok];
+#pragma unroll
+  for (int i = 0; i < kRouterTok; ++i) r[i] = rnorm[i];
+
+  // ---- pass 2: xn (bf16 copy out) and the 8 logits of every token
+  float lg[kRouterTok][kNumExperts];
+#pragma unroll
+  for (int i = 0; i < kRouterTok; ++i)
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) lg[i][e] = 0.f;
+
+  for (int c = threadIdx.x; c < nchunk; c += kRouterThreads) {
+    const float4 sa = *reinterpret_cast<const float4*>(s_pre + c * 8);
+    const float4 sb = *reinterpret_cast<const float4*>(s_pre + c * 8 + 4);
+    const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    float g[kNumExperts][8];
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) {
+      const float4 ga = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8);
+      const float4 gb = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8 + 4);
+      g[e][0] = ga.x; g[e][1] = ga.y; g[e][2] = ga.z; g[e][3] = ga.w;
+      g[e][4] = gb.x; g[e][5] = gb.y; g[e][6] = gb.z; g[e][7] = gb.w;
+    }
+#pragma unroll
+    for (int i = 0; i < kRouterTok; ++i) {
+      if (i < ntok) {
+        uint4 v = ld_nc_v4(x + (size_t)(t0 + i) * d + c * 8);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float xn[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          xn[2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
+          xn[2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
+        }
+        uint4 o;
+        o.x = pack_bf16x2(xn[0], xn[1]);
+        o.y = pack_bf16x2(xn[2], xn[3]);
+        o.z = pack_bf16x2(xn[4], xn[5]);
+        o.w = pack_bf16x2(xn[6], xn[7]);
+        *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
+#pragma unroll
+        for (int e = 0; e < kNumExperts; ++e)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xn[j], g[e][j], lg[i][e]);
+      }
+    }
+  }
+  // block reduction of the kRouterTok x 8 partial logits
+#pragma unroll
+  for (int i = 0; i < kRouterTok; ++i)
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) {
+      float v = lg[i][e];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      lg[i][e] = v;
+    }
+  __syncthreads();  // red[] is reused
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kRouterTok; ++i)
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) red[warp][i * kNumExperts + e] = lg[i][e];
+  }
+  __syncthreads();
+
+  // ---- softmax + top-2, one thread per token
+  if (threadIdx.x < ntok) {
+    const int i = threadIdx.x, t = t0 + i;
+    float l[kNumExperts];
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) {
+      float s = 0.f;
+      for (int w = 0; w < kRouterThreads / 32; ++w) s += red[w][i * kNumExperts + e];
+      l[e] = s + (gate_bias ? gate_bias[e] : 0.f);
+    }
+    float mx = l[0];
+#pragma unroll
+    for (int e = 1; e < kNumExperts; ++e) mx = fmaxf(mx, l[e]);
+    float p[kNumExperts], Z = 0.f;
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) {
+      p[e] = expf(l[e] - mx);
+      Z += p[e];
+    }
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) p[e] = p[e] / Z;
+    // strict '>' keeps the lower index on ties
+    int i0 = 0;
+    float b0 = p[0];
+#pragma unroll
+    for (int e = 1; e < kNumExperts; ++e)
+      if (p[e] > b0) {
+        b0 = p[e];
+        i0 = e;
+      }
+    int i1 = -1;
+    float b1 = -1.f;
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e)
+      if (e != i0 && p[e] > b1) {
+        b1 = p[e];
+        i1 = e;
+      }
+    idx_out[2 * t] = i0;
+    idx_out[2 * t + 1] = i1;
+    prob_out[2 * t] = b0;
+    prob_out[2 * t + 1] = b1;
+    if (user_idx) {
+      user_idx[2 * t] = i0;
+      user_idx[2 * t + 1] = i1;
+    }
+    if (user_prob) {
+      user_prob[2 * t] = b0;
+      user_prob[2 * t + 1] = b1;
+    }
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,476 @@
+// Host runtime and C ABI of the Grok-1 MoE layer (declared in include/moe_layer.h).
+//
+// moe_layer_create validates the configuration, keeps the borrowed weight
+// pointers, encodes the TMA descriptors of the expert weights and of the two
+// GEMM activation buffers, and allocates one workspace block.
+// moe_layer_forward enqueues, on the caller's stream and without any host wait:
+//   K1 router_kernel        pre-norm, router logits, softmax, top-2
+//   K2 permute_kernel       counts, padded row offsets, stable slot -> row map
+//      gather_rows_kernel   normed rows into expert-contiguous order
+//   K3 grouped_gemm<geglu>  act = GELU(A W^T) * (A Wv^T)        (tcgen05)
+//   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
+//   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <array>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "moe_layer.h"
+#include "common.cuh"
+#include "k_combine.cuh"
+#include "k_gemm.cuh"
+#include "k_permute.cuh"
+#include "k_router.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+moe_status_t ok() {
+  g_last_error.clear();
+  return MOE_OK;
+}
+
+#define MOE_CUDA_TRY(call)                                                                    \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major 2-D tensor [rows, inner] of 2-byte elements, box [box_rows, 64], 128-byte swizzle.
+moe_status_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+constexpr int kProfRing = 64;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct moe_layer {
+  moe_config_t cfg{};
+  moe_weights_t w{};
+  int device = 0;
+  int num_sms = 0;
+  int64_t rows_cap = 0;
+
+  void* ws = nullptr;
+  __nv_bfloat16* xn = nullptr;
+  int32_t* idx = nullptr;
+  float* prob = nullptr;
+  int32_t* sched = nullptr;
+  int32_t* row_of_slot = nullptr;
+  int32_t* token_of_row = nullptr;
+  float* prob_of_row = nullptr;
+  __nv_bfloat16* xn_perm = nullptr;
+  __nv_bfloat16* act = nullptr;
+  float* y_rows = nullptr;
+  uint32_t* err = nullptr;
+
+  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1{};
+
+  void* host_stage = nullptr;  // device staging for moe_layer_forward_host
+  size_t host_stage_bytes = 0;
+
+  bool profiling = false;
+  std::vector<std::array<cudaEvent_t, MOE_K_COUNT + 1>> ring;
+  std::vector<bool> pending;
+  int ring_next = 0;
+  double prof_ms[MOE_K_COUNT] = {};
+  int64_t prof_n[MOE_K_COUNT] = {};
+  std::atomic<int64_t> launches{0};
+};
+
+namespace {
+
+void harvest(moe_layer* L, int slot) {
+  if (!L->pending[slot]) return;
+  auto& ev = L->ring[slot];
+  cudaEventSynchronize(ev[MOE_K_COUNT]);
+  for (int k = 0; k < MOE_K_COUNT; ++k) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, ev[k], ev[k + 1]) == cudaSuccess) {
+      L->prof_ms[k] += ms;
+      L->prof_n[k] += 1;
+    }
+  }
+  L->pending[slot] = false;
+}
+
+moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T, cudaStream_t st,
+                             int32_t* topk_idx, float* topk_prob, int32_t* counts) {
+  const int d = L->cfg.d_model, F = L->cfg.d_ffn;
+  const int checks = (L->cfg.flags & MOE_FLAG_DEVICE_CHECKS) ? 1 : 0;
+  cudaEvent_t* ev = nullptr;
+  if (L->profiling) {
+    int slot = L->ring_next;
+    L->ring_next = (L->ring_next + 1) % kProfRing;
+    harvest(L, slot);
+    ev = L->ring[slot].data();
+    L->pending[slot] = true;
+  }
+  auto mark = [&](int k) {
+    if (ev) cudaEventRecord(ev[k], st);
+  };
+
+  mark(0);
+  router_kernel<<<(T + kRouterTok - 1) / kRouterTok, kRouterThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
+      L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob);
+  mark(1);
+  permute_kernel<<<1, kPermuteThreads, 0, st>>>(L->idx, L->prob, T, L->sched, L->row_of_slot, L->token_of_row,
+                                               L->prob_of_row, counts, (int)L->rows_cap, checks, L->err);
+  mark(2);
+  {
+    const int grid = (int)std::min<int64_t>(L->rows_cap, (int64_t)L->num_sms * 8);
+    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, L->xn_perm);
+  }
+  mark(3);
+  {
+    GemmParams p{};
+    p.sched = L->sched;
+    p.K = d;
+    p.n_tiles = F / (kGemmBN / 2);
+    p.b_rows_per_expert = F;
+    p.n_out = F;
+    p.out = L->act;
+    p.row_scale = nullptr;
+    p.err = L->err;
+    p.timeout_ns = kWaitLimitNs;
+    grouped_gemm_kernel<kEpiGeglu><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_xn_perm, L->tm_w,
+                                                                                     L->tm_wv, p);
+  }
+  mark(4);
+  {
+    GemmParams p{};
+    p.sched = L->sched;
+    p.K = F;
+    p.n_tiles = (d + kGemmBN - 1) / kGemmBN;
+    p.b_rows_per_expert = d;
+    p.n_out = d;
+    p.out = L->y_rows;
+    p.row_scale = L->prob_of_row;
+    p.err = L->err;
+    p.timeout_ns = kWaitLimitNs;
+    grouped_gemm_kernel<kEpiDown><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_act, L->tm_w1, L->tm_w1,
+                                                                                    p);
+  }
+  mark(5);
+  combine_kernel<<<T, kCombineThreads, 0, st>>>(L->y_rows, L->row_of_slot, static_cast<const __nv_bfloat16*>(hidden),
+                                                L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks,
+                                                L->err, static_cast<__nv_bfloat16*>(out));
+  mark(6);
+  L->launches += MOE_K_COUNT;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_error_message(void) { return g_last_error.c_str(); }
+
+moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, moe_layer_t** out) {
+  if (!cfg || !w || !out) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  const moe_config_t c = *cfg;
+  if (c.num_experts != kNumExperts) return fail(MOE_ERR_UNSUPPORTED, "num_experts must be 8 (got %d)", c.num_experts);
+  if (c.top_k != kTopK) return fail(MOE_ERR_UNSUPPORTED, "top_k must be 2 (got %d)", c.top_k);
+  if (c.d_model <= 0 || c.d_ffn <= 0 || c.d_model % 128 || c.d_ffn % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "d_model and d_ffn must be positive multiples of 128 (got %d, %d)", c.d_model,
+                c.d_ffn);
+  if (c.d_model > 4 * kCombineThreads * kCombineVec)
+    return fail(MOE_ERR_UNSUPPORTED, "d_model > %d", 4 * kCombineThreads * kCombineVec);
+  if ((int64_t)kNumExperts * c.d_ffn > INT32_MAX / 2)
+    return fail(MOE_ERR_UNSUPPORTED, "d_ffn too large");
+  if (c.max_tokens < 1 || c.max_tokens > (1 << 24)) return fail(MOE_ERR_INVALID_ARG, "max_tokens out of range");
+  if (!(c.eps > 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be > 0");
+  if (c.weight_dtype != MOE_WEIGHT_BF16 && c.weight_dtype != MOE_WEIGHT_INT8)
+    return fail(MOE_ERR_INVALID_ARG, "unknown weight_dtype %d", c.weight_dtype);
+  if (c.weight_dtype == MOE_WEIGHT_INT8)
+    return fail(MOE_ERR_UNSUPPORTED, "int8 expert weights are not implemented in this build");
+  if (c.flags & MOE_FLAG_FORCE_GEMV)
+    return fail(MOE_ERR_UNSUPPORTED, "the weight-streaming decode path is not implemented in this build");
+  const void* req[] = {w->gate, w->w, w->wv, w->w1, w->pre_norm_scale, w->post_norm_scale};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
+  if (w->gate_bias && !aligned4(w->gate_bias)) return fail(MOE_ERR_INVALID_ARG, "gate_bias misaligned");
+
+  int dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  MOE_CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
+  if (prop.sharedMemPerBlockOptin < kGemmSmemBytes)
+    return fail(MOE_ERR_UNSUPPORTED, "device offers %zu B shared memory per block, need %zu",
+                (size_t)prop.sharedMemPerBlockOptin, kGemmSmemBytes);
+
+  auto* L = new (std::nothrow) moe_layer();
+  if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
+  L->cfg = c;
+  L->w = *w;
+  L->device = dev;
+  L->num_sms = prop.multiProcessorCount;
+  const int64_t T = c.max_tokens, d = c.d_model, F = c.d_ffn;
+  L->rows_cap = (int64_t)align_up((size_t)(2 * T), kRowTile) + (int64_t)kNumExperts * kRowTile;
+  const int64_t R = L->rows_cap;
+
+  // one workspace block, every buffer 1 KB aligned
+  size_t offs[11], total = 0;
+  const size_t sizes[11] = {(size_t)(T * d * 2), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
+                            (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
+                            (size_t)(R * F * 2), (size_t)(R * d * 4), 256};
+  for (int i = 0; i < 11; ++i) {
+    offs[i] = total;
+    total = align_up(total + sizes[i], 1024);
+  }
+  cudaError_t e = cudaMalloc(&L->ws, total);
+  if (e != cudaSuccess) {
+    delete L;
+    cudaGetLastError();
+    return fail(MOE_ERR_OOM, "workspace of %zu bytes: %s", total, cudaGetErrorString(e));
+  }
+  char* b = static_cast<char*>(L->ws);
+  L->xn = reinterpret_cast<__nv_bfloat16*>(b + offs[0]);
+  L->idx = reinterpret_cast<int32_t*>(b + offs[1]);
+  L->prob = reinterpret_cast<float*>(b + offs[2]);
+  L->sched = reinterpret_cast<int32_t*>(b + offs[3]);
+  L->row_of_slot = reinterpret_cast<int32_t*>(b + offs[4]);
+  L->token_of_row = reinterpret_cast<int32_t*>(b + offs[5]);
+  L->prob_of_row = reinterpret_cast<float*>(b + offs[6]);
+  L->xn_perm = reinterpret_cast<__nv_bfloat16*>(b + offs[7]);
+  L->act = reinterpret_cast<__nv_bfloat16*>(b + offs[8]);
+  L->y_rows = reinterpret_cast<float*>(b + offs[9]);
+  L->err = reinterpret_cast<uint32_t*>(b + offs[10]);
+  moe_status_t s = MOE_OK;
+  if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmBM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmBM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmBN / 2);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmBN / 2);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1, w->w1, F, kNumExperts * d, kGemmBN);
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kGemmSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (up GEMM) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kGemmSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (down GEMM) failed");
+  if (s == MOE_OK) {
+    L->ring.resize(kProfRing);
+    L->pending.assign(kProfRing, false);
+    for (auto& r : L->ring)
+      for (auto& ev : r)
+        if (s == MOE_OK && cudaEventCreate(&ev) != cudaSuccess) s = fail(MOE_ERR_CUDA, "cudaEventCreate failed");
+  }
+  if (s != MOE_OK) {
+    std::string msg = g_last_error;
+    moe_layer_destroy(L);
+    g_last_error = msg;
+    return s;
+  }
+  *out = L;
+  return ok();
+}
+
+moe_status_t moe_layer_destroy(moe_layer_t* L) {
+  if (!L) return ok();
+  DeviceGuard g(L->device);
+  cudaDeviceSynchronize();
+  for (auto& r : L->ring)
+    for (auto& ev : r)
+      if (ev) cudaEventDestroy(ev);
+  if (L->ws) cudaFree(L->ws);
+  if (L->host_stage) cudaFree(L->host_stage);
+  delete L;
+  return ok();
+}
+
+moe_status_t moe_layer_forward(moe_layer_t* L, const void* hidden, void* out, int32_t T, void* stream,
+                               int32_t* topk_idx, float* topk_prob, int32_t* expert_counts) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  if (T < 0 || T > L->cfg.max_tokens) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, L->cfg.max_tokens);
+  if (T == 0) return ok();
+  if (!hidden || !out || !aligned16(hidden) || !aligned16(out))
+    return fail(MOE_ERR_INVALID_ARG, "hidden/out null or not 16-byte aligned");
+  if ((topk_idx && !aligned4(topk_idx)) || (topk_prob && !aligned4(topk_prob)) ||
+      (expert_counts && !aligned4(expert_counts)))
+    return fail(MOE_ERR_INVALID_ARG, "optional output pointer misaligned");
+  DeviceGuard g(L->device);
+  if (!g.ok) return fail(MOE_ERR_CUDA, "cannot select device %d", L->device);
+  return enqueue_forward(L, hidden, out, T, static_cast<cudaStream_t>(stream), topk_idx, topk_prob, expert_counts);
+}
+
+moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  DeviceGuard g(L->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA_TRY(cudaStreamSynchronize(st));
+  uint32_t h = 0;
+  MOE_CUDA_TRY(cudaMemcpyAsync(&h, L->err, sizeof(h), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA_TRY(cudaStreamSynchronize(st));
+  if (h) {
+    MOE_CUDA_TRY(cudaMemsetAsync(L->err, 0, sizeof(uint32_t), st));
+    MOE_CUDA_TRY(cudaStreamSynchronize(st));
+    if (h & kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device wait ran out of time (error word 0x%x)", h);
+    return fail(MOE_ERR_DEVICE_CHECK, "a device index check failed (error word 0x%x)", h);
+  }
+  return ok();
+}
+
+moe_status_t moe_layer_forward_host(moe_layer_t* L, const void* hidden_host, void* out_host, int32_t T,
+                                    void* stream, int32_t* topk_idx_host, float* topk_prob_host,
+                                    int32_t* expert_counts_host) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  if (T < 0 || T > L->cfg.max_tokens) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, L->cfg.max_tokens);
+  if (T == 0) return ok();
+  if (!hidden_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "null host buffer");
+  DeviceGuard g(L->device);
+  if (!g.ok) return fail(MOE_ERR_CUDA, "cannot select device %d", L->device);
+  const size_t d = (size_t)L->cfg.d_model, maxT = (size_t)L->cfg.max_tokens;
+  const size_t x_bytes = align_up(maxT * d * 2, 1024), ip_bytes = align_up(maxT * 2 * 4, 1024);
+  const size_t need = x_bytes + 2 * ip_bytes + 1024;
+  if (!L->host_stage) {
+    MOE_CUDA_TRY(cudaMalloc(&L->host_stage, need));
+    L->host_stage_bytes = need;
+  }
+  char* b = static_cast<char*>(L->host_stage);
+  void* xs = b;
+  int32_t* is = reinterpret_cast<int32_t*>(b + x_bytes);
+  float* ps = reinterpret_cast<float*>(b + x_bytes + ip_bytes);
+  int32_t* cs = reinterpret_cast<int32_t*>(b + x_bytes + 2 * ip_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t nb = (size_t)T * d * 2;
+  MOE_CUDA_TRY(cudaMemcpyAsync(xs, hidden_host, nb, cudaMemcpyHostToDevice, st));
+  moe_status_t s = enqueue_forward(L, xs, xs, T, st, topk_idx_host ? is : nullptr, topk_prob_host ? ps : nullptr,
+                                   expert_counts_host ? cs : nullptr);
+  if (s != MOE_OK) return s;
+  MOE_CUDA_TRY(cudaMemcpyAsync(out_host, xs, nb, cudaMemcpyDeviceToHost, st));
+  if (topk_idx_host)
+    MOE_CUDA_TRY(cudaMemcpyAsync(topk_idx_host, is, (size_t)T * 8, cudaMemcpyDeviceToHost, st));
+  if (topk_prob_host)
+    MOE_CUDA_TRY(cudaMemcpyAsync(topk_prob_host, ps, (size_t)T * 8, cudaMemcpyDeviceToHost, st));
+  if (expert_counts_host)
+    MOE_CUDA_TRY(cudaMemcpyAsync(expert_counts_host, cs, kNumExperts * 4, cudaMemcpyDeviceToHost, st));
+  return moe_layer_sync_status(L, stream);
+}
+
+moe_status_t moe_layer_set_profiling(moe_layer_t* L, int32_t enable) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  L->profiling = enable != 0;
+  return ok();
+}
+
+moe_status_t moe_layer_profile_read(moe_layer_t* L, double* ms_total, int64_t* launches, int32_t reset) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  DeviceGuard g(L->device);
+  for (int s = 0; s < kProfRing; ++s) harvest(L, s);
+  for (int k = 0; k < MOE_K_COUNT; ++k) {
+    if (ms_total) ms_total[k] = L->prof_ms[k];
+    if (launches) launches[k] = L->prof_n[k];
+  }
+  if (reset)
+    for (int k = 0; k < MOE_K_COUNT; ++k) {
+      L->prof_ms[k] = 0.0;
+      L->prof_n[k] = 0;
+    }
+  return ok();
+}
+
+int64_t moe_layer_launch_count(const moe_layer_t* L) { return L ? L->launches.load() : 0; }
+
+moe_status_t moe_layer_workspace(const moe_layer_t* L, moe_workspace_view_t* v) {
+  if (!L || !v) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  v->xn = L->xn;
+  v->counts = L->sched;
+  v->row_offset = L->sched + kNumExperts;
+  v->row_of_slot = L->row_of_slot;
+  v->xn_perm = L->xn_perm;
+  v->act = L->act;
+  v->y_rows = L->y_rows;
+  v->rows_cap = L->rows_cap;
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+"""C-ABI library: loads, exports what include/moe_layer.h declares, validates
+arguments on the host (no GPU needed: these paths return before any CUDA call)."""
+import ctypes
+import os
+
+import pytest
+
+import mixture_experts_transformer_gemv_b300 as moe
+from mixture_experts_transformer_gemv_b300 import build as moe_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.lib()
+
+
+def test_header_declares_the_boundary():
+    names = moe.declared_functions()
+    for n in ("moe_layer_create", "moe_layer_forward", "moe_layer_destroy", "moe_layer_forward_host",
+              "moe_layer_sync_status", "moe_status_string", "moe_last_error_message"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = moe.declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe_layer.h but not exported"
+
+
+def test_library_is_built_for_sm_103a():
+    src = open(moe_build.__file__).read()
+    assert "arch=compute_103a,code=sm_103a" in src
+    assert os.path.exists(moe.LIB_PATH)
+
+
+def test_status_strings(lib):
+    assert lib.moe_status_string(0) == b"MOE_OK"
+    assert lib.moe_status_string(1) == b"MOE_ERR_INVALID_ARG"
+    assert lib.moe_status_string(6) == b"MOE_ERR_TIMEOUT"
+    assert lib.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
+
+
+def _cfg(**kw):
+    c = dict(d_model=256, d_ffn=512, num_experts=8, top_k=2, max_tokens=64, eps=1e-5, weight_dtype=0, flags=0)
+    c.update(kw)
+    return moe.Config(**c)
+
+
+def _fake_weights(align=0):
+    w = moe.Weights()
+    for i, (name, _) in enumerate(moe.Weights._fields_):
+        if name in ("gate_bias", "w_scale", "wv_scale", "w1_scale"):
+            continue
+        setattr(w, name, 0x10000 * (i + 1) + align)
+    return w
+
+
+def _create(lib, cfg, w):
+    h = ctypes.c_void_p()
+    s = lib.moe_layer_create(ctypes.byref(cfg) if cfg is not None else None,
+                             ctypes.byref(w) if w is not None else None, ctypes.byref(h))
+    return s, h
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_experts=4), moe.MOE_ERR_UNSUPPORTED),
+    (dict(top_k=1), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d_model=200), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d_ffn=100), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d_model=0), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d_model=32768), moe.MOE_ERR_UNSUPPORTED),
+    (dict(max_tokens=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(eps=0.0), moe.MOE_ERR_INVALID_ARG),
+    (dict(weight_dtype=7), moe.MOE_ERR_INVALID_ARG),
+])
+def test_create_rejects_bad_config(lib, kw, status):
+    s, h = _create(lib, _cfg(**kw), _fake_weights())
+    assert s == status, lib.moe_last_error_message()
+    assert not h.value
+    assert lib.moe_last_error_message() != b""
+
+
+def test_create_rejects_null_and_misaligned_pointers(lib):
+    assert _create(lib, None, _fake_weights())[0] == moe.MOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(), None)[0] == moe.MOE_ERR_INVALID_ARG
+    w = _fake_weights()
+    w.w1 = None
+    assert _create(lib, _cfg(), w)[0] == moe.MOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(), _fake_weights(align=8))[0] == moe.MOE_ERR_INVALID_ARG
+
+
+def test_null_handle_calls(lib):
+    assert lib.moe_layer_forward(None, None, None, 1, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_host(None, None, None, 1, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_sync_status(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_destroy(None) == moe.MOE_OK
+    assert lib.moe_layer_launch_count(None) == 0
+    assert lib.moe_layer_set_profiling(None, 1) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(moe, "_lib_handle", None)
+    with pytest.raises(ImportError):
+        moe.lib()
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.dirname(moe.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text and "moe_oracle" not in text

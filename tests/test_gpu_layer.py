@@ -1,0 +1,209 @@
+"""GPU parity of the whole layer against the CPU oracle, through the C ABI, at
+sizes the oracle runs in seconds: several tiles along every dimension, ragged
+row blocks, ragged d, the degenerate routers and the argument edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import mixture_experts_transformer_gemv_b300 as moe
+
+from layer_helpers import (assert_routing, assert_values, bf16_tensor, device_weights, make_layer, run,
+                           value_report)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mixture_experts_transformer_gemv_b300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _full_check(inp, flags=0, max_tokens=None):
+    layer = make_layer(inp, max_tokens=max_tokens, flags=flags)
+    y, idx, prob, counts = run(layer, inp)
+    ref = oracle.moe_tokens(inp)
+    assert_routing(idx, prob, counts, ref, inp.name)
+    rep = assert_values(y, ref.y, inp.name)
+    layer.close()
+    return rep
+
+
+def test_tiny_workload_all_tokens():
+    _full_check(synth.workload("tiny"))
+
+
+@pytest.mark.parametrize("T,d,F,seed", [
+    (300, 512, 1024, 31),    # 8 up-tiles x 2 down-tiles, one ragged row block per expert
+    (1000, 256, 640, 32),    # two row blocks per expert, F/128 = 5
+    (200, 384, 512, 33),     # d = 384: the last down-projection tile is half outside d
+    (7, 256, 512, 34),       # fewer slots than a tile in every expert
+])
+def test_mid_shapes(T, d, F, seed):
+    _full_check(synth.make_inputs(T, d, F, seed, name=f"mid{T}x{d}x{F}"))
+
+
+def test_skewed_bias_small():
+    inp = synth.make_inputs(256, 256, 512, 35, bias=synth.SKEW_BIAS, name="skew_small")
+    _full_check(inp)
+
+
+def test_single_token_and_empty():
+    inp = synth.make_inputs(1, 256, 512, 36, name="one")
+    _full_check(inp, max_tokens=16)
+    layer = make_layer(inp, max_tokens=16)
+    x = bf16_tensor(inp.x)
+    before = layer.launch_count()
+    layer.forward(x[:0])
+    assert layer.launch_count() == before  # T = 0 enqueues nothing
+    layer.close()
+
+
+def test_one_hot_router_single_expert():
+    """All tokens to expert 5 with weight 1; the second pick has weight 0."""
+    inp = synth.make_inputs(200, 256, 512, 37, name="onehot")
+    b = np.zeros(8, np.float32)
+    b[5] = 1e4
+    inp.bias = b
+    layer = make_layer(inp)
+    y, idx, prob, counts = run(layer, inp)
+    assert np.all(idx[:, 0] == 5) and np.all(idx[:, 1] == 0)
+    assert np.all(prob[:, 0] == 1.0) and np.all(prob[:, 1] == 0.0)
+    assert counts[5] == 200 and counts[0] == 200
+    ref = oracle.moe_tokens(inp)
+    assert_values(y, ref.y, "one-hot")
+
+
+def test_uniform_router_picks_first_two():
+    inp = synth.make_inputs(64, 256, 512, 38, name="uniform")
+    inp.gate[:] = 0.0
+    layer = make_layer(inp)
+    y, idx, prob, counts = run(layer, inp)
+    assert np.all(idx == np.array([0, 1]))
+    assert np.all(prob == 0.125)
+    assert list(counts) == [64, 64, 0, 0, 0, 0, 0, 0]
+    assert_values(y, oracle.moe_tokens(inp).y, "uniform")
+
+
+def test_in_place_and_host_entry_point():
+    inp = synth.make_inputs(96, 256, 512, 39, name="inplace")
+    layer = make_layer(inp)
+    y_ref = oracle.moe_tokens(inp).y
+    x = bf16_tensor(inp.x)
+    out = layer.forward(x.clone())
+    xi = x.clone()
+    layer.forward(xi, out=xi)
+    torch.cuda.synchronize()
+    layer.sync_status()
+    assert torch.equal(out, xi)
+    assert_values(xi.float().cpu().numpy().astype(np.float64), y_ref, "in place")
+    xh = bf16_tensor(inp.x, device=None).pin_memory()
+    oh, idx, prob, counts = layer.forward_host(xh, routing=True)
+    assert torch.equal(oh, out.cpu())
+    assert counts.sum().item() == 2 * inp.T
+
+
+def test_token_permutation():
+    inp = synth.make_inputs(400, 256, 512, 40, name="perm")
+    layer = make_layer(inp)
+    y, idx, prob, counts = run(layer, inp)
+    perm = np.random.default_rng(1).permutation(inp.T)
+    x2 = bf16_tensor(np.ascontiguousarray(inp.x[perm]))
+    y2, idx2, prob2, counts2 = run(layer, inp, x_dev=x2)
+    np.testing.assert_array_equal(idx2, idx[perm])
+    np.testing.assert_array_equal(prob2, prob[perm])
+    np.testing.assert_array_equal(counts2, counts)
+    r = value_report(y2, y[perm])
+    assert r["violations"] == 0, r
+
+
+def test_token_limits():
+    inp = synth.make_inputs(32, 256, 512, 41, name="limits")
+    layer = make_layer(inp, max_tokens=32)
+    x = bf16_tensor(inp.x)
+    layer.forward(x)  # T == max_tokens
+    big = torch.zeros((33, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        layer.forward(big)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    layer.sync_status()
+
+
+def test_device_checks_flag_clean_run():
+    inp = synth.make_inputs(128, 256, 512, 42, name="checks")
+    _full_check(inp, flags=moe.MOE_FLAG_DEVICE_CHECKS)
+
+
+def test_intermediates_match_oracle():
+    """Normed rows, expert grouping, GeGLU activations and scaled expert outputs."""
+    inp = synth.workload("tiny")
+    layer = make_layer(inp)
+    run(layer, inp)
+    ws = layer.workspace()
+    R = ws.rows_cap
+    T, d, F = inp.T, inp.d, inp.F
+    xn = _read(ws.xn, (inp.T, d), torch.bfloat16)
+    counts = _read(ws.counts, (8,), torch.int32)
+    off = _read(ws.row_offset, (9,), torch.int32)
+    ros = _read(ws.row_of_slot, (T, 2), torch.int32)
+    act = _read(ws.act, (R, F), torch.bfloat16)
+    yr = _read(ws.y_rows, (R, d), torch.float32)
+    r = oracle.route(inp, keep_xn=True)
+    np.testing.assert_allclose(xn, r.xn, rtol=2 ** -8, atol=1e-6)
+    np.testing.assert_array_equal(counts, np.bincount(r.idx.ravel(), minlength=8))
+    assert np.all(off % 128 == 0) and np.all(np.diff(off) >= counts)
+    for t in (0, 17, T - 1):
+        for rank in range(2):
+            e = int(r.idx[t, rank])
+            row = int(ros[t, rank])
+            assert off[e] <= row < off[e] + counts[e]
+            h, v, a, o = oracle.expert_ffn(inp, r.xn[t], e)
+            ga = act[row]
+            assert np.max(np.abs(ga - a)) <= 0.02 * np.max(np.abs(a)) + 1e-6, (t, rank)
+            go = yr[row]
+            wo = r.w[t, rank] * o
+            assert np.max(np.abs(go - wo)) <= 0.02 * np.max(np.abs(wo)) + 1e-7, (t, rank)
+    # rows of each expert are in token order (stable grouping)
+    for e in range(8):
+        toks = sorted(t for t in range(T) for k in range(2) if r.idx[t, k] == e)
+        rows = [int(ros[t, k]) for t in toks for k in range(2) if r.idx[t, k] == e]
+        assert rows == list(range(off[e], off[e] + counts[e]))
+
+
+def _read(ptr, shape, dtype):
+    n = int(np.prod(shape))
+    buf = torch.empty(n, dtype=dtype, device="cuda")
+    _cudart().cudaMemcpy(ctypes_c_void_p(buf.data_ptr()), ctypes_c_void_p(ptr), n * buf.element_size(), 3)
+    torch.cuda.synchronize()
+    return buf.view(*shape).float().cpu().numpy().astype(np.float64) if dtype != torch.int32 else \
+        buf.view(*shape).cpu().numpy()
+
+
+_CUDART = None
+
+
+def _cudart():
+    """libcudart of the CUDA toolkit, for device-to-device copies of raw
+    workspace pointers into torch tensors (test introspection only)."""
+    global _CUDART
+    if _CUDART is None:
+        import ctypes
+        import glob
+        for cand in ("libcudart.so", *glob.glob("/usr/local/cuda/lib64/libcudart.so*")):
+            try:
+                _CUDART = ctypes.CDLL(cand)
+                break
+            except OSError:
+                continue
+        _CUDART.cudaMemcpy.restype = ctypes.c_int
+        _CUDART.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+    return _CUDART
+
+
+def ctypes_c_void_p(v):
+    import ctypes
+    return ctypes.c_void_p(v)
