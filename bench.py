@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the Grok-1 MoE feed-forward layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: the Grok-1-shape prefill layer, T = 8192 tokens, d = 6144, F = 32768,
+8 experts, top-2, bf16 activations and weights (seeded synthetic inputs,
+seed 1002; expert weights 9.66 GB, larger than L2, so no flush is needed).
+A step is one moe_layer_forward over the whole batch: router, grouping, both
+expert GEMMs, combine, post-norm and residual.
+
+One JSON line on rank 0 (the keys are described in the design doc).  With N > 1
+(torchrun) every rank runs its own replica of the workload on its own GPU: the
+layer is token-parallel with no exchange, so scaling is weak and value = N * T
+/ max-over-ranks step time.
+
+--impl reference times the CPU oracle (fp64, OpenMP) on the host cores, one
+bounded token sample per step, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Grok-1 MoE layer tokens/s (T=8192, bf16); % of bf16 TC / HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "prefill"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SOURCES = {
+    "router": ["k_router.cuh"],
+    "permute": ["k_permute.cuh"],
+    "gather": ["k_permute.cuh"],
+    "up_geglu": ["k_gemm.cuh", "ptx.cuh"],
+    "down": ["k_gemm.cuh", "ptx.cuh"],
+    "combine": ["k_combine.cuh"],
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# extra workloads: the other Grok-1-shape configurations, and a reduced-F case
+# (same d, 2.4 GB of weights, still larger than L2) sized for ncu captures
+PROFILE_SMALL = dict(T=2048, d=6144, F=4096, seed=2000)
+
+
+def make_workload(name):
+    import synth
+    if name == "profile_small":
+        c = PROFILE_SMALL
+        return synth.make_inputs(c["T"], c["d"], c["F"], c["seed"], name=name)
+    return synth.workload(name)
+
+
+def config_block(inp):
+    return {
+        "workload": f"grok1_moe_layer_{inp.name} T={inp.T} d={inp.d} F={inp.F} E=8 top-2 {inp.weight_dtype} "
+                    f"(seed {inp.seed})",
+        "T": inp.T, "d_model": inp.d, "d_ffn": inp.F, "experts": 8, "top_k": 2,
+        "global_batch_tokens": inp.T, "parallelism": "token replicas, no exchange",
+        "l2": f"inputs larger than L2: {inp.w.nbytes * 3 / 1e9:.2f} GB of expert weights read every step (no flush)",
+    }
+
+
+def algorithmic_work(inp, counts):
+    """Per-launch algorithmic work of each kernel (padding rows not counted).
+    S = 2T routed slots; flops of the GEMMs, bytes of the memory-bound kernels."""
+    T, d, F = inp.T, inp.d, inp.F
+    S = 2 * T
+    return {
+        "router": ("hbm", T * d * 2 * 2 + 8 * d * 4 + T * 16),
+        "permute": ("hbm", S * 4 * 2 + S * 4 * 3),
+        "gather": ("hbm", S * d * 2 * 2),
+        "up_geglu": ("tensor", 2.0 * 2 * d * F * S),
+        "down": ("tensor", 2.0 * d * F * S),
+        "combine": ("hbm", S * d * 4 + T * d * 2 * 2),
+    }
+
+
+def source_hash(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "mixture_experts_transformer_gemv_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 300] or sm
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import synth
+    import mixture_experts_transformer_gemv_b300 as moe
+    from mixture_experts_transformer_gemv_b300 import build as moe_build
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    moe_build.build()
+
+    t0 = time.time()
+    inp = make_workload(args.workload)
+    log(f"[rank {rank}] inputs generated in {time.time() - t0:.1f} s")
+    x_host = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16)
+    weights = {
+        "gate": torch.from_numpy(inp.gate).cuda(),
+        "gate_bias": None if inp.bias is None else torch.from_numpy(inp.bias).cuda(),
+        "pre_norm_scale": torch.from_numpy(inp.s_pre).cuda(), "post_norm_scale": torch.from_numpy(inp.s_post).cuda(),
+    }
+    for k in ("w", "wv", "w1"):
+        a = getattr(inp, k)
+        weights[k] = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if inp.weight_dtype == "bf16"
+                      else torch.from_numpy(a)).cuda()
+    if inp.weight_dtype == "int8":
+        for k in ("w_scale", "wv_scale", "w1_scale"):
+            weights[k] = torch.from_numpy(getattr(inp, k).view(np.int16)).view(torch.bfloat16).cuda()
+    x = x_host.cuda()
+    out = torch.empty_like(x)
+    layer = moe.MoeLayer(inp.d, inp.F, inp.T, weights, eps=inp.eps, weight_dtype=inp.weight_dtype)
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    layer.sync_status()
+    _, _, _, counts = layer.forward(x, out, routing=True)
+    counts = counts.cpu().numpy()
+    torch.cuda.synchronize()
+
+    # timed region: K forwards, per-kernel events recorded on the same stream
+    layer.set_profiling(True)
+    layer.profile_read(reset=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    launches0 = layer.launch_count()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        layer.forward(x, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = layer.launch_count() - launches0
+    ms_total = ev0.elapsed_time(ev1)
+    layer.sync_status()
+    prof = layer.profile_read(reset=True)
+    layer.set_profiling(False)
+
+    ms_step = ms_total / args.steps
+    if dist:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * inp.T / (ms_step / 1e3)
+
+    # end to end through the host-buffer entry point (pinned memory, copies inside)
+    xh = x_host.pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    for _ in range(2):
+        layer.forward_host(xh, oh)
+    e2e_steps = max(3, min(args.steps, 20))
+    if dist:
+        dist.barrier()
+    t1 = time.perf_counter()
+    for _ in range(e2e_steps):
+        layer.forward_host(xh, oh)
+    e2e_s = (time.perf_counter() - t1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * inp.T / e2e_s
+
+    # kernels: average device time per launch, dominant kernel's roofline
+    pk, peak_kind = peaks()
+    work = algorithmic_work(inp, counts)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        kernels[name] = {"ms_per_launch": ms / max(n, 1), "launches": n}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
+    bound, amount = work[dom]
+    dur_s = kernels[dom]["ms_per_launch"] / 1e3
+    if bound == "tensor":
+        achieved = amount / dur_s / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
+                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4)}
+    else:
+        achieved = amount / dur_s / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})"}
+    roof["kernel"] = dom
+    roof["algorithmic_per_launch"] = amount
+    roof["traffic"] = recorded_traffic(dom)
+    for name in kernels:
+        b, a = work[name]
+        d_s = kernels[name]["ms_per_launch"] / 1e3
+        kernels[name]["achieved"] = round(a / d_s / (1e12 if b == "tensor" else 1e9), 1) if d_s > 0 else None
+        kernels[name]["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
+        kernels[name]["ms_per_launch"] = round(kernels[name]["ms_per_launch"], 4)
+    layer_flops = 6.0 * inp.d * inp.F * 2 * inp.T
+    layer_tc_frac = layer_flops / (ms_step / 1e3) / 1e12 / pk["bf16_tflops_sustained"]
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)",
+        "config": config_block(inp),
+        "roofline": roof,
+        "layer_tc_frac": round(layer_tc_frac, 4),
+        "kernels": kernels,
+        "expert_counts": [int(c) for c in counts],
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(inp.T * inp.d * 2),
+                "d2h_bytes_per_step": int(inp.T * inp.d * 2), "ms_per_step": round(e2e_s * 1e3, 3),
+                "entry_point": "moe_layer_forward_host (pinned host buffers)"},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    layer.close()
+    del weights
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+# --------------------------------------------------------------- oracle arm
+def oracle_token_sample(inp, n, seed=7):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(inp.T, size=n, replace=False))
+
+
+def cpu_baseline(inp, budget_s=20.0):
+    """The oracle as it stands on this host: routing of all T tokens plus the
+    full layer on a seeded token sample sized to ~budget_s; tokens/s =
+    1 / (layer seconds per sampled token + routing seconds per token)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.route(inp)
+    t_route = (time.perf_counter() - t0) / inp.T
+    t0 = time.perf_counter()
+    oracle.moe_tokens(inp, oracle_token_sample(inp, 1, seed=1))
+    t_one = time.perf_counter() - t0
+    n = int(max(1, min(64, budget_s / max(t_one, 1e-3))))
+    toks = oracle_token_sample(inp, n)
+    t0 = time.perf_counter()
+    oracle.moe_tokens(inp, toks)
+    t_tok = (time.perf_counter() - t0) / n
+    per_token = t_tok + t_route
+    return {"value": round(1.0 / per_token, 4), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"routing of all {inp.T} tokens ({t_route * inp.T:.2f} s) + full layer on {n} seeded tokens "
+                      f"({t_tok * n:.1f} s); fp64 C oracle, OpenMP over rows",
+            "seconds_per_token": round(per_token, 4)}
+
+
+def run_reference(args):
+    import oracle
+    import synth
+    inp = make_workload(args.workload)
+    cores = oracle.max_threads()
+    rng_base = 100
+    # each step: routing of a 512-token slice + the full layer on one sampled token
+    def step(i):
+        lo = (i * 512) % inp.T
+        sub = synth.MoeInputs(**{**inp.__dict__, "T": 512, "x": np.ascontiguousarray(inp.x[lo:lo + 512])})
+        t0 = time.perf_counter()
+        oracle.route(sub)
+        tr = (time.perf_counter() - t0) / 512
+        t0 = time.perf_counter()
+        oracle.moe_tokens(inp, oracle_token_sample(inp, 1, seed=rng_base + i))
+        tl = time.perf_counter() - t0
+        return tl + tr
+    for i in range(args.warmup):
+        step(i)
+    per_tok = [step(args.warmup + i) for i in range(args.steps)]
+    mean_tok = float(np.mean(per_tok))
+    value = 1.0 / mean_tok
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_tok * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)", "config": config_block(inp),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "per step: routing of a 512-token slice + full layer on one seeded token; "
+                                   "fp64 C oracle on the host cores"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["prefill", "decode", "skew", "int8", "tiny", "profile_small"],
+                    help="prefill (T=8192) is the headline workload")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = run_reference(args)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -52,6 +52,8 @@ def _load():
         # oracle (mutation checks of the pins); nothing else sets this.
         lib = ctypes.CDLL(os.environ.get("MOE_ORACLE_LIB_OVERRIDE") or build())
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_max_threads.restype = i32
+        lib.oracle_max_threads.argtypes = []
         lib.oracle_gelu_tanh.restype = dbl
         lib.oracle_gelu_tanh.argtypes = [dbl]
         lib.oracle_rmsnorm.restype = None
@@ -75,6 +77,11 @@ def _p(a: Optional[np.ndarray]):
         return None
     assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
     return a.ctypes.data
+
+
+def max_threads() -> int:
+    """Threads the oracle's OpenMP loops run on."""
+    return int(_load().oracle_max_threads())
 
 
 def gelu_tanh(u: float) -> float:

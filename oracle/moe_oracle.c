@@ -52,6 +52,10 @@
 #include <stdlib.h>
 #include <string.h>
 
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
 #define ORACLE_W_BF16 0
 #define ORACLE_W_INT8 1
 
@@ -60,6 +64,15 @@ static inline float bf16_bits_to_float(uint16_t b) {
   float f;
   memcpy(&f, &u, 4);
   return f;
+}
+
+/* Threads the OpenMP loops of this file use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }
 
 /* One expert-stacked weight tensor, stored [E, N, K] (PyTorch [out, in]). */
