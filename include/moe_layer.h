@@ -189,6 +189,33 @@ typedef struct {
 
 moe_status_t moe_layer_workspace(const moe_layer_t* layer, moe_workspace_view_t* view);
 
+/* ------------------------------------------------ allocation-free grouping */
+
+/*
+ * Groups T tokens' routed slots by expert exactly as moe_layer_forward does
+ * internally, without allocating any memory.  The pages have no counterpart:
+ * this is for callers that cannot call cudaMalloc, such as a serving runtime
+ * that reserved all free device memory for its own pool at start-up or a plugin
+ * host that gives an op only its input and output buffers (there cudaMalloc
+ * fails or stalls the device mid-step).
+ *   topk_idx      DEVICE [T, 2] int32, experts in [0, 8) (e.g. moe_layer_forward's
+ *                 topk_idx); an out-of-range index is counted as expert 0
+ *   topk_prob     DEVICE [T, 2] fp32, their probabilities
+ *   T             0 <= T <= 16384 (larger T: MOE_ERR_INVALID_ARG); T == 0 is a no-op
+ *   expert_counts DEVICE [8] int32, written: slots per expert
+ *   row_of_slot   DEVICE [T, 2] int32, written: row of slot (t, r) when each
+ *                 expert's slots are laid out contiguously in token order and
+ *                 each expert's block is padded to a multiple of 128 rows
+ *   stream        cudaStream_t (as void*), asynchronous
+ * Scratch lives in one static device array of about 264 KB that every GPU
+ * loading this library holds until the process exits.  All calls share it, so
+ * calls that overlap on the GPU (other streams, other threads) race: order them.
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up); make that first call before any CUDA stream capture.
+ */
+moe_status_t moe_group_slots_noalloc(const int32_t* topk_idx, const float* topk_prob, int32_t T,
+                                     int32_t* expert_counts, int32_t* row_of_slot, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -82,6 +82,8 @@ def lib():
         L.moe_layer_launch_count.argtypes = [vp]
         L.moe_layer_workspace.restype = i32
         L.moe_layer_workspace.argtypes = [vp, ctypes.POINTER(WorkspaceView)]
+        L.moe_group_slots_noalloc.restype = i32
+        L.moe_group_slots_noalloc.argtypes = [vp, vp, i32, vp, vp, vp]
         _lib_handle = L
     return _lib_handle
 
@@ -113,6 +115,22 @@ def _stream_handle(stream) -> Optional[int]:
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream
+
+
+def group_slots_noalloc(topk_idx, topk_prob, expert_counts, row_of_slot, stream=None):
+    """moe_group_slots_noalloc: per-expert counts and the slot -> row map of the
+    layer's grouping step, with no memory allocated (scratch is a static device
+    array; T <= 16384; calls must not overlap on the GPU).  All tensors CUDA,
+    int32 / fp32, contiguous: topk_idx, topk_prob [T, 2] in; expert_counts [8],
+    row_of_slot [T, 2] out."""
+    import torch
+    T = topk_idx.shape[0]
+    for t, dt in ((topk_idx, torch.int32), (topk_prob, torch.float32), (expert_counts, torch.int32),
+                  (row_of_slot, torch.int32)):
+        if not (t.is_cuda and t.dtype == dt and t.is_contiguous()):
+            raise ValueError("group_slots_noalloc: tensors must be contiguous CUDA int32 / fp32")
+    _check(lib().moe_group_slots_noalloc(topk_idx.data_ptr(), topk_prob.data_ptr(), T, expert_counts.data_ptr(),
+                                         row_of_slot.data_ptr(), _stream_handle(stream)), "moe_group_slots_noalloc")
 
 
 class MoeLayer:

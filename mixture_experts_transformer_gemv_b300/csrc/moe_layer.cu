@@ -18,6 +18,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -474,3 +475,69 @@ moe_status_t moe_layer_workspace(const moe_layer_t* L, moe_workspace_view_t* v) 
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Allocation-free grouping of routed slots (moe_group_slots_noalloc).
+//
+// Some callers cannot call cudaMalloc: a serving runtime that reserved all free
+// device memory for its own pool at start-up, or a plugin host that hands an op
+// only its input and output buffers.  There cudaMalloc either fails or stalls the
+// device in the middle of a latency-critical step.  This entry point runs the
+// grouping kernel with its scratch (schedule block, row -> token map, row
+// weights) in the file-scope array below instead of a handle's workspace.
+//
+// The array is modest (see kNoAllocScratchBytes) and every GPU that loads this
+// library holds it until the process exits.  Host code cannot use the array's
+// name as a device address: the first call on each device asks the runtime for
+// the address (cudaGetSymbolAddress, with that device current) and caches it.
+namespace {
+constexpr int kNoAllocMaxTokens = 16384;
+constexpr int kNoAllocRows = 2 * kNoAllocMaxTokens + kNumExperts * kRowTile;
+constexpr size_t kNoAllocSchedBytes = 256;  // kSchedInts int32, padded
+constexpr size_t kNoAllocScratchBytes = kNoAllocSchedBytes + 2 * (size_t)kNoAllocRows * 4 + 256;
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+extern "C" moe_status_t moe_group_slots_noalloc(const int32_t* topk_idx, const float* topk_prob, int32_t T,
+                                                int32_t* expert_counts, int32_t* row_of_slot, void* stream) {
+  if (T < 0 || T > kNoAllocMaxTokens)
+    return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, %d], the limit of the static scratch array", T,
+                kNoAllocMaxTokens);
+  if (T == 0) return ok();
+  if (!topk_idx || !topk_prob || !expert_counts || !row_of_slot)
+    return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned4(topk_idx) || !aligned4(topk_prob) || !aligned4(expert_counts) || !aligned4(row_of_slot))
+    return fail(MOE_ERR_INVALID_ARG, "pointer argument not 4-byte aligned");
+  int dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || !p)
+        return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
+      g_noalloc_addr[dev] = p;
+    }
+    base = g_noalloc_addr[dev];
+  }
+  char* b = static_cast<char*>(base);
+  int32_t* sched = reinterpret_cast<int32_t*>(b);
+  int32_t* token_of_row = reinterpret_cast<int32_t*>(b + kNoAllocSchedBytes);
+  float* prob_of_row = reinterpret_cast<float*>(b + kNoAllocSchedBytes + (size_t)kNoAllocRows * 4);
+  uint32_t* err = reinterpret_cast<uint32_t*>(b + kNoAllocSchedBytes + 2 * (size_t)kNoAllocRows * 4);
+  // Index checks on: the indices come from the caller, and an out-of-range one
+  // is counted as expert 0 instead of indexing past the arrays.  The kernel
+  // writes every scratch word it later reads, so nothing needs clearing.
+  permute_kernel<<<1, kPermuteThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      topk_idx, topk_prob, T, sched, row_of_slot, token_of_row, prob_of_row, expert_counts, kNoAllocRows, 1, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}

@@ -118,3 +118,38 @@ def stratified_tokens(ref_idx, T, per_expert=3, seed=0, extra=(0,)):
         if cand.size:
             pick.update(int(t) for t in rng.choice(cand, size=min(per_expert, cand.size), replace=False))
     return np.array(sorted(pick), dtype=np.int64)
+
+
+_CUDART = None
+
+
+def _cudart():
+    """libcudart of the CUDA toolkit, for device-to-device copies of raw
+    workspace pointers into torch tensors (test introspection only)."""
+    global _CUDART
+    if _CUDART is None:
+        import ctypes
+        import glob
+        for cand in ("libcudart.so", *sorted(glob.glob("/usr/local/cuda/lib64/libcudart.so*"))):
+            try:
+                _CUDART = ctypes.CDLL(cand)
+                break
+            except OSError:
+                continue
+        _CUDART.cudaMemcpy.restype = ctypes.c_int
+        _CUDART.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+    return _CUDART
+
+
+def read_device(ptr, shape, dtype):
+    """Copy a raw device buffer (e.g. a workspace pointer) to a numpy array:
+    float64 for floating types, int32 as is."""
+    n = int(np.prod(shape))
+    buf = torch.empty(n, dtype=dtype, device="cuda")
+    torch.cuda.synchronize()
+    rc = _cudart().cudaMemcpy(buf.data_ptr(), ptr, n * buf.element_size(), 3)  # device to device
+    assert rc == 0, f"cudaMemcpy failed ({rc})"
+    torch.cuda.synchronize()
+    if dtype == torch.int32:
+        return buf.view(*shape).cpu().numpy()
+    return buf.view(*shape).float().cpu().numpy().astype(np.float64)

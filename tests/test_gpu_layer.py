@@ -9,8 +9,8 @@ import oracle
 import synth
 import mixture_experts_transformer_gemv_b300 as moe
 
-from layer_helpers import (assert_routing, assert_values, bf16_tensor, device_weights, make_layer, run,
-                           value_report)
+from layer_helpers import (assert_routing, assert_values, bf16_tensor, device_weights, make_layer, read_device,
+                           run, value_report)
 
 pytestmark = pytest.mark.gpu
 
@@ -146,12 +146,12 @@ def test_intermediates_match_oracle():
     ws = layer.workspace()
     R = ws.rows_cap
     T, d, F = inp.T, inp.d, inp.F
-    xn = _read(ws.xn, (inp.T, d), torch.bfloat16)
-    counts = _read(ws.counts, (8,), torch.int32)
-    off = _read(ws.row_offset, (9,), torch.int32)
-    ros = _read(ws.row_of_slot, (T, 2), torch.int32)
-    act = _read(ws.act, (R, F), torch.bfloat16)
-    yr = _read(ws.y_rows, (R, d), torch.float32)
+    xn = read_device(ws.xn, (inp.T, d), torch.bfloat16)
+    counts = read_device(ws.counts, (8,), torch.int32)
+    off = read_device(ws.row_offset, (9,), torch.int32)
+    ros = read_device(ws.row_of_slot, (T, 2), torch.int32)
+    act = read_device(ws.act, (R, F), torch.bfloat16)
+    yr = read_device(ws.y_rows, (R, d), torch.float32)
     r = oracle.route(inp, keep_xn=True)
     np.testing.assert_allclose(xn, r.xn, rtol=2 ** -8, atol=1e-6)
     np.testing.assert_array_equal(counts, np.bincount(r.idx.ravel(), minlength=8))
@@ -172,38 +172,3 @@ def test_intermediates_match_oracle():
         toks = sorted(t for t in range(T) for k in range(2) if r.idx[t, k] == e)
         rows = [int(ros[t, k]) for t in toks for k in range(2) if r.idx[t, k] == e]
         assert rows == list(range(off[e], off[e] + counts[e]))
-
-
-def _read(ptr, shape, dtype):
-    n = int(np.prod(shape))
-    buf = torch.empty(n, dtype=dtype, device="cuda")
-    _cudart().cudaMemcpy(ctypes_c_void_p(buf.data_ptr()), ctypes_c_void_p(ptr), n * buf.element_size(), 3)
-    torch.cuda.synchronize()
-    return buf.view(*shape).float().cpu().numpy().astype(np.float64) if dtype != torch.int32 else \
-        buf.view(*shape).cpu().numpy()
-
-
-_CUDART = None
-
-
-def _cudart():
-    """libcudart of the CUDA toolkit, for device-to-device copies of raw
-    workspace pointers into torch tensors (test introspection only)."""
-    global _CUDART
-    if _CUDART is None:
-        import ctypes
-        import glob
-        for cand in ("libcudart.so", *glob.glob("/usr/local/cuda/lib64/libcudart.so*")):
-            try:
-                _CUDART = ctypes.CDLL(cand)
-                break
-            except OSError:
-                continue
-        _CUDART.cudaMemcpy.restype = ctypes.c_int
-        _CUDART.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
-    return _CUDART
-
-
-def ctypes_c_void_p(v):
-    import ctypes
-    return ctypes.c_void_p(v)
