@@ -13,7 +13,8 @@
  *
  * Sources (page title, section): "Jah-yee/grok" README, architecture diagram
  * (8 experts, top-2, GELU(x W) (*) (x Wv) then the output projection, RMSNorm);
- * "Unveiling Grok-1" (oneruby-dev), "Expert Routing Details" (softmax of the
+ * "Grok-1: 314B Total Parameters, 25B Active Per Token (MoE Explained)"
+ * (oneruby-dev blog), "Expert Routing Details" (softmax of the
  * gate logits, then top_k(k=2) of the softmax outputs) and "How MoE Works in
  * Practice" (gate-weighted sum of the expert outputs); "TevunahAi/Grok-1-BF16"
  * model card, "Grok-1 Specific Behaviors" (pre-MoE and post-MoE norms),

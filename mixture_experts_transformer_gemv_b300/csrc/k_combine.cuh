@@ -1,6 +1,7 @@
 // K5: combine of the two expert rows + post-MoE RMSNorm + residual add.
 //
-// Per token t ("Unveiling Grok-1", "How MoE Works in Practice": gate-weighted
+// Per token t ("Grok-1: 314B Total Parameters, 25B Active Per Token (MoE Explained)",
+// "How MoE Works in Practice": gate-weighted
 // sum of the chosen experts' outputs; "TevunahAi/Grok-1-BF16", "Grok-1 Specific
 // Behaviors": post-MoE norm; "Why JAX Instead of PyTorch" block listing:
 // x + sublayer output):

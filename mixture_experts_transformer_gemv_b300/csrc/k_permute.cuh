@@ -1,7 +1,8 @@
 // K2: per-expert grouping of the 2T (token, rank) slots, and the row gather.
 //
 // The sources route every token to two experts and sum the experts' outputs
-// ("Unveiling Grok-1", "How MoE Works in Practice"); they do not say how the
+// ("Grok-1: 314B Total Parameters, 25B Active Per Token (MoE Explained)",
+// "How MoE Works in Practice"); they do not say how the
 // work is grouped.  Here the slots are grouped so each expert's rows are
 // contiguous and its expert FFN becomes a dense GEMM:
 //   counts[e]      = #slots with expert e

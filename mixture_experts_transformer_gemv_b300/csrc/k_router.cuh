@@ -1,8 +1,9 @@
 // K1: pre-MoE RMSNorm + router logits + softmax + top-2, fused.
 //
 // Per token t ("TevunahAi/Grok-1-BF16" model card, "Grok-1 Specific Behaviors":
-// pre-MoE norm; "Unveiling Grok-1", "Expert Routing Details": softmax of the gate
-// logits, then top_k(k=2) of the softmax outputs):
+// pre-MoE norm; "Grok-1: 314B Total Parameters, 25B Active Per Token (MoE Explained)",
+// "Expert Routing Details": softmax of the gate logits, then top_k(k=2) of the
+// softmax outputs):
 //   r      = 1 / sqrt(mean_j x_j^2 + eps)
 //   xn_j   = x_j * r * s_pre_j               (fp32; written out rounded to bf16)
 //   l_e    = sum_j xn_j G[e, j] + b_e        (from the fp32 xn, not the bf16 copy)

@@ -20,7 +20,8 @@
  *  - "Jah-yee/grok" README, architecture diagram: MoE FFN with 8 experts and
  *    top-2 routing, expert form GELU(x W) (*) (x Wv) followed by an output
  *    projection; RMSNorm; list item "Gated GELU".
- *  - "Unveiling Grok-1" (oneruby-dev), section "Expert Routing Details": the
+ *  - "Grok-1: 314B Total Parameters, 25B Active Per Token (MoE Explained)"
+ *    (oneruby-dev blog), section "Expert Routing Details": the
  *    router applies softmax to the gate logits and takes jax.lax.top_k(k=2) of
  *    the softmax outputs, returning those gates unrenormalised; the gating
  *    noise is for training only.  Section "How MoE Works in Practice": each
