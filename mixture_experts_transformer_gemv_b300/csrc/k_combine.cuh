@@ -5,7 +5,8 @@
 // sum of the chosen experts' outputs; "TevunahAi/Grok-1-BF16", "Grok-1 Specific
 // Behaviors": post-MoE norm; "Why JAX Instead of PyTorch" block listing:
 // x + sublayer output):
-//   m   = Y[row(t,0)] + Y[row(t,1)]       (Y rows already hold p * o, fp32)
+//   m   = Y[row(t,0)] + Y[row(t,1)]       (Y rows already hold p * o, fp32;
+//                                          the decode path first sums o's split-K parts)
 //   out = bf16(x + m / sqrt(mean(m^2) + eps) * s_post)
 // One CTA of 256 threads per token; m stays in registers between the two
 // passes (d <= 256 * 4 * kCombineVec), 16-byte loads and stores throughout.
@@ -17,10 +18,14 @@ namespace moe {
 constexpr int kCombineThreads = 256;
 constexpr int kCombineVec = 16;  // float4 per thread kept in registers: d <= 16384
 
+// kSplit = false: Y rows of the grouped GEMM path, Y[row] = p * o.
+// kSplit = true:  decode path, o split over `ksplit` reduction chunks:
+//                 part[kc][e][s][:], s = row - row_offset[e]; summed in kc order.
+template <bool kSplit>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
-    const float* __restrict__ y_rows, const int32_t* __restrict__ row_of_slot, const __nv_bfloat16* x,
-    const float* __restrict__ s_post, float eps, int d, int rows_valid_cap, int checks, uint32_t* __restrict__ err,
-    __nv_bfloat16* out) {
+    const float* __restrict__ y_rows, const int32_t* __restrict__ row_of_slot, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ sched, int ksplit, const __nv_bfloat16* x, const float* __restrict__ s_post,
+    float eps, int d, int rows_valid_cap, int checks, uint32_t* __restrict__ err, __nv_bfloat16* out) {
   __shared__ float red[kCombineThreads / 32];
   const int t = blockIdx.x;
   int r0 = row_of_slot[2 * t], r1 = row_of_slot[2 * t + 1];
@@ -28,8 +33,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     if (threadIdx.x == 0) atomicOr(err, kErrCheck);
     r0 = r1 = 0;
   }
-  const float4* y0 = reinterpret_cast<const float4*>(y_rows + (size_t)r0 * d);
-  const float4* y1 = reinterpret_cast<const float4*>(y_rows + (size_t)r1 * d);
+  const float4* y0;
+  const float4* y1;
+  size_t kc_stride = 0;  // in float4
+  if (kSplit) {
+    int e0 = idx[2 * t], e1 = idx[2 * t + 1];
+    int s0 = r0 - sched[kNumExperts + e0], s1 = r1 - sched[kNumExperts + e1];
+    if (checks && (e0 < 0 || e0 >= kNumExperts || e1 < 0 || e1 >= kNumExperts || s0 < 0 || s0 >= 16 || s1 < 0 ||
+                   s1 >= 16)) {
+      if (threadIdx.x == 0) atomicOr(err, kErrCheck);
+      e0 = e1 = s0 = s1 = 0;
+    }
+    y0 = reinterpret_cast<const float4*>(y_rows + ((size_t)e0 * 16 + s0) * d);
+    y1 = reinterpret_cast<const float4*>(y_rows + ((size_t)e1 * 16 + s1) * d);
+    kc_stride = (size_t)kNumExperts * 16 * d / 4;
+  } else {
+    y0 = reinterpret_cast<const float4*>(y_rows + (size_t)r0 * d);
+    y1 = reinterpret_cast<const float4*>(y_rows + (size_t)r1 * d);
+  }
   const int nv = d >> 2;
   float4 m[kCombineVec];
   float ss = 0.f;
@@ -37,7 +58,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   for (int i = 0; i < kCombineVec; ++i) {
     const int c = threadIdx.x + i * kCombineThreads;
     if (c < nv) {
-      const float4 a = y0[c], b = y1[c];
+      float4 a = y0[c], b = y1[c];
+      if (kSplit) {
+        for (int kc = 1; kc < ksplit; ++kc) {
+          const float4 a2 = y0[kc * kc_stride + c], b2 = y1[kc * kc_stride + c];
+          a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
+          b = make_float4(b.x + b2.x, b.y + b2.y, b.z + b2.z, b.w + b2.w);
+        }
+      }
       m[i] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
       ss = fmaf(m[i].x, m[i].x, ss);
       ss = fmaf(m[i].y, m[i].y, ss);

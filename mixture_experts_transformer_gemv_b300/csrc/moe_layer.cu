@@ -10,9 +10,12 @@
 //   K3 grouped_gemm<geglu>  act = GELU(A W^T) * (A Wv^T)        (tcgen05)
 //   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
 //   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
+// For T <= 16 (or MOE_FLAG_FORCE_GEMV) K3/K4 are replaced by the weight-streaming
+// decode kernels (k_decode.cuh) and K5 sums their split-K partials.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <array>
 #include <atomic>
 #include <cstdarg>
@@ -25,6 +28,7 @@
 #include "moe_layer.h"
 #include "common.cuh"
 #include "k_combine.cuh"
+#include "k_decode.cuh"
 #include "k_gemm.cuh"
 #include "k_permute.cuh"
 #include "k_router.cuh"
@@ -92,6 +96,7 @@ EncodeTiledFn get_encoder() {
 
 // Row-major 2-D tensor [rows, inner] of 2-byte elements, box [box_rows, 64], 128-byte swizzle.
 moe_status_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  static_assert(kGemmBK == kDecBK, "both GEMM families use 64-element boxes");
   EncodeTiledFn enc = get_encoder();
   if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner, rows};
@@ -130,9 +135,12 @@ struct moe_layer {
   __nv_bfloat16* xn_perm = nullptr;
   __nv_bfloat16* act = nullptr;
   float* y_rows = nullptr;
+  float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
   uint32_t* err = nullptr;
+  int ksplit = 1;         // decode path: chunks of the down-projection reduction
 
   CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1{};
+  CUtensorMap tm_xn_perm16{}, tm_act16{}, tm_w1_128{};  // decode path boxes
 
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
   size_t host_stage_bytes = 0;
@@ -191,7 +199,22 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, L->xn_perm);
   }
   mark(3);
-  {
+  const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) ||
+                      (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
+  if (decode) {
+    DecParams p{};
+    p.sched = L->sched;
+    p.K = d;
+    p.rows_per_expert = F;
+    p.n_out = F;
+    p.ksplit = 1;
+    p.out = L->act;
+    p.row_scale = nullptr;
+    p.err = L->err;
+    p.timeout_ns = kWaitLimitNs;
+    decode_gemm_kernel<kEpiGeglu><<<L->num_sms, kDecThreads, DecCfg<kEpiGeglu>::kSmemBytes, st>>>(
+        L->tm_w, L->tm_wv, L->tm_xn_perm16, p);
+  } else {
     GemmParams p{};
     p.sched = L->sched;
     p.K = d;
@@ -206,7 +229,20 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
                                                                                      L->tm_wv, p);
   }
   mark(4);
-  {
+  if (decode) {
+    DecParams p{};
+    p.sched = L->sched;
+    p.K = F;
+    p.rows_per_expert = d;
+    p.n_out = d;
+    p.ksplit = L->ksplit;
+    p.out = L->part;
+    p.row_scale = L->prob_of_row;
+    p.err = L->err;
+    p.timeout_ns = kWaitLimitNs;
+    decode_gemm_kernel<kEpiDown><<<L->num_sms, kDecThreads, DecCfg<kEpiDown>::kSmemBytes, st>>>(
+        L->tm_w1_128, L->tm_w1_128, L->tm_act16, p);
+  } else {
     GemmParams p{};
     p.sched = L->sched;
     p.K = F;
@@ -221,9 +257,14 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
                                                                                     p);
   }
   mark(5);
-  combine_kernel<<<T, kCombineThreads, 0, st>>>(L->y_rows, L->row_of_slot, static_cast<const __nv_bfloat16*>(hidden),
-                                                L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks,
-                                                L->err, static_cast<__nv_bfloat16*>(out));
+  if (decode)
+    combine_kernel<true><<<T, kCombineThreads, 0, st>>>(
+        L->part, L->row_of_slot, L->idx, L->sched, L->ksplit, static_cast<const __nv_bfloat16*>(hidden),
+        L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks, L->err, static_cast<__nv_bfloat16*>(out));
+  else
+    combine_kernel<false><<<T, kCombineThreads, 0, st>>>(
+        L->y_rows, L->row_of_slot, L->idx, L->sched, 1, static_cast<const __nv_bfloat16*>(hidden),
+        L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks, L->err, static_cast<__nv_bfloat16*>(out));
   mark(6);
   L->launches += MOE_K_COUNT;
   cudaError_t e = cudaGetLastError();
@@ -269,8 +310,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     return fail(MOE_ERR_INVALID_ARG, "unknown weight_dtype %d", c.weight_dtype);
   if (c.weight_dtype == MOE_WEIGHT_INT8)
     return fail(MOE_ERR_UNSUPPORTED, "int8 expert weights are not implemented in this build");
-  if (c.flags & MOE_FLAG_FORCE_GEMV)
-    return fail(MOE_ERR_UNSUPPORTED, "the weight-streaming decode path is not implemented in this build");
+  if ((c.flags & MOE_FLAG_FORCE_GEMV) && (c.flags & MOE_FLAG_FORCE_TC))
+    return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_FORCE_GEMV and MOE_FLAG_FORCE_TC are exclusive");
   const void* req[] = {w->gate, w->w, w->wv, w->w1, w->pre_norm_scale, w->post_norm_scale};
   for (const void* p : req)
     if (!p || !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
@@ -282,9 +323,11 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   MOE_CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
   if (!(prop.major == 10 && prop.minor == 3))
     return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
-  if (prop.sharedMemPerBlockOptin < kGemmSmemBytes)
+  const size_t smem_need =
+      std::max(kGemmSmemBytes, std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes));
+  if (prop.sharedMemPerBlockOptin < smem_need)
     return fail(MOE_ERR_UNSUPPORTED, "device offers %zu B shared memory per block, need %zu",
-                (size_t)prop.sharedMemPerBlockOptin, kGemmSmemBytes);
+                (size_t)prop.sharedMemPerBlockOptin, smem_need);
 
   auto* L = new (std::nothrow) moe_layer();
   if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
@@ -297,11 +340,12 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   const int64_t R = L->rows_cap;
 
   // one workspace block, every buffer 1 KB aligned
-  size_t offs[11], total = 0;
-  const size_t sizes[11] = {(size_t)(T * d * 2), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
+  size_t offs[12], total = 0;
+  const size_t sizes[12] = {(size_t)(T * d * 2), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
                             (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
-                            (size_t)(R * F * 2), (size_t)(R * d * 4), 256};
-  for (int i = 0; i < 11; ++i) {
+                            (size_t)(R * F * 2), (size_t)(R * d * 4), 256,
+                            (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4};
+  for (int i = 0; i < 12; ++i) {
     offs[i] = total;
     total = align_up(total + sizes[i], 1024);
   }
@@ -323,6 +367,10 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   L->act = reinterpret_cast<__nv_bfloat16*>(b + offs[8]);
   L->y_rows = reinterpret_cast<float*>(b + offs[9]);
   L->err = reinterpret_cast<uint32_t*>(b + offs[10]);
+  L->part = reinterpret_cast<float*>(b + offs[11]);
+  // decode-path split of the F reduction: up to kDecMaxSplit chunks of whole 64-wide blocks
+  L->ksplit = kDecMaxSplit;
+  while (L->ksplit > 1 && (F / kDecBK) % L->ksplit) L->ksplit /= 2;
   moe_status_t s = MOE_OK;
   if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmBM);
@@ -330,6 +378,9 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmBN / 2);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmBN / 2);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1, w->w1, F, kNumExperts * d, kGemmBN);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kDecBM);
   if (s == MOE_OK &&
       cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
@@ -338,6 +389,14 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
       cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (down GEMM) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(decode_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)DecCfg<kEpiGeglu>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (decode up) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(decode_gemm_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)DecCfg<kEpiDown>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (decode down) failed");
   if (s == MOE_OK) {
     L->ring.resize(kProfRing);
     L->pending.assign(kProfRing, false);
@@ -375,6 +434,8 @@ moe_status_t moe_layer_forward(moe_layer_t* L, const void* hidden, void* out, in
   if (T == 0) return ok();
   if (!hidden || !out || !aligned16(hidden) || !aligned16(out))
     return fail(MOE_ERR_INVALID_ARG, "hidden/out null or not 16-byte aligned");
+  if ((L->cfg.flags & MOE_FLAG_FORCE_GEMV) && T > kDecNS)
+    return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_FORCE_GEMV handles T <= %d (got %d)", kDecNS, T);
   if ((topk_idx && !aligned4(topk_idx)) || (topk_prob && !aligned4(topk_prob)) ||
       (expert_counts && !aligned4(expert_counts)))
     return fail(MOE_ERR_INVALID_ARG, "optional output pointer misaligned");

@@ -172,3 +172,48 @@ def test_intermediates_match_oracle():
         toks = sorted(t for t in range(T) for k in range(2) if r.idx[t, k] == e)
         rows = [int(ros[t, k]) for t in toks for k in range(2) if r.idx[t, k] == e]
         assert rows == list(range(off[e], off[e] + counts[e]))
+
+
+@pytest.mark.parametrize("T,d,F,seed", [
+    (1, 256, 512, 61),
+    (5, 384, 640, 62),     # ragged: d/128 = 3 row blocks, F/64 = 10 -> 2-way split
+    (8, 512, 1024, 63),
+    (16, 256, 512, 64),    # the largest T the decode path takes
+])
+@pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_FORCE_TC])
+def test_decode_path_and_forced_tensor_core_path(T, d, F, seed, flags):
+    """T <= 16 runs the weight-streaming decode kernels unless the tensor-core
+    grouped GEMM path is forced; both must match the oracle."""
+    _full_check(synth.make_inputs(T, d, F, seed, name=f"dec{T}x{d}x{F}"), flags=flags)
+
+
+def test_force_gemv_flag():
+    inp = synth.make_inputs(40, 256, 512, 65, name="force_gemv")
+    layer = make_layer(inp, flags=moe.MOE_FLAG_FORCE_GEMV)
+    x = bf16_tensor(inp.x)
+    with pytest.raises(moe.MoeError) as ei:
+        layer.forward(x)  # 40 tokens: beyond the decode path's 16
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    sub = synth.make_inputs(12, 256, 512, 65, name="force_gemv12")
+    y, idx, prob, counts = run(layer, sub, x_dev=x[:12].contiguous())
+    ref = oracle.moe_tokens(sub)
+    assert_routing(idx, prob, counts, ref, "force_gemv")
+    assert_values(y, ref.y, "force_gemv")
+
+
+def test_decode_and_tensor_core_paths_agree_on_one_expert_heavy_batch():
+    """All 16 tokens to expert 3 (16 slots, the decode path's limit)."""
+    inp = synth.make_inputs(16, 256, 512, 66, name="dec_onehot")
+    b = np.zeros(8, np.float32)
+    b[3] = 1e4
+    inp.bias = b
+    outs = []
+    for flags in (0, moe.MOE_FLAG_FORCE_TC):
+        layer = make_layer(inp, flags=flags)
+        y, idx, prob, counts = run(layer, inp)
+        assert counts[3] == 16
+        outs.append(y)
+        layer.close()
+    ref = oracle.moe_tokens(inp)
+    for y in outs:
+        assert_values(y, ref.y, "dec_onehot")
