@@ -8,10 +8,11 @@
 //
 // Structure (one CTA per SM, persistent, static round-robin over tiles):
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage,
-//               128-byte swizzle, into a kGemmStages-deep shared-memory ring
+//               128-byte swizzle, into a 4-stage shared-memory ring (3 for int8)
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (M=128, N=256, K=16, bf16 -> fp32) and tcgen05.commit
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, GeGLU or scale, stores
+//   warps 6-9   int8 weights only: int8 -> bf16 conversion of the B tile
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap the
 // mainloop of tile i+1.  In K3 the B tile stacks 128 rows of W over the same 128
 // rows of Wv, so one N=256 MMA produces both branches of 128 output columns.
@@ -20,6 +21,15 @@
 // row_offset[e+1]), a multiple of 128.  Tile t maps to (expert, n-block,
 // m-block) with the m-block fastest, so CTAs working at the same time share the
 // same weight tile through L2.
+//
+// int8 weights ("TevunahAi/Grok-1-BF16", "Conversion Details": int8 values
+// with bf16 scales, one per expert and output channel for the (8, 1, N) scale
+// shape): TMA brings the raw int8 B tile into a staging buffer; four converter
+// warps (6-9) rewrite it as bf16 in the 128-byte-swizzled K-major layout the MMA
+// reads (|q| <= 127 is exact in bf16), make it visible to the tensor core's
+// async proxy and release the stage to the MMA warp.  Because the scale belongs
+// to an output channel it factors out of the reduction and is applied in fp32
+// in the epilogue: sum_k a_k (q_nk s_n) = s_n sum_k a_k q_nk.
 //
 // Every wait is bounded (wait_bounded).  A role that times out raises the CTA's
 // abort flag and the device error word; the others stop at their next wait; the
@@ -34,16 +44,31 @@ namespace moe {
 constexpr int kGemmBM = 128;   // MMA M: permuted rows per tile
 constexpr int kGemmBN = 256;   // MMA N
 constexpr int kGemmBK = 64;    // K per stage (64 bf16 = one 128-byte swizzle row)
-constexpr int kGemmStages = 4;
-constexpr int kGemmThreads = 192;
-constexpr int kEpiWarp0 = 2;   // first epilogue warp
+constexpr int kEpiWarp0 = 2;   // first epilogue warp (warps 2-5)
+constexpr int kConvWarp0 = 6;  // first converter warp (warps 6-9, int8 weights only)
+constexpr int kEpiThreads = 128;
+constexpr int kConvThreads = 128;
 constexpr int kATileBytes = kGemmBM * kGemmBK * 2;  // 16 KB
-constexpr int kBTileBytes = kGemmBN * kGemmBK * 2;  // 32 KB
-constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kBTileBytes = kGemmBN * kGemmBK * 2;  // 32 KB (bf16, swizzled)
+constexpr int kB8TileBytes = kGemmBN * kGemmBK;     // 16 KB (int8 staging, dense rows of 64 B)
 constexpr uint32_t kTmemCols = 2 * kGemmBN;  // two fp32 accumulators of 128 x 256
-constexpr int kNumBars = 2 * kGemmStages + 5;   // full, empty, tmem_full x2, tmem_empty x2, drain
-constexpr size_t kGemmSmemBytes = 1024 + (size_t)kGemmStages * kStageBytes + kNumBars * 8 + 16;
 constexpr uint32_t kGemmIdesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+
+// Per weight type: ring depth, bytes per stage, threads.
+//   bf16: A 16 KB + B 32 KB per stage, 4 stages, 6 warps
+//   int8: A 16 KB + B 32 KB + int8 B 16 KB per stage, 3 stages, 10 warps
+template <bool WQ>
+struct GemmCfg {
+  static constexpr int kStages = WQ ? 3 : 4;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes + (WQ ? kB8TileBytes : 0);
+  static constexpr int kTxBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
+  static constexpr int kThreads = WQ ? 320 : 192;
+  // full, empty, converted (int8), tmem_full x2, tmem_empty x2, drain
+  static constexpr int kNumBars = 3 * kStages + 5;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kNumBars * 8 + 16;
+};
+constexpr int kGemmThreads = GemmCfg<false>::kThreads;
+constexpr size_t kGemmSmemBytes = GemmCfg<false>::kSmemBytes;
 
 enum : int { kEpiGeglu = 0, kEpiDown = 1 };
 
@@ -55,6 +80,8 @@ struct GemmParams {
   int n_out;                     // output columns / leading dimension: F (act) or d (Y)
   void* out;                     // act [rows_cap, F] bf16 or Y [rows_cap, d] fp32
   const float* row_scale;        // down: combine weight of each permuted row
+  const uint16_t* scale0;        // int8: bf16 bits [E, n_out], scale of W (up) or W1 (down)
+  const uint16_t* scale1;        // int8 up: bf16 bits [E, F], scale of Wv
   uint32_t* err;                 // device error word
   uint64_t timeout_ns;           // limit of every wait
 };
@@ -84,23 +111,47 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* abort_flag, uint3
   atomicOr(err, kErrTimeout);
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// 4 int8 (one 32-bit word, element i in byte i) -> 4 bf16 in two words, exact:
+// with u = q + 128 placed in the low mantissa bits of 2^23, the float
+// (2^23 + u) - (2^23 + 128) equals q, and |q| <= 128 fits bf16's 8-bit
+// significand, so the bf16 rounding is exact too.
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
+  const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
+  const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
+  const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
+  lo = pack_bf16x2(f0, f1);
+  hi = pack_bf16x2(f2, f3);
+}
+
+// 8 bf16 scales (16 bytes of bf16 bits) -> fp32.
+__device__ __forceinline__ void load_scales8(const uint16_t* p, float (&s)[8]) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  s[0] = bf16_lo(v.x); s[1] = bf16_hi(v.x); s[2] = bf16_lo(v.y); s[3] = bf16_hi(v.y);
+  s[4] = bf16_lo(v.z); s[5] = bf16_hi(v.z); s[6] = bf16_lo(v.w); s[7] = bf16_hi(v.w);
+}
+
+template <int EPI, bool WQ>
+__global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const GemmParams p) {
+  using C = GemmCfg<WQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kGemmStages * kATileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kGemmStages * kBTileBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint8_t* sA = smem;                                 // [stages][128 x 64] bf16, swizzled
+  uint8_t* sB = sA + C::kStages * kATileBytes;        // [stages][256 x 64] bf16, swizzled
+  uint8_t* sB8 = sB + C::kStages * kBTileBytes;       // [stages][256 x 64] int8 staging (WQ only)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB8 + (WQ ? C::kStages * kB8TileBytes : 0));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const uint32_t bar0 = smem_addr(bars);
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kGemmStages + s); };
-  auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kGemmStages + a); };
-  auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kGemmStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kGemmStages + 4);
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (C::kStages + s); };
+  auto conv_bar = [&](uint32_t s) { return bar0 + 8u * (2 * C::kStages + s); };
+  auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (3 * C::kStages + a); };
+  auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (3 * C::kStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * C::kStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -111,13 +162,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int kb_count = p.K / kGemmBK;
 
   if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < kGemmStages; ++s) {
+    for (uint32_t s = 0; s < (uint32_t)C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(conv_bar(s), kConvThreads);
     }
     for (uint32_t a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 32 * (kGemmThreads / 32 - kEpiWarp0));
+      mbar_init(tempty_bar(a), kEpiThreads);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -141,9 +193,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      int issued[kGemmStages];
+      int issued[C::kStages];
 #pragma unroll
-      for (int s = 0; s < kGemmStages; ++s) issued[s] = -1;
+      for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         const TileCoord tc = decode_tile(t, off, p.n_tiles);
@@ -153,30 +205,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, kStageBytes);
+          mbar_arrive_expect_tx(fb, C::kTxBytes);
           const uint32_t a_dst = smem_addr(sA + stage * kATileBytes);
-          const uint32_t b_dst = smem_addr(sB + stage * kBTileBytes);
+          // bf16 weights land in the MMA's B buffer; int8 weights in the staging buffer
+          const uint32_t b_dst = WQ ? smem_addr(sB8 + stage * kB8TileBytes) : smem_addr(sB + stage * kBTileBytes);
+          const int b_half = WQ ? kB8TileBytes / 2 : kBTileBytes / 2;
           tma_load_2d(a_dst, &tm_a, fb, kb * kGemmBK, tc.row0);
           if (EPI == kEpiGeglu) {
             const int brow = tc.e * p.b_rows_per_expert + tc.n_blk * (kGemmBN / 2);
             tma_load_2d(b_dst, &tm_b0, fb, kb * kGemmBK, brow);
-            tma_load_2d(b_dst + kBTileBytes / 2, &tm_b1, fb, kb * kGemmBK, brow);
+            tma_load_2d(b_dst + b_half, &tm_b1, fb, kb * kGemmBK, brow);
           } else {
             const int brow = tc.e * p.b_rows_per_expert + tc.n_blk * kGemmBN;
             tma_load_2d(b_dst, &tm_b0, fb, kb * kGemmBK, brow);
           }
-          for (int s = 0; s < kGemmStages; ++s)
+          for (int s = 0; s < C::kStages; ++s)
             if (s == (int)stage) issued[s] = (int)phase;
-          if (++stage == kGemmStages) {
+          if (++stage == (uint32_t)C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       // every release of a stage by the MMA issuer has landed before exit
-      for (int i = 0; i < kGemmStages && ok; ++i) {
+      for (int i = 0; i < C::kStages && ok; ++i) {
         if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) ok = false;
-        if (++stage == kGemmStages) {
+        if (++stage == (uint32_t)C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -184,7 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) {
         raise_abort(abort_flag, p.err);
         // this role's copies still in flight complete before the CTA exits
-        for (int s = 0; s < kGemmStages; ++s)
+        for (int s = 0; s < C::kStages; ++s)
           if (issued[s] >= 0) wait_bounded(full_bar(s), (uint32_t)issued[s], nullptr, p.timeout_ns);
       }
     }
@@ -201,7 +255,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kGemmBN;
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+          if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
+              (WQ && !wait_bounded(conv_bar(stage), phase, abort_flag, p.timeout_ns))) {
             ok = false;
             break;
           }
@@ -212,7 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
             umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kGemmIdesc, (kb | kk) != 0);
           umma_commit(empty_bar(stage));
-          if (++stage == kGemmStages) {
+          if (++stage == (uint32_t)C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -227,7 +282,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!wait_bounded(drain_bar, 0, nullptr, p.timeout_ns)) ok = false;
       if (!ok) raise_abort(abort_flag, p.err);
     }
-  } else {
+  } else if (warp < kConvWarp0) {
     // --------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are reachable from this warp
     uint32_t acc = 0, acc_phase = 0;
@@ -243,14 +298,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row = tc.row0 + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kGemmBN;
       if (EPI == kEpiGeglu) {
-        __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.n_out + tc.n_blk * (kGemmBN / 2);
+        const int n0 = tc.n_blk * (kGemmBN / 2);
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.n_out + n0;
 #pragma unroll 1
         for (int c = 0; c < kGemmBN / 2 / 32; ++c) {
           uint32_t h[32], v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, h);
           tmem_ld_32x32b_x32(tbase + kGemmBN / 2 + c * 32, v);
           tmem_ld_wait();
+          if (WQ) {  // per-output-channel scales of W and Wv (same for every row)
+            const size_t so = (size_t)tc.e * p.n_out + n0 + c * 32;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              float sw[8], sv[8];
+              load_scales8(p.scale0 + so + 8 * g, sw);
+              load_scales8(p.scale1 + so + 8 * g, sv);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                h[8 * g + j] = __float_as_uint(__uint_as_float(h[8 * g + j]) * sw[j]);
+                v[8 * g + j] = __float_as_uint(__uint_as_float(v[8 * g + j]) * sv[j]);
+              }
+            }
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -272,11 +341,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t y[32];
           tmem_ld_32x32b_x32(tbase + c * 32, y);
           tmem_ld_wait();
+          float sc[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sc[j] = ps;
+          if (WQ) {  // per-output-channel scale of W1
+            const size_t so = (size_t)tc.e * p.n_out + col0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              float s8[8];
+              load_scales8(p.scale0 + so + 8 * g, s8);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) sc[8 * g + j] = s8[j] * ps;
+            }
+          }
           float4* dst = reinterpret_cast<float4*>(orow + col0);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(y[4 * k]) * ps, __uint_as_float(y[4 * k + 1]) * ps,
-                                 __uint_as_float(y[4 * k + 2]) * ps, __uint_as_float(y[4 * k + 3]) * ps);
+            dst[k] = make_float4(__uint_as_float(y[4 * k]) * sc[4 * k], __uint_as_float(y[4 * k + 1]) * sc[4 * k + 1],
+                                 __uint_as_float(y[4 * k + 2]) * sc[4 * k + 2],
+                                 __uint_as_float(y[4 * k + 3]) * sc[4 * k + 3]);
         }
       }
       tc_fence_before_sync();
@@ -284,6 +367,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+  } else if (WQ) {
+    // -------------------------------------------------- int8 -> bf16 converter
+    // Staging tile: 256 rows x 64 int8, row r at byte 64 r.  MMA tile: 256 rows x
+    // 64 bf16 in 128-byte swizzle atoms of 8 rows: element (r, k) at
+    // (r / 8) * 1024 + (r % 8) * 128 + ((k / 8) ^ (r % 8)) * 16 + (k % 8) * 2.
+    const int ct = threadIdx.x - kConvWarp0 * 32;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < kb_count; ++kb) {
+        ok = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns));
+        if (!ok) break;
+        const uint8_t* src = sB8 + stage * kB8TileBytes;
+        uint8_t* dst = sB + stage * kBTileBytes;
+#pragma unroll
+        for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
+          const int u = ct + i * kConvThreads;  // 16-byte unit: row u / 4, int8 columns [16 (u % 4), +16)
+          const int r = u >> 2, c = u & 3;
+          const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
+          uint4 o0, o1;
+          i8x4_to_bf16x4(qv.x, o0.x, o0.y);
+          i8x4_to_bf16x4(qv.y, o0.z, o0.w);
+          i8x4_to_bf16x4(qv.z, o1.x, o1.y);
+          i8x4_to_bf16x4(qv.w, o1.z, o1.w);
+          uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
+          *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = o0;
+          *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
+        mbar_arrive(conv_bar(stage));
+        if (++stage == (uint32_t)C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_abort(abort_flag, p.err);
   }
 
   tc_fence_before_sync();

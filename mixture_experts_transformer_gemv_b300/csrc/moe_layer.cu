@@ -10,8 +10,10 @@
 //   K3 grouped_gemm<geglu>  act = GELU(A W^T) * (A Wv^T)        (tcgen05)
 //   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
 //   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
-// For T <= 16 (or MOE_FLAG_FORCE_GEMV) K3/K4 are replaced by the weight-streaming
-// decode kernels (k_decode.cuh) and K5 sums their split-K partials.
+// For T <= 16 (or MOE_FLAG_FORCE_GEMV) with bf16 weights K3/K4 are replaced by the
+// weight-streaming decode kernels (k_decode.cuh) and K5 sums their split-K
+// partials.  int8 weights always take the grouped GEMMs (int8 -> bf16 in shared
+// memory, per-channel scale in the epilogue).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -110,6 +112,22 @@ moe_status_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, ui
   return MOE_OK;
 }
 
+// Row-major 2-D int8 tensor [rows, inner], box [box_rows, 64] (64-byte rows, no
+// swizzle): the staging layout the int8 -> bf16 converter warps read.
+moe_status_t make_tmap_i8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (int8) failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 constexpr int kProfRing = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -141,6 +159,7 @@ struct moe_layer {
 
   CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1{};
   CUtensorMap tm_xn_perm16{}, tm_act16{}, tm_w1_128{};  // decode path boxes
+  CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes)
 
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
   size_t host_stage_bytes = 0;
@@ -199,8 +218,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, L->xn_perm);
   }
   mark(3);
-  const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) ||
-                      (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
+  const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
+  const bool decode = !int8 && ((L->cfg.flags & MOE_FLAG_FORCE_GEMV) ||
+                                (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS));
   if (decode) {
     DecParams p{};
     p.sched = L->sched;
@@ -223,10 +243,16 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.n_out = F;
     p.out = L->act;
     p.row_scale = nullptr;
+    p.scale0 = L->w.w_scale;
+    p.scale1 = L->w.wv_scale;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
-    grouped_gemm_kernel<kEpiGeglu><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_xn_perm, L->tm_w,
-                                                                                     L->tm_wv, p);
+    if (int8)
+      grouped_gemm_kernel<kEpiGeglu, true><<<L->num_sms, GemmCfg<true>::kThreads, GemmCfg<true>::kSmemBytes, st>>>(
+          L->tm_xn_perm, L->tm_w8, L->tm_wv8, p);
+    else
+      grouped_gemm_kernel<kEpiGeglu, false><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_xn_perm,
+                                                                                             L->tm_w, L->tm_wv, p);
   }
   mark(4);
   if (decode) {
@@ -251,10 +277,16 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.n_out = d;
     p.out = L->y_rows;
     p.row_scale = L->prob_of_row;
+    p.scale0 = L->w.w1_scale;
+    p.scale1 = nullptr;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
-    grouped_gemm_kernel<kEpiDown><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_act, L->tm_w1, L->tm_w1,
-                                                                                    p);
+    if (int8)
+      grouped_gemm_kernel<kEpiDown, true><<<L->num_sms, GemmCfg<true>::kThreads, GemmCfg<true>::kSmemBytes, st>>>(
+          L->tm_act, L->tm_w18, L->tm_w18, p);
+    else
+      grouped_gemm_kernel<kEpiDown, false><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_act, L->tm_w1,
+                                                                                            L->tm_w1, p);
   }
   mark(5);
   if (decode)
@@ -308,14 +340,20 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (!(c.eps > 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be > 0");
   if (c.weight_dtype != MOE_WEIGHT_BF16 && c.weight_dtype != MOE_WEIGHT_INT8)
     return fail(MOE_ERR_INVALID_ARG, "unknown weight_dtype %d", c.weight_dtype);
-  if (c.weight_dtype == MOE_WEIGHT_INT8)
-    return fail(MOE_ERR_UNSUPPORTED, "int8 expert weights are not implemented in this build");
+  if ((c.flags & MOE_FLAG_FORCE_GEMV) && c.weight_dtype == MOE_WEIGHT_INT8)
+    return fail(MOE_ERR_UNSUPPORTED, "MOE_FLAG_FORCE_GEMV: the weight-streaming path takes bf16 weights only");
   if ((c.flags & MOE_FLAG_FORCE_GEMV) && (c.flags & MOE_FLAG_FORCE_TC))
     return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_FORCE_GEMV and MOE_FLAG_FORCE_TC are exclusive");
   const void* req[] = {w->gate, w->w, w->wv, w->w1, w->pre_norm_scale, w->post_norm_scale};
   for (const void* p : req)
     if (!p || !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
   if (w->gate_bias && !aligned4(w->gate_bias)) return fail(MOE_ERR_INVALID_ARG, "gate_bias misaligned");
+  if (c.weight_dtype == MOE_WEIGHT_INT8) {
+    const void* sc[] = {w->w_scale, w->wv_scale, w->w1_scale};
+    for (const void* p : sc)
+      if (!p || !aligned16(p))
+        return fail(MOE_ERR_INVALID_ARG, "int8 weights need w_scale, wv_scale, w1_scale (16-byte aligned)");
+  }
 
   int dev = 0;
   MOE_CUDA_TRY(cudaGetDevice(&dev));
@@ -324,7 +362,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (!(prop.major == 10 && prop.minor == 3))
     return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
   const size_t smem_need =
-      std::max(kGemmSmemBytes, std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes));
+      std::max(std::max(kGemmSmemBytes, GemmCfg<true>::kSmemBytes),
+               std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes));
   if (prop.sharedMemPerBlockOptin < smem_need)
     return fail(MOE_ERR_UNSUPPORTED, "device offers %zu B shared memory per block, need %zu",
                 (size_t)prop.sharedMemPerBlockOptin, smem_need);
@@ -375,20 +414,34 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmBM);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmBM);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmBN / 2);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmBN / 2);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1, w->w1, F, kNumExperts * d, kGemmBN);
+  if (c.weight_dtype == MOE_WEIGHT_BF16) {
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmBN / 2);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmBN / 2);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1, w->w1, F, kNumExperts * d, kGemmBN);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kDecBM);
+  } else {
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmBN / 2);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmBN / 2);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmBN);
+  }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kDecBM);
   if (s == MOE_OK &&
-      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (up GEMM) failed");
   if (s == MOE_OK &&
-      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (down GEMM) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<true>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 up GEMM) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<true>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 down GEMM) failed");
   if (s == MOE_OK &&
       cudaFuncSetAttribute(decode_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)DecCfg<kEpiGeglu>::kSmemBytes) != cudaSuccess)

@@ -15,7 +15,7 @@ from layer_helpers import assert_routing, assert_values, device_weights, make_la
 
 pytestmark = pytest.mark.gpu
 
-CASES = ["decode", "prefill", "skew"]
+CASES = ["decode", "prefill", "int8", "skew"]
 
 
 @pytest.fixture(scope="module", params=CASES)

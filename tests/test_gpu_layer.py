@@ -217,3 +217,44 @@ def test_decode_and_tensor_core_paths_agree_on_one_expert_heavy_batch():
     ref = oracle.moe_tokens(inp)
     for y in outs:
         assert_values(y, ref.y, "dec_onehot")
+
+
+# ------------------------------------------------------------- int8 weights
+# int8 expert weights with bf16 scales, one per expert and output channel (the
+# (8, 1, N) scale shape; "TevunahAi/Grok-1-BF16", "Conversion Details").  The
+# kernels convert int8 -> bf16 in shared memory and apply the scale in the epilogue.
+
+@pytest.mark.parametrize("T,d,F,seed", [
+    (300, 512, 1024, 71),    # several up and down tiles, ragged row blocks
+    (200, 384, 640, 72),     # ragged d (half a down tile) and F/128 = 5
+    (9, 256, 512, 73),       # T <= 16: int8 weights take the tensor-core path
+])
+def test_int8_weights(T, d, F, seed):
+    inp = synth.make_inputs(T, d, F, seed, name=f"int8_{T}x{d}x{F}", weight_dtype="int8")
+    _full_check(inp)
+
+
+def test_int8_skewed_and_checks():
+    inp = synth.make_inputs(256, 256, 512, 74, name="int8_skew", weight_dtype="int8", bias=synth.SKEW_BIAS)
+    _full_check(inp, flags=moe.MOE_FLAG_DEVICE_CHECKS)
+
+
+def test_int8_intermediates_match_oracle():
+    """GeGLU activations and scaled expert outputs of int8 experts."""
+    inp = synth.make_inputs(64, 256, 512, 75, name="int8_inter", weight_dtype="int8")
+    layer = make_layer(inp)
+    run(layer, inp)
+    ws = layer.workspace()
+    act = read_device(ws.act, (ws.rows_cap, inp.F), torch.bfloat16)
+    yr = read_device(ws.y_rows, (ws.rows_cap, inp.d), torch.float32)
+    ros = read_device(ws.row_of_slot, (inp.T, 2), torch.int32)
+    r = oracle.route(inp, keep_xn=True)
+    for t in (0, 31, inp.T - 1):
+        for rank in range(2):
+            e = int(r.idx[t, rank])
+            row = int(ros[t, rank])
+            h, v, a, o = oracle.expert_ffn(inp, r.xn[t], e)
+            assert np.max(np.abs(act[row] - a)) <= 0.02 * np.max(np.abs(a)) + 1e-6, (t, rank)
+            wo = r.w[t, rank] * o
+            assert np.max(np.abs(yr[row] - wo)) <= 0.02 * np.max(np.abs(wo)) + 1e-7, (t, rank)
+    layer.close()
