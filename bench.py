@@ -39,14 +39,22 @@ UNIT = "tokens/s"
 WORKLOAD = "prefill"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-KERNEL_SOURCES = {
-    "router": ["k_router.cuh"],
-    "permute": ["k_permute.cuh"],
-    "gather": ["k_permute.cuh"],
-    "up_geglu": ["k_gemm.cuh", "ptx.cuh"],
-    "down": ["k_gemm.cuh", "ptx.cuh"],
-    "combine": ["k_combine.cuh"],
-}
+# CUDA kernel behind each role of a forward, and the source files it is built from
+def kernel_function(role, inp):
+    """(kernel function name, source files) of a role for this workload's path."""
+    int8 = inp.weight_dtype == "int8"
+    if role in ("up_geglu", "down"):
+        epi = 0 if role == "up_geglu" else 1
+        if inp.T <= DECODE_MAX_T and not int8:
+            return f"decode_gemm_kernel<{epi}>", ["k_decode.cuh", "ptx.cuh", "common.cuh"]
+        return f"grouped_gemm_kernel<{epi}, {int(int8)}>", ["k_gemm.cuh", "ptx.cuh", "common.cuh"]
+    src = {"router": "k_router.cuh", "permute": "k_permute.cuh", "gather": "k_permute.cuh",
+           "combine": "k_combine.cuh"}[role]
+    name = {"router": "router_kernel", "permute": "permute_kernel", "gather": "gather_rows_kernel",
+            "combine": "combine_kernel"}[role]
+    return name, [src, "common.cuh"]
+
+
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -63,16 +71,23 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# extra workloads: the other Grok-1-shape configurations, and a reduced-F case
-# (same d, 2.4 GB of weights, still larger than L2) sized for ncu captures
-PROFILE_SMALL = dict(T=2048, d=6144, F=4096, seed=2000)
+# extra workloads: the other Grok-1-shape configurations, and reduced-F cases
+# (same d, weights still larger than L2) sized for ncu captures:
+#   profile_small        T=2048, F=4096, bf16 weights (1.2 GB)
+#   profile_small_int8   T=2048, F=4096, int8 weights (0.6 GB) + bf16 scales
+#   profile_decode_small T=8,    F=8192, bf16 weights (2.4 GB), the decode kernels
+PROFILE_CASES = {
+    "profile_small": dict(T=2048, d=6144, F=4096, seed=2000, weight_dtype="bf16"),
+    "profile_small_int8": dict(T=2048, d=6144, F=4096, seed=2001, weight_dtype="int8"),
+    "profile_decode_small": dict(T=8, d=6144, F=8192, seed=2002, weight_dtype="bf16"),
+}
 
 
 def make_workload(name):
     import synth
-    if name == "profile_small":
-        c = PROFILE_SMALL
-        return synth.make_inputs(c["T"], c["d"], c["F"], c["seed"], name=name)
+    if name in PROFILE_CASES:
+        c = PROFILE_CASES[name]
+        return synth.make_inputs(c["T"], c["d"], c["F"], c["seed"], name=name, weight_dtype=c["weight_dtype"])
     return synth.workload(name)
 
 
@@ -112,25 +127,44 @@ def algorithmic_work(inp, counts):
     return work
 
 
-def source_hash(kernel):
+def source_hash(files):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[kernel]:
+    for f in files:
         with open(os.path.join(ROOT, "mixture_experts_transformer_gemv_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of that kernel; else None."""
+def compulsory_bytes(role, inp, counts):
+    """Bytes a GEMM launch must move at least once: the chosen experts' weights,
+    its activation rows in and its output rows out (padded rows included, as
+    the kernel reads and writes them)."""
+    d, F = inp.d, inp.F
+    wb = 1 if inp.weight_dtype == "int8" else 2
+    n_act = int(sum(1 for c in counts if c > 0))
+    if inp.T <= DECODE_MAX_T and inp.weight_dtype == "bf16":
+        rows = 2 * inp.T
+    else:
+        rows = int(sum((c + 127) // 128 * 128 for c in counts))
+    if role == "up_geglu":
+        return n_act * 2 * F * d * wb + rows * d * 2 + rows * F * 2
+    return n_act * d * F * wb + rows * F * 2 + rows * d * 4
+
+
+def recorded_traffic(role, inp, counts):
+    """DRAM bytes per launch of this role's kernel from the committed ncu
+    summary (profiles/ncu_traffic.json), if it was captured on the kernel's
+    current source: the captured launch's DRAM bytes scaled by the ratio of
+    compulsory bytes (this workload / the captured one).  Else None."""
+    name, files = kernel_function(role, inp)
     try:
         with open(TRAFFIC_PATH) as f:
-            rec = json.load(f).get(kernel)
+            rec = json.load(f).get(name)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_sha") != source_hash(kernel):
+    if not rec or rec.get("source_sha") != source_hash(files) or role not in ("up_geglu", "down"):
         return None
-    return rec.get("dram_bytes_per_launch")
+    return int(rec["dram_bytes_per_launch"] * compulsory_bytes(role, inp, counts) / rec["compulsory_bytes"])
 
 
 class ClockSampler:
@@ -305,7 +339,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)}
     roof["kernel"] = dom
     roof["algorithmic_per_launch"] = amount
-    roof["traffic"] = recorded_traffic(dom)
+    roof["kernel_function"] = kernel_function(dom, inp)[0]
+    roof["traffic"] = recorded_traffic(dom, inp, counts)
     for name in kernels:
         b, a = work[name]
         d_s = kernels[name]["ms_per_launch"] / 1e3
@@ -414,7 +449,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["prefill", "decode", "skew", "int8", "tiny", "profile_small"],
+                    choices=["prefill", "decode", "skew", "int8", "tiny", *PROFILE_CASES],
                     help="prefill (T=8192) is the headline workload")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -19,6 +19,17 @@ constexpr uint32_t kErrCheck = 2u;
 //                                 row_offset[E] = total padded rows
 constexpr int kSchedInts = 2 * kNumExperts + 1;
 
+// Epilogues of the expert GEMMs: GeGLU of the up projections, or the
+// combine-weight scaling of the down projection.
+enum : int { kEpiGeglu = 0, kEpiDown = 1 };
+
+// A role of a warp-specialised kernel gave up waiting: tell the CTA's other
+// roles (shared abort flag) and the host (device error word).
+__device__ __forceinline__ void raise_abort(volatile uint32_t* abort_flag, uint32_t* err) {
+  *abort_flag = 1u;
+  atomicOr(err, kErrTimeout);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 

@@ -19,7 +19,6 @@
 // rings since each stage is small: 6 stages of 34 KB (K3d), 11 of 18 KB (K4d).
 #pragma once
 #include "common.cuh"
-#include "k_gemm.cuh"
 #include "ptx.cuh"
 
 namespace moe {

@@ -8,11 +8,11 @@
 //
 // Structure (one CTA per SM, persistent, static round-robin over tiles):
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage,
-//               128-byte swizzle, into a 4-stage shared-memory ring (3 for int8)
+//               128-byte swizzle, into a 4-stage shared-memory ring
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (M=128, N=256, K=16, bf16 -> fp32) and tcgen05.commit
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, GeGLU or scale, stores
-//   warps 6-9   int8 weights only: int8 -> bf16 conversion of the B tile
+//   warps 6-13  int8 weights only: int8 -> bf16 conversion of the B tile
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap the
 // mainloop of tile i+1.  In K3 the B tile stacks 128 rows of W over the same 128
 // rows of Wv, so one N=256 MMA produces both branches of 128 output columns.
@@ -24,8 +24,8 @@
 //
 // int8 weights ("TevunahAi/Grok-1-BF16", "Conversion Details": int8 values
 // with bf16 scales, one per expert and output channel for the (8, 1, N) scale
-// shape): TMA brings the raw int8 B tile into a staging buffer; four converter
-// warps (6-9) rewrite it as bf16 in the 128-byte-swizzled K-major layout the MMA
+// shape): TMA brings the raw int8 B tile into a staging buffer; eight converter
+// warps (6-13) rewrite it as bf16 in the 128-byte-swizzled K-major layout the MMA
 // reads (|q| <= 127 is exact in bf16), make it visible to the tensor core's
 // async proxy and release the stage to the MMA warp.  Because the scale belongs
 // to an output channel it factors out of the reduction and is applied in fp32
@@ -45,32 +45,34 @@ constexpr int kGemmBM = 128;   // MMA M: permuted rows per tile
 constexpr int kGemmBN = 256;   // MMA N
 constexpr int kGemmBK = 64;    // K per stage (64 bf16 = one 128-byte swizzle row)
 constexpr int kEpiWarp0 = 2;   // first epilogue warp (warps 2-5)
-constexpr int kConvWarp0 = 6;  // first converter warp (warps 6-9, int8 weights only)
+constexpr int kConvWarp0 = 6;  // first converter warp (warps 6-13, int8 weights only)
 constexpr int kEpiThreads = 128;
-constexpr int kConvThreads = 128;
+constexpr int kConvThreads = 256;
 constexpr int kATileBytes = kGemmBM * kGemmBK * 2;  // 16 KB
 constexpr int kBTileBytes = kGemmBN * kGemmBK * 2;  // 32 KB (bf16, swizzled)
 constexpr int kB8TileBytes = kGemmBN * kGemmBK;     // 16 KB (int8 staging, dense rows of 64 B)
 constexpr uint32_t kTmemCols = 2 * kGemmBN;  // two fp32 accumulators of 128 x 256
 constexpr uint32_t kGemmIdesc = idesc_bf16_f32(kGemmBM, kGemmBN);
 
-// Per weight type: ring depth, bytes per stage, threads.
-//   bf16: A 16 KB + B 32 KB per stage, 4 stages, 6 warps
-//   int8: A 16 KB + B 32 KB + int8 B 16 KB per stage, 3 stages, 10 warps
+// Per weight type:
+//   bf16: one TMA ring of 4 stages, A 16 KB + B 32 KB each; 6 warps.
+//   int8: a TMA ring of 5 stages, A 16 KB + int8 B 16 KB each, and a ring of 2
+//         converted bf16 B tiles (32 KB each) between the converter warps and
+//         the MMA warp; 14 warps.  The TMA ring stays deep (5 k-blocks of MMA
+//         work in flight) while conversion runs one k-block ahead of the MMA.
 template <bool WQ>
 struct GemmCfg {
-  static constexpr int kStages = WQ ? 3 : 4;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes + (WQ ? kB8TileBytes : 0);
-  static constexpr int kTxBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
-  static constexpr int kThreads = WQ ? 320 : 192;
-  // full, empty, converted (int8), tmem_full x2, tmem_empty x2, drain
-  static constexpr int kNumBars = 3 * kStages + 5;
-  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kNumBars * 8 + 16;
+  static constexpr int kStages = WQ ? 5 : 4;   // TMA ring
+  static constexpr int kBStages = WQ ? 2 : 0;  // converted-B ring
+  static constexpr int kStageBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
+  static constexpr int kThreads = WQ ? 32 * kConvWarp0 + kConvThreads : 192;
+  // full, empty (TMA ring), bfull, bempty (converted ring), tmem_full x2, tmem_empty x2, drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 5;
+  static constexpr size_t kSmemBytes =
+      1024 + (size_t)kStages * kStageBytes + (size_t)kBStages * kBTileBytes + kNumBars * 8 + 16;
 };
 constexpr int kGemmThreads = GemmCfg<false>::kThreads;
 constexpr size_t kGemmSmemBytes = GemmCfg<false>::kSmemBytes;
-
-enum : int { kEpiGeglu = 0, kEpiDown = 1 };
 
 struct GemmParams {
   const int32_t* sched;          // counts[E], row_offset[E + 1] (written by K2)
@@ -106,23 +108,22 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExp
   return c;
 }
 
-__device__ __forceinline__ void raise_abort(volatile uint32_t* abort_flag, uint32_t* err) {
-  *abort_flag = 1u;
-  atomicOr(err, kErrTimeout);
+// 4 int8 (one 32-bit word, element i in byte i) -> 4 bf16 in two words, exact,
+// with integer byte shuffles and one bf16x2 subtraction per pair.  For the
+// two's-complement byte q = m - 128 s (m = low 7 bits, s = sign bit), the bf16
+// with high byte 0x43 and low byte m is 128 + m, and with low byte 0x80 s it is
+// 128 + 128 s; their difference is q, exactly representable, so the
+// subtraction is exact.
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
-
-// 4 int8 (one 32-bit word, element i in byte i) -> 4 bf16 in two words, exact:
-// with u = q + 128 placed in the low mantissa bits of 2^23, the float
-// (2^23 + u) - (2^23 + 128) equals q, and |q| <= 128 fits bf16's 8-bit
-// significand, so the bf16 rounding is exact too.
 __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
-  const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
-  const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
-  const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
-  lo = pack_bf16x2(f0, f1);
-  hi = pack_bf16x2(f2, f3);
+  const uint32_t m = w & 0x7F7F7F7Fu;
+  const uint32_t s = w & 0x80808080u;
+  lo = bf16x2_sub(__byte_perm(m, 0x43u, 0x4140), __byte_perm(s, 0x43u, 0x4140));
+  hi = bf16x2_sub(__byte_perm(m, 0x43u, 0x4342), __byte_perm(s, 0x43u, 0x4342));
 }
 
 // 8 bf16 scales (16 bytes of bf16 bits) -> fp32.
@@ -139,19 +140,23 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
   using C = GemmCfg<WQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                                 // [stages][128 x 64] bf16, swizzled
-  uint8_t* sB = sA + C::kStages * kATileBytes;        // [stages][256 x 64] bf16, swizzled
-  uint8_t* sB8 = sB + C::kStages * kBTileBytes;       // [stages][256 x 64] int8 staging (WQ only)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB8 + (WQ ? C::kStages * kB8TileBytes : 0));
+  // bf16: sA [4][128 x 64] | sB [4][256 x 64]                (bf16, 128-byte swizzle)
+  // int8: sA [5][128 x 64] | sB8 [5][256 x 64] int8 staging | sB [2][256 x 64] bf16
+  uint8_t* sA = smem;
+  uint8_t* sB8 = sA + C::kStages * kATileBytes;
+  uint8_t* sB = WQ ? sB8 + C::kStages * kB8TileBytes : sA + C::kStages * kATileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (WQ ? C::kBStages : C::kStages) * kBTileBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const uint32_t bar0 = smem_addr(bars);
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (C::kStages + s); };
-  auto conv_bar = [&](uint32_t s) { return bar0 + 8u * (2 * C::kStages + s); };
-  auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (3 * C::kStages + a); };
-  auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (3 * C::kStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * C::kStages + 4);
+  auto bfull_bar = [&](uint32_t j) { return bar0 + 8u * (2 * C::kStages + j); };
+  auto bempty_bar = [&](uint32_t j) { return bar0 + 8u * (2 * C::kStages + C::kBStages + j); };
+  const uint32_t bar_t = bar0 + 8u * (2 * C::kStages + 2 * C::kBStages);
+  auto tfull_bar = [&](uint32_t a) { return bar_t + 8u * a; };
+  auto tempty_bar = [&](uint32_t a) { return bar_t + 8u * (2 + a); };
+  const uint32_t drain_bar = bar_t + 8u * 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -165,7 +170,10 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
     for (uint32_t s = 0; s < (uint32_t)C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(conv_bar(s), kConvThreads);
+    }
+    for (int j = 0; j < C::kBStages; ++j) {
+      mbar_init(bfull_bar(j), kConvThreads);
+      mbar_init(bempty_bar(j), 1);
     }
     for (uint32_t a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -205,10 +213,10 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::kTxBytes);
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
           const uint32_t a_dst = smem_addr(sA + stage * kATileBytes);
           // bf16 weights land in the MMA's B buffer; int8 weights in the staging buffer
-          const uint32_t b_dst = WQ ? smem_addr(sB8 + stage * kB8TileBytes) : smem_addr(sB + stage * kBTileBytes);
+          const uint32_t b_dst = smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes);
           const int b_half = WQ ? kB8TileBytes / 2 : kBTileBytes / 2;
           tma_load_2d(a_dst, &tm_a, fb, kb * kGemmBK, tc.row0);
           if (EPI == kEpiGeglu) {
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -256,13 +264,13 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * kGemmBN;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
-              (WQ && !wait_bounded(conv_bar(stage), phase, abort_flag, p.timeout_ns))) {
+              (WQ && !wait_bounded(bfull_bar(bstage), bphase, abort_flag, p.timeout_ns))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint64_t adesc = smem_desc_k_sw128(smem_addr(sA + stage * kATileBytes));
-          const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sB + stage * kBTileBytes));
+          const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sB + (WQ ? bstage : stage) * kBTileBytes));
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
             umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kGemmIdesc, (kb | kk) != 0);
@@ -270,6 +278,13 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
           if (++stage == (uint32_t)C::kStages) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (WQ) {
+            umma_commit(bempty_bar(bstage));
+            if (++bstage == (uint32_t)C::kBStages) {
+              bstage = 0;
+              bphase ^= 1u;
+            }
           }
         }
         if (!ok) break;
@@ -373,14 +388,15 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
     // 64 bf16 in 128-byte swizzle atoms of 8 rows: element (r, k) at
     // (r / 8) * 1024 + (r % 8) * 128 + ((k / 8) ^ (r % 8)) * 16 + (k % 8) * 2.
     const int ct = threadIdx.x - kConvWarp0 * 32;
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       for (int kb = 0; kb < kb_count; ++kb) {
-        ok = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns));
+        ok = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
+                                         wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag, p.timeout_ns));
         if (!ok) break;
         const uint8_t* src = sB8 + stage * kB8TileBytes;
-        uint8_t* dst = sB + stage * kBTileBytes;
+        uint8_t* dst = sB + bstage * kBTileBytes;
 #pragma unroll
         for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
           const int u = ct + i * kConvThreads;  // 16-byte unit: row u / 4, int8 columns [16 (u % 4), +16)
@@ -396,10 +412,14 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
           *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
         }
         fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
-        mbar_arrive(conv_bar(stage));
+        mbar_arrive(bfull_bar(bstage));
         if (++stage == (uint32_t)C::kStages) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++bstage == (uint32_t)C::kBStages) {
+          bstage = 0;
+          bphase ^= 1u;
         }
       }
     }
