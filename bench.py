@@ -145,7 +145,7 @@ def compulsory_bytes(role, inp, counts):
     if inp.T <= DECODE_MAX_T and inp.weight_dtype == "bf16":
         rows = 2 * inp.T
     else:
-        rows = int(sum((c + 127) // 128 * 128 for c in counts))
+        rows = int(sum((c + 255) // 256 * 256 for c in counts))
     if role == "up_geglu":
         return n_act * 2 * F * d * wb + rows * d * 2 + rows * F * 2
     return n_act * d * F * wb + rows * F * 2 + rows * d * 4
@@ -366,6 +366,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": int(inp.T * inp.d * 2), "ms_per_step": round(e2e_s * 1e3, 3),
                 "entry_point": "moe_layer_forward_host (pinned host buffers)"},
         "gpu_launches": int(launches),
+        "gemm_grid": layer.gemm_grid(),
         "clocks": clk,
     }
     layer.close()

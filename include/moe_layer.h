@@ -172,6 +172,11 @@ moe_status_t moe_layer_set_profiling(moe_layer_t* layer, int32_t enable);
  * reset != 0 clears the sums afterwards. */
 moe_status_t moe_layer_profile_read(moe_layer_t* layer, double* ms_total, int64_t* launches, int32_t reset);
 
+/* Grid sizes (CTAs) of the grouped-GEMM launches this handle makes:
+ * grid[0] up / bf16, grid[1] down / bf16, grid[2] up / int8, grid[3] down / int8.
+ * Each is twice the number of CTA pairs that can be resident at once. */
+moe_status_t moe_layer_gemm_grid(const moe_layer_t* layer, int32_t grid[4]);
+
 /* Kernel launches enqueued by this handle since creation (all kernels). */
 int64_t moe_layer_launch_count(const moe_layer_t* layer);
 

@@ -78,6 +78,8 @@ def lib():
         L.moe_layer_set_profiling.argtypes = [vp, i32]
         L.moe_layer_profile_read.restype = i32
         L.moe_layer_profile_read.argtypes = [vp, vp, vp, i32]
+        L.moe_layer_gemm_grid.restype = i32
+        L.moe_layer_gemm_grid.argtypes = [vp, vp]
         L.moe_layer_launch_count.restype = i64
         L.moe_layer_launch_count.argtypes = [vp]
         L.moe_layer_workspace.restype = i32
@@ -211,6 +213,12 @@ class MoeLayer:
         n = (ctypes.c_int64 * len(KERNEL_NAMES))()
         _check(lib().moe_layer_profile_read(self._h, ms, n, 1 if reset else 0), "moe_layer_profile_read")
         return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_NAMES)}
+
+    def gemm_grid(self) -> dict:
+        """CTAs per grouped-GEMM launch: {"up_bf16", "down_bf16", "up_int8", "down_int8"}."""
+        g = (ctypes.c_int32 * 4)()
+        _check(lib().moe_layer_gemm_grid(self._h, g), "moe_layer_gemm_grid")
+        return dict(zip(("up_bf16", "down_bf16", "up_int8", "down_int8"), list(g)))
 
     def launch_count(self) -> int:
         return int(lib().moe_layer_launch_count(self._h))

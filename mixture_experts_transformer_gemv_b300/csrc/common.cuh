@@ -7,7 +7,7 @@ namespace moe {
 
 constexpr int kNumExperts = 8;   // Grok-1: 8 experts ("Jah-yee/grok" README, architecture diagram)
 constexpr int kTopK = 2;         // top-2 routing
-constexpr int kRowTile = 128;    // rows of one expert tile; expert row blocks are padded to it
+constexpr int kRowTile = 256;    // rows of one expert GEMM tile (a CTA pair); expert row blocks are padded to it
 
 // Device error word bits (latched in the handle, read by moe_layer_sync_status).
 constexpr uint32_t kErrTimeout = 1u;

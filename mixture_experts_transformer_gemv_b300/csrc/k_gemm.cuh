@@ -1,4 +1,5 @@
-// K3 / K4: expert-grouped GEMMs on the 5th-generation tensor cores.
+// K3 / K4: expert-grouped GEMMs on the 5th-generation tensor cores, one CTA pair
+// (a cluster of two CTAs on neighbouring SMs) per 256-row tile.
 //
 //   K3 (up, GeGLU):  act[r, n] = GELU(sum_k A[r,k] W[e,n,k]) * (sum_k A[r,k] Wv[e,n,k])
 //   K4 (down):       Y[r, j]   = p[r] * sum_n act[r,n] W1[e,j,n]
@@ -6,66 +7,86 @@
 // diagram: GELU(x W) (*) (x Wv), then the output projection; weights in PyTorch
 // [out, in] order per "TevunahAi/Grok-1-BF16", "Weight Verification").
 //
-// Structure (one CTA per SM, persistent, static round-robin over tiles):
-//   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage,
-//               128-byte swizzle, into a 4-stage shared-memory ring
-//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//               (M=128, N=256, K=16, bf16 -> fp32) and tcgen05.commit
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, GeGLU or scale, stores
-//   warps 6-13  int8 weights only: int8 -> bf16 conversion of the B tile
+// A tile is M = 256 permuted rows x N = 256 accumulator columns.  One thread of
+// the even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16): A rows
+// [0,128) and B rows [0,128) come from the even CTA's shared memory, A rows
+// [128,256) and B rows [128,256) from the odd CTA's, and each CTA's Tensor Memory
+// receives the accumulator of its own 128 rows.  Each CTA therefore stages only
+// half of the weight tile: per k-block of 64 it loads A 128 x 64 and B 128 x 64
+// (32 KB in bf16) for 128 x 256 x 64 MMA work, against 48 KB when a CTA works
+// alone.  In K3 the even CTA's B half is 128 rows of W and the odd CTA's the
+// same 128 rows of Wv, so accumulator columns [0,128) hold x W and [128,256)
+// hold x Wv for the same 128 output channels; in K4 the halves are 2 x 128 rows
+// of W1 (256 output columns of d).
+//
+// Warp roles in each CTA (one CTA per SM, persistent, static round-robin of
+// tiles over pairs):
+//   warp 0      TMA producer: the CTA's A and B halves per k-block into a
+//               6-stage shared-memory ring, 128-byte swizzle
+//   warp 1      allocates 512 TMEM columns (both CTAs, cta_group::2).  Even CTA:
+//               issues the MMAs and tcgen05.commit, multicast to both CTAs'
+//               barriers.  Odd CTA, bf16 weights: forwards the completion of each
+//               of its own TMA stages to the even CTA's barrier.
+//   warps 2-5   epilogue of the CTA's 128 rows: tcgen05.ld, GeGLU or scaling,
+//               stores; then tell the even CTA's MMA warp the accumulator is free
+//   warps 6-13  int8 weights only: int8 -> bf16 conversion of the CTA's B half
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap the
-// mainloop of tile i+1.  In K3 the B tile stacks 128 rows of W over the same 128
-// rows of Wv, so one N=256 MMA produces both branches of 128 output columns.
+// mainloop of tile i+1.
 //
 // Tiles never mix experts: expert e owns permuted rows [row_offset[e],
-// row_offset[e+1]), a multiple of 128.  Tile t maps to (expert, n-block,
-// m-block) with the m-block fastest, so CTAs working at the same time share the
-// same weight tile through L2.
+// row_offset[e+1]), a multiple of 256.  Tile t maps to (expert, n-block,
+// m-block) with the m-block fastest, so pairs working at the same time share
+// the same weight tile through L2.
 //
 // int8 weights ("TevunahAi/Grok-1-BF16", "Conversion Details": int8 values
 // with bf16 scales, one per expert and output channel for the (8, 1, N) scale
-// shape): TMA brings the raw int8 B tile into a staging buffer; eight converter
-// warps (6-13) rewrite it as bf16 in the 128-byte-swizzled K-major layout the MMA
-// reads (|q| <= 127 is exact in bf16), make it visible to the tensor core's
-// async proxy and release the stage to the MMA warp.  Because the scale belongs
-// to an output channel it factors out of the reduction and is applied in fp32
-// in the epilogue: sum_k a_k (q_nk s_n) = s_n sum_k a_k q_nk.
+// shape): TMA brings the CTA's raw int8 B half into a staging buffer; the
+// converter warps rewrite it as bf16 in the 128-byte-swizzled K-major layout
+// the MMA reads (|q| <= 127 is exact in bf16), make it visible to the tensor
+// core's async proxy and tell the even CTA's MMA warp.  Because the scale
+// belongs to an output channel it factors out of the reduction and is applied
+// in fp32 in the epilogue: sum_k a_k (q_nk s_n) = s_n sum_k a_k q_nk.
 //
-// Every wait is bounded (wait_bounded).  A role that times out raises the CTA's
-// abort flag and the device error word; the others stop at their next wait; the
-// producer then waits (bounded) for its own TMA copies in flight, the MMA issuer
-// for its own MMAs, and TMEM is freed before the CTA exits.
+// Every wait is bounded (wait_bounded).  A role that times out raises its CTA's
+// abort flag and the device error word; the others stop at their next wait
+// (the other CTA's roles run out of time on theirs); the producer then waits
+// (bounded) for its own TMA copies in flight, the MMA issuer for its own MMAs,
+// and both CTAs meet at a cluster barrier before TMEM is freed and they exit.
 #pragma once
 #include "common.cuh"
 #include "ptx.cuh"
+#include "ptx_pair.cuh"
 
 namespace moe {
 
-constexpr int kGemmBM = 128;   // MMA M: permuted rows per tile
-constexpr int kGemmBN = 256;   // MMA N
-constexpr int kGemmBK = 64;    // K per stage (64 bf16 = one 128-byte swizzle row)
-constexpr int kEpiWarp0 = 2;   // first epilogue warp (warps 2-5)
-constexpr int kConvWarp0 = 6;  // first converter warp (warps 6-13, int8 weights only)
-constexpr int kEpiThreads = 128;
-constexpr int kConvThreads = 256;
-constexpr int kATileBytes = kGemmBM * kGemmBK * 2;  // 16 KB
-constexpr int kBTileBytes = kGemmBN * kGemmBK * 2;  // 32 KB (bf16, swizzled)
-constexpr int kB8TileBytes = kGemmBN * kGemmBK;     // 16 KB (int8 staging, dense rows of 64 B)
-constexpr uint32_t kTmemCols = 2 * kGemmBN;  // two fp32 accumulators of 128 x 256
+constexpr int kGemmBM = 256;     // rows per tile (pair)
+constexpr int kGemmHalfM = 128;  // rows per CTA
+constexpr int kGemmBN = 256;     // MMA N (accumulator columns)
+constexpr int kGemmHalfN = 128;  // B rows per CTA
+constexpr int kGemmBK = 64;      // K per stage (64 bf16 = one 128-byte swizzle row)
+constexpr int kEpiWarp0 = 2;     // first epilogue warp (warps 2-5)
+constexpr int kConvWarp0 = 6;    // first converter warp (warps 6-13, int8 weights only)
+constexpr int kEpiWarps = 4;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kATileBytes = kGemmHalfM * kGemmBK * 2;   // 16 KB
+constexpr int kBTileBytes = kGemmHalfN * kGemmBK * 2;   // 16 KB (bf16, swizzled)
+constexpr int kB8TileBytes = kGemmHalfN * kGemmBK;      // 8 KB (int8 staging, dense rows of 64 B)
+constexpr uint32_t kTmemCols = 2 * kGemmBN;              // two fp32 accumulators of 128 x 256 per CTA
 constexpr uint32_t kGemmIdesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+static_assert(kGemmBM == kRowTile, "expert row blocks are whole tiles");
 
 // Per weight type:
-//   bf16: one TMA ring of 4 stages, A 16 KB + B 32 KB each; 6 warps.
-//   int8: a TMA ring of 5 stages, A 16 KB + int8 B 16 KB each, and a ring of 2
-//         converted bf16 B tiles (32 KB each) between the converter warps and
-//         the MMA warp; 14 warps.  The TMA ring stays deep (5 k-blocks of MMA
-//         work in flight) while conversion runs one k-block ahead of the MMA.
+//   bf16: a TMA ring of 6 stages, A 16 KB + B 16 KB each; 6 warps.
+//   int8: a TMA ring of 6 stages, A 16 KB + int8 B 8 KB each, and a ring of 3
+//         converted bf16 B halves (16 KB each) between the converter warps and
+//         the MMA warp; 14 warps.
 template <bool WQ>
 struct GemmCfg {
-  static constexpr int kStages = WQ ? 5 : 4;   // TMA ring
-  static constexpr int kBStages = WQ ? 2 : 0;  // converted-B ring
+  static constexpr int kStages = 6;             // TMA ring
+  static constexpr int kBStages = WQ ? 3 : 0;   // converted-B ring
   static constexpr int kStageBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
-  static constexpr int kThreads = WQ ? 32 * kConvWarp0 + kConvThreads : 192;
+  static constexpr int kThreads = 32 * (kConvWarp0 + (WQ ? kConvWarps : 0));
   // full, empty (TMA ring), bfull, bempty (converted ring), tmem_full x2, tmem_empty x2, drain
   static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 5;
   static constexpr size_t kSmemBytes =
@@ -93,18 +114,18 @@ struct TileCoord {
 };
 
 // Tile t -> (expert, first row, n-block); tiles of expert e are
-// [ (off[e]/128) * n_tiles, (off[e+1]/128) * n_tiles ), m-block fastest.
+// [ (off[e]/256) * n_tiles, (off[e+1]/256) * n_tiles ), m-block fastest.
 __device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExperts + 1], int n_tiles) {
   int e = 0;
 #pragma unroll
   for (int q = 1; q < kNumExperts; ++q)
-    if (t >= (off[q] / kRowTile) * n_tiles) e = q;
-  const int mt = off[e + 1] / kRowTile - off[e] / kRowTile;
-  const int local = t - (off[e] / kRowTile) * n_tiles;
+    if (t >= (off[q] / kGemmBM) * n_tiles) e = q;
+  const int mt = off[e + 1] / kGemmBM - off[e] / kGemmBM;
+  const int local = t - (off[e] / kGemmBM) * n_tiles;
   TileCoord c;
   c.e = e;
   c.n_blk = local / mt;
-  c.row0 = off[e] + (local % mt) * kRowTile;
+  c.row0 = off[e] + (local % mt) * kGemmBM;
   return c;
 }
 
@@ -134,14 +155,16 @@ __device__ __forceinline__ void load_scales8(const uint16_t* p, float (&s)[8]) {
 }
 
 template <int EPI, bool WQ>
-__global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const GemmParams p) {
   using C = GemmCfg<WQ>;
   extern __shared__ uint8_t smem_raw[];
+  // The layout depends only on compile-time sizes, so the offsets are the same
+  // in both CTAs of the pair (the MMA relies on that).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // bf16: sA [4][128 x 64] | sB [4][256 x 64]                (bf16, 128-byte swizzle)
-  // int8: sA [5][128 x 64] | sB8 [5][256 x 64] int8 staging | sB [2][256 x 64] bf16
+  // sA [6][128 x 64] bf16 | sB [6][128 x 64] bf16                      (bf16 weights)
+  // sA [6][128 x 64] bf16 | sB8 [6][128 x 64] int8 | sB [3][128 x 64] bf16  (int8 weights)
   uint8_t* sA = smem;
   uint8_t* sB8 = sA + C::kStages * kATileBytes;
   uint8_t* sB = WQ ? sB8 + C::kStages * kB8TileBytes : sA + C::kStages * kATileBytes;
@@ -159,25 +182,30 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
   const uint32_t drain_bar = bar_t + 8u * 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its partner
+  const bool leader = rank == 0;
+  const int pair = (int)cluster_id_x(), num_pairs = (int)num_clusters_x();
 
   int off[kNumExperts + 1];
 #pragma unroll
   for (int q = 0; q <= kNumExperts; ++q) off[q] = p.sched[kNumExperts + q];
-  const int num_tiles = (off[kNumExperts] / kRowTile) * p.n_tiles;
+  const int num_tiles = (off[kNumExperts] / kGemmBM) * p.n_tiles;
   const int kb_count = p.K / kGemmBK;
 
   if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < (uint32_t)C::kStages; ++s) {
-      mbar_init(full_bar(s), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      // bf16: the even CTA's stage is full when its own copies landed and the
+      // odd CTA forwarded the completion of its copies
+      mbar_init(full_bar(s), (!WQ && leader) ? 2 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int j = 0; j < C::kBStages; ++j) {
-      mbar_init(bfull_bar(j), kConvThreads);
+      mbar_init(bfull_bar(j), 2);  // one arrival per CTA (after all its converter warps)
       mbar_init(bempty_bar(j), 1);
     }
-    for (uint32_t a = 0; a < 2; ++a) {
+    for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads);
+      mbar_init(tempty_bar(a), 2 * kEpiWarps);  // one arrival per epilogue warp of either CTA
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -189,11 +217,11 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
     if (EPI == kEpiGeglu) tma_prefetch_desc(&tm_b1);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -205,8 +233,14 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
 #pragma unroll
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
         const TileCoord tc = decode_tile(t, off, p.n_tiles);
+        const int arow = tc.row0 + (int)rank * kGemmHalfM;
+        // this CTA's 128 rows of B: W (even) or Wv (odd) for the up projection,
+        // the first or second 128 output rows of W1 for the down projection
+        const int brow = (EPI == kEpiGeglu) ? tc.e * p.b_rows_per_expert + tc.n_blk * kGemmHalfN
+                                            : tc.e * p.b_rows_per_expert + tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
+        const CUtensorMap* bmap = (EPI == kEpiGeglu && !leader) ? &tm_b1 : &tm_b0;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             ok = false;
@@ -214,19 +248,9 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, C::kStageBytes);
-          const uint32_t a_dst = smem_addr(sA + stage * kATileBytes);
-          // bf16 weights land in the MMA's B buffer; int8 weights in the staging buffer
-          const uint32_t b_dst = smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes);
-          const int b_half = WQ ? kB8TileBytes / 2 : kBTileBytes / 2;
-          tma_load_2d(a_dst, &tm_a, fb, kb * kGemmBK, tc.row0);
-          if (EPI == kEpiGeglu) {
-            const int brow = tc.e * p.b_rows_per_expert + tc.n_blk * (kGemmBN / 2);
-            tma_load_2d(b_dst, &tm_b0, fb, kb * kGemmBK, brow);
-            tma_load_2d(b_dst + b_half, &tm_b1, fb, kb * kGemmBK, brow);
-          } else {
-            const int brow = tc.e * p.b_rows_per_expert + tc.n_blk * kGemmBN;
-            tma_load_2d(b_dst, &tm_b0, fb, kb * kGemmBK, brow);
-          }
+          tma_load_2d(smem_addr(sA + stage * kATileBytes), &tm_a, fb, kb * kGemmBK, arow);
+          tma_load_2d(smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes), bmap, fb, kb * kGemmBK,
+                      brow);
           for (int s = 0; s < C::kStages; ++s)
             if (s == (int)stage) issued[s] = (int)phase;
           if (++stage == (uint32_t)C::kStages) {
@@ -246,25 +270,28 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
       if (!ok) {
         raise_abort(abort_flag, p.err);
         // this role's copies still in flight complete before the CTA exits
+        // (each one completes the phase of this CTA's own full barrier it was
+        // issued for; the even CTA's barrier also needs the odd CTA's arrival,
+        // which the bounded wait gives up on)
         for (int s = 0; s < C::kStages; ++s)
           if (issued[s] >= 0) wait_bounded(full_bar(s), (uint32_t)issued[s], nullptr, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (leader && lane == 0) {
+      // --------------------------------------------------- MMA issuer (even CTA)
       uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        if (!wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kGemmBN;
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
-              (WQ && !wait_bounded(bfull_bar(bstage), bphase, abort_flag, p.timeout_ns))) {
+          if (!wait_bounded_cluster(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
+              (WQ && !wait_bounded_cluster(bfull_bar(bstage), bphase, abort_flag, p.timeout_ns))) {
             ok = false;
             break;
           }
@@ -273,14 +300,14 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
           const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sB + (WQ ? bstage : stage) * kBTileBytes));
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
-            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kGemmIdesc, (kb | kk) != 0);
-          umma_commit(empty_bar(stage));
+            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kGemmIdesc, (kb | kk) != 0);
+          umma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == (uint32_t)C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
           if (WQ) {
-            umma_commit(bempty_bar(bstage));
+            umma_commit_pair(bempty_bar(bstage), 0x3);
             if (++bstage == (uint32_t)C::kBStages) {
               bstage = 0;
               bphase ^= 1u;
@@ -288,20 +315,43 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        umma_commit_pair(tfull_bar(acc), 0x3);  // both CTAs' epilogues may read
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // all MMAs issued by this thread are complete before TMEM is freed
-      umma_commit(drain_bar);
+      umma_commit_pair(drain_bar, 0x1);
       if (!wait_bounded(drain_bar, 0, nullptr, p.timeout_ns)) ok = false;
       if (!ok) raise_abort(abort_flag, p.err);
+    } else if (!WQ && !leader && lane == 0) {
+      // ------------------------- odd CTA, bf16: forward its stage completions
+      // The MMA of the even CTA reads this CTA's A and B halves; it may start a
+      // k-block once this CTA's copies of it have landed.
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        for (int kb = 0; kb < kb_count; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          // The copies were made by this CTA's TMA and are complete (the local
+          // phase completed); this thread wrote nothing, so a relaxed arrival
+          // is enough and avoids a cluster-scope release per k-block.
+          mbar_arrive_cluster_relaxed(map_to_cta(full_bar(stage), 0));
+          if (++stage == (uint32_t)C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort_flag, p.err);
     }
-  } else if (warp < kConvWarp0) {
+  } else if (warp < kEpiWarp0 + kEpiWarps) {
     // --------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are reachable from this warp
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int t = pair; t < num_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile(t, off, p.n_tiles);
       bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
@@ -310,16 +360,16 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const int row = tc.row0 + q * 32 + lane;
+      const int row = tc.row0 + (int)rank * kGemmHalfM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kGemmBN;
       if (EPI == kEpiGeglu) {
-        const int n0 = tc.n_blk * (kGemmBN / 2);
+        const int n0 = tc.n_blk * kGemmHalfN;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.n_out + n0;
 #pragma unroll 1
-        for (int c = 0; c < kGemmBN / 2 / 32; ++c) {
+        for (int c = 0; c < kGemmHalfN / 32; ++c) {
           uint32_t h[32], v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, h);
-          tmem_ld_32x32b_x32(tbase + kGemmBN / 2 + c * 32, v);
+          tmem_ld_32x32b_x32(tbase + kGemmHalfN + c * 32, v);
           tmem_ld_wait();
           if (WQ) {  // per-output-channel scales of W and Wv (same for every row)
             const size_t so = (size_t)tc.e * p.n_out + n0 + c * 32;
@@ -377,42 +427,64 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
                                  __uint_as_float(y[4 * k + 3]) * sc[4 * k + 3]);
         }
       }
+      // this warp's TMEM reads are complete: free the accumulator for the MMA warp
       tc_fence_before_sync();
-      mbar_arrive(tempty_bar(acc));
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(tempty_bar(acc));
+        else
+          mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
   } else if (WQ) {
     // -------------------------------------------------- int8 -> bf16 converter
-    // Staging tile: 256 rows x 64 int8, row r at byte 64 r.  MMA tile: 256 rows x
+    // Staging tile: 128 rows x 64 int8, row r at byte 64 r.  MMA tile: 128 rows x
     // 64 bf16 in 128-byte swizzle atoms of 8 rows: element (r, k) at
     // (r / 8) * 1024 + (r % 8) * 128 + ((k / 8) ^ (r % 8)) * 16 + (k % 8) * 2.
     const int ct = threadIdx.x - kConvWarp0 * 32;
     uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
       for (int kb = 0; kb < kb_count; ++kb) {
-        ok = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
-                                         wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag, p.timeout_ns));
-        if (!ok) break;
-        const uint8_t* src = sB8 + stage * kB8TileBytes;
-        uint8_t* dst = sB + bstage * kBTileBytes;
+        const bool got = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
+                                                     wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag,
+                                                                  p.timeout_ns));
+        if (got) {
+          const uint8_t* src = sB8 + stage * kB8TileBytes;
+          uint8_t* dst = sB + bstage * kBTileBytes;
 #pragma unroll
-        for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
-          const int u = ct + i * kConvThreads;  // 16-byte unit: row u / 4, int8 columns [16 (u % 4), +16)
-          const int r = u >> 2, c = u & 3;
-          const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
-          uint4 o0, o1;
-          i8x4_to_bf16x4(qv.x, o0.x, o0.y);
-          i8x4_to_bf16x4(qv.y, o0.z, o0.w);
-          i8x4_to_bf16x4(qv.z, o1.x, o1.y);
-          i8x4_to_bf16x4(qv.w, o1.z, o1.w);
-          uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
-          *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = o0;
-          *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+          for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
+            const int u = ct + i * kConvThreads;  // 16-byte unit: row u / 4, int8 columns [16 (u % 4), +16)
+            const int r = u >> 2, c = u & 3;
+            const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
+            uint4 o0, o1;
+            i8x4_to_bf16x4(qv.x, o0.x, o0.y);
+            i8x4_to_bf16x4(qv.y, o0.z, o0.w);
+            i8x4_to_bf16x4(qv.z, o1.x, o1.y);
+            i8x4_to_bf16x4(qv.w, o1.z, o1.w);
+            uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
+            *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
         }
-        fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
-        mbar_arrive(bfull_bar(bstage));
+        // Every converter warp of this CTA reaches this barrier each k-block and
+        // they leave the loop together (a warp that gave up waiting makes all
+        // give up).  After it every converted row of the buffer is written and
+        // fenced for the async proxy; one thread tells the even CTA's MMA warp.
+        // The odd CTA's arrival is relaxed: a cluster-scope release costs about
+        // a microsecond per k-block, and the barrier already ordered the writes.
+        ok = named_bar_and(1, kConvThreads, got);
+        if (!ok) break;
+        if (threadIdx.x == kConvWarp0 * 32) {
+          if (leader)
+            mbar_arrive(bfull_bar(bstage));
+          else
+            mbar_arrive_cluster_relaxed(map_to_cta(bfull_bar(bstage), 0));
+        }
         if (++stage == (uint32_t)C::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -423,14 +495,24 @@ __global__ void __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
         }
       }
     }
+    // every release of a converted buffer by the MMA issuer has landed before exit
+    for (int i = 0; i < C::kBStages && ok; ++i) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag, p.timeout_ns));
+      if (++bstage == (uint32_t)C::kBStages) {
+        bstage = 0;
+        bphase ^= 1u;
+      }
+    }
     if (!ok && lane == 0) raise_abort(abort_flag, p.err);
   }
 
+  // Both CTAs are done with each other's shared memory and barriers, and every
+  // TMEM read of either epilogue is complete, before TMEM is freed and the CTAs exit.
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 

@@ -140,6 +140,7 @@ struct moe_layer {
   moe_weights_t w{};
   int device = 0;
   int num_sms = 0;
+  int gemm_grid[2][2] = {};  // [epilogue][int8]: CTAs of a grouped GEMM launch (whole resident pairs)
   int64_t rows_cap = 0;
 
   void* ws = nullptr;
@@ -157,8 +158,8 @@ struct moe_layer {
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
 
-  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1{};
-  CUtensorMap tm_xn_perm16{}, tm_act16{}, tm_w1_128{};  // decode path boxes
+  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1_128{};  // boxes of 128 rows x 64
+  CUtensorMap tm_xn_perm16{}, tm_act16{};                             // decode path: 16-row boxes
   CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes)
 
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
@@ -174,6 +175,21 @@ struct moe_layer {
 };
 
 namespace {
+
+// CTAs of a persistent cluster launch of `kernel`: 2 x the clusters of 2 CTAs
+// that can be resident at once, capped at one CTA per SM.
+moe_status_t gemm_pairs(moe_layer* L, const void* kernel, int threads, size_t smem, int* grid) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(2 * (L->num_sms / 2), 1, 1);
+  lc.blockDim = dim3(threads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  int clusters = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &lc);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+  if (clusters < 1) return fail(MOE_ERR_UNSUPPORTED, "no CTA pair of the grouped GEMM fits on this device");
+  *grid = 2 * std::min(clusters, L->num_sms / 2);
+  return MOE_OK;
+}
 
 void harvest(moe_layer* L, int slot) {
   if (!L->pending[slot]) return;
@@ -238,7 +254,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     GemmParams p{};
     p.sched = L->sched;
     p.K = d;
-    p.n_tiles = F / (kGemmBN / 2);
+    p.n_tiles = F / kGemmHalfN;
     p.b_rows_per_expert = F;
     p.n_out = F;
     p.out = L->act;
@@ -248,11 +264,12 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     if (int8)
-      grouped_gemm_kernel<kEpiGeglu, true><<<L->num_sms, GemmCfg<true>::kThreads, GemmCfg<true>::kSmemBytes, st>>>(
+      grouped_gemm_kernel<kEpiGeglu, true><<<L->gemm_grid[kEpiGeglu][1], GemmCfg<true>::kThreads,
+                                             GemmCfg<true>::kSmemBytes, st>>>(
           L->tm_xn_perm, L->tm_w8, L->tm_wv8, p);
     else
-      grouped_gemm_kernel<kEpiGeglu, false><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_xn_perm,
-                                                                                             L->tm_w, L->tm_wv, p);
+      grouped_gemm_kernel<kEpiGeglu, false><<<L->gemm_grid[kEpiGeglu][0], kGemmThreads, kGemmSmemBytes, st>>>(
+          L->tm_xn_perm, L->tm_w, L->tm_wv, p);
   }
   mark(4);
   if (decode) {
@@ -282,11 +299,11 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     if (int8)
-      grouped_gemm_kernel<kEpiDown, true><<<L->num_sms, GemmCfg<true>::kThreads, GemmCfg<true>::kSmemBytes, st>>>(
-          L->tm_act, L->tm_w18, L->tm_w18, p);
+      grouped_gemm_kernel<kEpiDown, true><<<L->gemm_grid[kEpiDown][1], GemmCfg<true>::kThreads,
+                                            GemmCfg<true>::kSmemBytes, st>>>(L->tm_act, L->tm_w18, L->tm_w18, p);
     else
-      grouped_gemm_kernel<kEpiDown, false><<<L->num_sms, kGemmThreads, kGemmSmemBytes, st>>>(L->tm_act, L->tm_w1,
-                                                                                            L->tm_w1, p);
+      grouped_gemm_kernel<kEpiDown, false><<<L->gemm_grid[kEpiDown][0], kGemmThreads, kGemmSmemBytes, st>>>(
+          L->tm_act, L->tm_w1_128, L->tm_w1_128, p);
   }
   mark(5);
   if (decode)
@@ -412,17 +429,17 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   while (L->ksplit > 1 && (F / kDecBK) % L->ksplit) L->ksplit /= 2;
   moe_status_t s = MOE_OK;
   if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmBM);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmBM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmHalfM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmHalfM);
   if (c.weight_dtype == MOE_WEIGHT_BF16) {
-    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmBN / 2);
-    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmBN / 2);
-    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1, w->w1, F, kNumExperts * d, kGemmBN);
-    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kDecBM);
+    static_assert(kGemmHalfN == kDecBM, "the GEMM and decode paths share the 128-row weight boxes");
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmHalfN);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmHalfN);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kGemmHalfN);
   } else {
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmBN / 2);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmBN / 2);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmBN);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmHalfN);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmHalfN);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmHalfN);
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
@@ -450,6 +467,16 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
       cudaFuncSetAttribute(decode_gemm_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)DecCfg<kEpiDown>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (decode down) failed");
+  // Grouped GEMMs run one CTA pair per two SMs, persistent: launch as many
+  // pairs as can be resident at once (whole clusters only), at most one per SM pair.
+  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, false>, kGemmThreads,
+                                  kGemmSmemBytes, &L->gemm_grid[kEpiGeglu][0]);
+  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, false>, kGemmThreads,
+                                  kGemmSmemBytes, &L->gemm_grid[kEpiDown][0]);
+  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, true>, GemmCfg<true>::kThreads,
+                                  GemmCfg<true>::kSmemBytes, &L->gemm_grid[kEpiGeglu][1]);
+  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, true>, GemmCfg<true>::kThreads,
+                                  GemmCfg<true>::kSmemBytes, &L->gemm_grid[kEpiDown][1]);
   if (s == MOE_OK) {
     L->ring.resize(kProfRing);
     L->pending.assign(kProfRing, false);
@@ -570,6 +597,15 @@ moe_status_t moe_layer_profile_read(moe_layer_t* L, double* ms_total, int64_t* l
       L->prof_ms[k] = 0.0;
       L->prof_n[k] = 0;
     }
+  return ok();
+}
+
+moe_status_t moe_layer_gemm_grid(const moe_layer_t* L, int32_t grid[4]) {
+  if (!L || !grid) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  grid[0] = L->gemm_grid[kEpiGeglu][0];
+  grid[1] = L->gemm_grid[kEpiDown][0];
+  grid[2] = L->gemm_grid[kEpiGeglu][1];
+  grid[3] = L->gemm_grid[kEpiDown][1];
   return ok();
 }
 

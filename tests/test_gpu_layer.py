@@ -155,7 +155,7 @@ def test_intermediates_match_oracle():
     r = oracle.route(inp, keep_xn=True)
     np.testing.assert_allclose(xn, r.xn, rtol=2 ** -8, atol=1e-6)
     np.testing.assert_array_equal(counts, np.bincount(r.idx.ravel(), minlength=8))
-    assert np.all(off % 128 == 0) and np.all(np.diff(off) >= counts)
+    assert np.all(off % 256 == 0) and np.all(np.diff(off) >= counts)
     for t in (0, 17, T - 1):
         for rank in range(2):
             e = int(r.idx[t, rank])
