@@ -45,7 +45,10 @@ def kernel_function(role, inp):
     int8 = inp.weight_dtype == "int8"
     if role in ("up_geglu", "down"):
         epi = 0 if role == "up_geglu" else 1
-        if inp.T <= DECODE_MAX_T and not int8:
+        if inp.T <= DECODE_MAX_T and int8:
+            return f"decode_gemm_i8_kernel<{epi}>", ["k_decode_i8.cuh", "k_decode.cuh", "k_gemm.cuh", "ptx.cuh",
+                                                     "ptx_pair.cuh", "ptx_tmem.cuh", "common.cuh"]
+        if inp.T <= DECODE_MAX_T:
             return f"decode_gemm_kernel<{epi}>", ["k_decode.cuh", "ptx.cuh", "common.cuh"]
         return f"grouped_gemm_kernel<{epi}, {int(int8)}>", ["k_gemm.cuh", "ptx.cuh", "common.cuh"]
     src = {"router": "k_router.cuh", "permute": "k_permute.cuh", "gather": "k_permute.cuh",
@@ -76,15 +79,21 @@ def peaks():
 #   profile_small        T=2048, F=4096, bf16 weights (1.2 GB)
 #   profile_small_int8   T=2048, F=4096, int8 weights (0.6 GB) + bf16 scales
 #   profile_decode_small T=8,    F=8192, bf16 weights (2.4 GB), the decode kernels
+#   profile_decode_small_int8   the same with int8 weights (1.2 GB)
 PROFILE_CASES = {
     "profile_small": dict(T=2048, d=6144, F=4096, seed=2000, weight_dtype="bf16"),
     "profile_small_int8": dict(T=2048, d=6144, F=4096, seed=2001, weight_dtype="int8"),
     "profile_decode_small": dict(T=8, d=6144, F=8192, seed=2002, weight_dtype="bf16"),
+    "profile_decode_small_int8": dict(T=8, d=6144, F=8192, seed=2003, weight_dtype="int8"),
 }
 
 
 def make_workload(name):
     import synth
+    if name == "int8_decode":  # the int8 workload's weights with its first 8 tokens
+        inp = synth.workload("int8", T=8)
+        inp.name = name
+        return inp
     if name in PROFILE_CASES:
         c = PROFILE_CASES[name]
         return synth.make_inputs(c["T"], c["d"], c["F"], c["seed"], name=name, weight_dtype=c["weight_dtype"])
@@ -142,7 +151,7 @@ def compulsory_bytes(role, inp, counts):
     d, F = inp.d, inp.F
     wb = 1 if inp.weight_dtype == "int8" else 2
     n_act = int(sum(1 for c in counts if c > 0))
-    if inp.T <= DECODE_MAX_T and inp.weight_dtype == "bf16":
+    if inp.T <= DECODE_MAX_T:
         rows = 2 * inp.T
     else:
         rows = int(sum((c + 255) // 256 * 256 for c in counts))
@@ -450,7 +459,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["prefill", "decode", "skew", "int8", "tiny", *PROFILE_CASES],
+                    choices=["prefill", "decode", "skew", "int8", "int8_decode", "tiny", *PROFILE_CASES],
                     help="prefill (T=8192) is the headline workload")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")

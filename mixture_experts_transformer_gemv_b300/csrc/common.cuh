@@ -1,6 +1,7 @@
 // Shared constants and small helpers of the MoE layer kernels.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace moe {
@@ -36,6 +37,20 @@ __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two bf16 (low, high halves) -> two fp16, round to nearest.
+__device__ __forceinline__ uint32_t f16x2_from_bf16x2(uint32_t u) {
+  __half2 h = __floats2half2_rn(bf16_lo(u), bf16_hi(u));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two fp32 -> two fp16 (lo in the low half), round to nearest, saturating to
+// +-65504 instead of overflowing to infinity.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {

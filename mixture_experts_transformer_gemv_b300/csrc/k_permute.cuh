@@ -112,9 +112,12 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
 
 // xn_perm[row] = xn[token_of_row[row]] (zeros for padding rows); rows beyond
 // row_offset[E] are left alone.  Grid-stride over rows, 16-byte accesses.
+// to_f16 != 0 (int8 weight-streaming path) stores the rows as fp16 instead of
+// bf16: every bf16 value of a normed row converts exactly unless it is below
+// the fp16 normal range (|v| < 2^-14), where the error is under 2^-24.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ xn,
                                                           const int32_t* __restrict__ token_of_row,
-                                                          const int32_t* __restrict__ sched, int d,
+                                                          const int32_t* __restrict__ sched, int d, int to_f16,
                                                           __nv_bfloat16* __restrict__ xn_perm) {
   const int rows = sched[2 * kNumExperts];
   const int nchunk = d >> 3;
@@ -123,7 +126,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
     uint4* dst = reinterpret_cast<uint4*>(xn_perm + (size_t)row * d);
     if (tok >= 0) {
       const uint4* src = reinterpret_cast<const uint4*>(xn + (size_t)tok * d);
-      for (int c = threadIdx.x; c < nchunk; c += blockDim.x) dst[c] = src[c];
+      for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+        uint4 v = src[c];
+        if (to_f16) {
+          v.x = f16x2_from_bf16x2(v.x);
+          v.y = f16x2_from_bf16x2(v.y);
+          v.z = f16x2_from_bf16x2(v.z);
+          v.w = f16x2_from_bf16x2(v.w);
+        }
+        dst[c] = v;
+      }
     } else {
       for (int c = threadIdx.x; c < nchunk; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
     }

@@ -10,10 +10,10 @@
 //   K3 grouped_gemm<geglu>  act = GELU(A W^T) * (A Wv^T)        (tcgen05)
 //   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
 //   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
-// For T <= 16 (or MOE_FLAG_FORCE_GEMV) with bf16 weights K3/K4 are replaced by the
-// weight-streaming decode kernels (k_decode.cuh) and K5 sums their split-K
-// partials.  int8 weights always take the grouped GEMMs (int8 -> bf16 in shared
-// memory, per-channel scale in the epilogue).
+// For T <= 16 (or MOE_FLAG_FORCE_GEMV) K3/K4 are replaced by the weight-streaming
+// decode kernels (k_decode.cuh for bf16 weights, k_decode_i8.cuh for int8) and K5
+// sums their split-K partials.  int8 weights are converted to bf16 on chip and
+// their per-channel scales applied in the epilogues.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "k_combine.cuh"
 #include "k_decode.cuh"
+#include "k_decode_i8.cuh"
 #include "k_gemm.cuh"
 #include "k_permute.cuh"
 #include "k_router.cuh"
@@ -112,17 +113,20 @@ moe_status_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, ui
   return MOE_OK;
 }
 
-// Row-major 2-D int8 tensor [rows, inner], box [box_rows, 64] (64-byte rows, no
-// swizzle): the staging layout the int8 -> bf16 converter warps read.
-moe_status_t make_tmap_i8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+// Row-major 2-D int8 tensor [rows, inner], box [box_rows, box_inner]: the staging
+// layout the int8 converter warps read; 64-byte rows without swizzle for the
+// grouped GEMMs (threads read along rows), 128-byte rows with 128-byte swizzle
+// for the decode kernels (each thread reads one row).
+moe_status_t make_tmap_i8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                          uint32_t box_inner, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn enc = get_encoder();
   if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), box_rows};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (int8) failed (%d)", (int)r);
   return MOE_OK;
@@ -157,10 +161,12 @@ struct moe_layer {
   float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
+  int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
   CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1_128{};  // boxes of 128 rows x 64
   CUtensorMap tm_xn_perm16{}, tm_act16{};                             // decode path: 16-row boxes
   CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes)
+  CUtensorMap tm_w8d{}, tm_wv8d{}, tm_w18d{};           // int8 weights, 64-byte swizzle (decode)
 
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
   size_t host_stage_bytes = 0;
@@ -221,6 +227,8 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     if (ev) cudaEventRecord(ev[k], st);
   };
 
+  const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
+  const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) || (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
   mark(0);
   router_kernel<<<(T + kRouterTok - 1) / kRouterTok, kRouterThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
@@ -231,13 +239,28 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   mark(2);
   {
     const int grid = (int)std::min<int64_t>(L->rows_cap, (int64_t)L->num_sms * 8);
-    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, L->xn_perm);
+    // the int8 weight-streaming kernels multiply in fp16 (int8 -> fp16 is one
+    // shuffle and one subtraction), so their activation rows are fp16
+    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, decode && int8 ? 1 : 0,
+                                             L->xn_perm);
   }
   mark(3);
-  const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
-  const bool decode = !int8 && ((L->cfg.flags & MOE_FLAG_FORCE_GEMV) ||
-                                (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS));
-  if (decode) {
+  if (decode && int8) {
+    DecI8Params p{};
+    p.sched = L->sched;
+    p.K = d;
+    p.rows_per_expert = F;
+    p.n_out = F;
+    p.ksplit = 1;
+    p.out = L->act;
+    p.row_scale = nullptr;
+    p.scale0 = L->w.w_scale;
+    p.scale1 = L->w.wv_scale;
+    p.err = L->err;
+    p.timeout_ns = kWaitLimitNs;
+    decode_gemm_i8_kernel<kEpiGeglu><<<L->num_sms, DecI8Cfg<kEpiGeglu>::kThreads, DecI8Cfg<kEpiGeglu>::kSmemBytes,
+                                       st>>>(L->tm_w8d, L->tm_wv8d, L->tm_xn_perm16, p);
+  } else if (decode) {
     DecParams p{};
     p.sched = L->sched;
     p.K = d;
@@ -272,7 +295,22 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
           L->tm_xn_perm, L->tm_w, L->tm_wv, p);
   }
   mark(4);
-  if (decode) {
+  if (decode && int8) {
+    DecI8Params p{};
+    p.sched = L->sched;
+    p.K = F;
+    p.rows_per_expert = d;
+    p.n_out = d;
+    p.ksplit = L->ksplit_i8;
+    p.out = L->part;
+    p.row_scale = L->prob_of_row;
+    p.scale0 = L->w.w1_scale;
+    p.scale1 = nullptr;
+    p.err = L->err;
+    p.timeout_ns = kWaitLimitNs;
+    decode_gemm_i8_kernel<kEpiDown><<<L->num_sms, DecI8Cfg<kEpiDown>::kThreads, DecI8Cfg<kEpiDown>::kSmemBytes,
+                                      st>>>(L->tm_w18d, L->tm_w18d, L->tm_act16, p);
+  } else if (decode) {
     DecParams p{};
     p.sched = L->sched;
     p.K = F;
@@ -308,7 +346,8 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   mark(5);
   if (decode)
     combine_kernel<true><<<T, kCombineThreads, 0, st>>>(
-        L->part, L->row_of_slot, L->idx, L->sched, L->ksplit, static_cast<const __nv_bfloat16*>(hidden),
+        L->part, L->row_of_slot, L->idx, L->sched, int8 ? L->ksplit_i8 : L->ksplit,
+        static_cast<const __nv_bfloat16*>(hidden),
         L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks, L->err, static_cast<__nv_bfloat16*>(out));
   else
     combine_kernel<false><<<T, kCombineThreads, 0, st>>>(
@@ -357,8 +396,6 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (!(c.eps > 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be > 0");
   if (c.weight_dtype != MOE_WEIGHT_BF16 && c.weight_dtype != MOE_WEIGHT_INT8)
     return fail(MOE_ERR_INVALID_ARG, "unknown weight_dtype %d", c.weight_dtype);
-  if ((c.flags & MOE_FLAG_FORCE_GEMV) && c.weight_dtype == MOE_WEIGHT_INT8)
-    return fail(MOE_ERR_UNSUPPORTED, "MOE_FLAG_FORCE_GEMV: the weight-streaming path takes bf16 weights only");
   if ((c.flags & MOE_FLAG_FORCE_GEMV) && (c.flags & MOE_FLAG_FORCE_TC))
     return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_FORCE_GEMV and MOE_FLAG_FORCE_TC are exclusive");
   const void* req[] = {w->gate, w->w, w->wv, w->w1, w->pre_norm_scale, w->post_norm_scale};
@@ -380,7 +417,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
   const size_t smem_need =
       std::max(std::max(kGemmSmemBytes, GemmCfg<true>::kSmemBytes),
-               std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes));
+               std::max(std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes),
+                        std::max(DecI8Cfg<kEpiGeglu>::kSmemBytes, DecI8Cfg<kEpiDown>::kSmemBytes)));
   if (prop.sharedMemPerBlockOptin < smem_need)
     return fail(MOE_ERR_UNSUPPORTED, "device offers %zu B shared memory per block, need %zu",
                 (size_t)prop.sharedMemPerBlockOptin, smem_need);
@@ -427,6 +465,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   // decode-path split of the F reduction: up to kDecMaxSplit chunks of whole 64-wide blocks
   L->ksplit = kDecMaxSplit;
   while (L->ksplit > 1 && (F / kDecBK) % L->ksplit) L->ksplit /= 2;
+  L->ksplit_i8 = kDecMaxSplit;
+  while (L->ksplit_i8 > 1 && (F / kDq8BK) % L->ksplit_i8) L->ksplit_i8 /= 2;
   moe_status_t s = MOE_OK;
   if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmHalfM);
@@ -437,9 +477,14 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmHalfN);
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kGemmHalfN);
   } else {
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmHalfN);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmHalfN);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmHalfN);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8d, w->w, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == MOE_OK)
+      s = make_tmap_i8(&L->tm_wv8d, w->wv, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == MOE_OK)
+      s = make_tmap_i8(&L->tm_w18d, w->w1, F, kNumExperts * d, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
@@ -467,6 +512,14 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
       cudaFuncSetAttribute(decode_gemm_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)DecCfg<kEpiDown>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (decode down) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(decode_gemm_i8_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)DecI8Cfg<kEpiGeglu>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 decode up) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(decode_gemm_i8_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)DecI8Cfg<kEpiDown>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 decode down) failed");
   // Grouped GEMMs run one CTA pair per two SMs, persistent: launch as many
   // pairs as can be resident at once (whole clusters only), at most one per SM pair.
   if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, false>, kGemmThreads,

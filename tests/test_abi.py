@@ -75,7 +75,7 @@ def _create(lib, cfg, w):
     (dict(eps=0.0), moe.MOE_ERR_INVALID_ARG),
     (dict(weight_dtype=7), moe.MOE_ERR_INVALID_ARG),
     (dict(weight_dtype=1), moe.MOE_ERR_INVALID_ARG),  # int8 weights without their scales
-    (dict(weight_dtype=1, flags=moe.MOE_FLAG_FORCE_GEMV), moe.MOE_ERR_UNSUPPORTED),
+    (dict(weight_dtype=1, flags=moe.MOE_FLAG_FORCE_GEMV), moe.MOE_ERR_INVALID_ARG),  # no scales
     (dict(flags=moe.MOE_FLAG_FORCE_GEMV | moe.MOE_FLAG_FORCE_TC), moe.MOE_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_config(lib, kw, status):

@@ -54,3 +54,21 @@ def test_skew_shares_reported(grok):
     # the stated bias makes expert 0 the most frequent first choice and expert 7 the rarest
     assert first[0] == first.max() and first[7] == first.min()
     print("skew first-choice shares", np.round(first, 4).tolist(), "slots", list(grok["counts"]))
+
+
+def test_int8_decode_full_shape():
+    """int8 weights at the Grok-1 shape with T = 8 (the int8 workload's first 8
+    tokens): the int8 weight-streaming kernels against the oracle on every token."""
+    from mixture_experts_transformer_gemv_b300 import build
+    build.build()
+    inp = synth.workload("int8", T=8)
+    weights = device_weights(inp)
+    layer = make_layer(inp, weights=weights)
+    y, idx, prob, counts = run(layer, inp)
+    ref = oracle.moe_tokens(inp)
+    assert_routing(idx, prob, counts, ref, "int8 decode")
+    rep = assert_values(y, ref.y, "int8 decode")
+    print("int8 decode T=8 values", rep)
+    layer.close()
+    del weights
+    torch.cuda.empty_cache()

@@ -227,11 +227,39 @@ def test_decode_and_tensor_core_paths_agree_on_one_expert_heavy_batch():
 @pytest.mark.parametrize("T,d,F,seed", [
     (300, 512, 1024, 71),    # several up and down tiles, ragged row blocks
     (200, 384, 640, 72),     # ragged d (half a down tile) and F/128 = 5
-    (9, 256, 512, 73),       # T <= 16: int8 weights take the tensor-core path
 ])
 def test_int8_weights(T, d, F, seed):
     inp = synth.make_inputs(T, d, F, seed, name=f"int8_{T}x{d}x{F}", weight_dtype="int8")
     _full_check(inp)
+
+
+@pytest.mark.parametrize("T,d,F,seed", [
+    (1, 256, 512, 76),
+    (5, 384, 640, 77),      # ragged: d/128 = 3 weight blocks, F/64 = 10 -> 2-way split
+    (9, 512, 1024, 73),
+    (16, 256, 512, 78),     # the largest T the decode path takes
+])
+@pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_FORCE_TC])
+def test_int8_decode_path_and_forced_tensor_core_path(T, d, F, seed, flags):
+    """int8 weights at T <= 16 run the int8 weight-streaming kernels (weights
+    converted into Tensor Memory) unless the grouped GEMMs are forced."""
+    inp = synth.make_inputs(T, d, F, seed, name=f"int8dec{T}x{d}x{F}", weight_dtype="int8")
+    _full_check(inp, flags=flags)
+
+
+def test_int8_decode_one_expert_heavy_batch():
+    """All 16 tokens to expert 6, int8 weights: decode and grouped-GEMM paths."""
+    inp = synth.make_inputs(16, 384, 640, 79, name="int8dec_onehot", weight_dtype="int8")
+    b = np.zeros(8, np.float32)
+    b[6] = 1e4
+    inp.bias = b
+    ref = oracle.moe_tokens(inp)
+    for flags in (0, moe.MOE_FLAG_FORCE_TC, moe.MOE_FLAG_FORCE_GEMV):
+        layer = make_layer(inp, flags=flags)
+        y, idx, prob, counts = run(layer, inp)
+        assert counts[6] == 16
+        assert_values(y, ref.y, f"int8dec_onehot flags={flags}")
+        layer.close()
 
 
 def test_int8_skewed_and_checks():
@@ -257,4 +285,30 @@ def test_int8_intermediates_match_oracle():
             assert np.max(np.abs(act[row] - a)) <= 0.02 * np.max(np.abs(a)) + 1e-6, (t, rank)
             wo = r.w[t, rank] * o
             assert np.max(np.abs(yr[row] - wo)) <= 0.02 * np.max(np.abs(wo)) + 1e-7, (t, rank)
+    layer.close()
+
+
+@pytest.mark.parametrize("T,weights,flags", [
+    (8, "bf16", 0),                           # weight-streaming decode kernels
+    (8, "int8", 0),                           # int8 weight-streaming decode kernels
+    (200, "bf16", 0),                         # grouped GEMMs on CTA pairs
+    (200, "int8", 0),                         # int8 grouped GEMMs
+    (8, "int8", moe.MOE_FLAG_FORCE_TC),
+])
+def test_back_to_back_forwards_are_deterministic(T, weights, flags):
+    """Forty forwards queued back to back on one stream: no device wait may run
+    out, and every output must equal the first bit for bit (every reduction in
+    the layer has a fixed order).  Races between pipeline roles or between
+    consecutive launches show up here as timeouts or changed bits."""
+    inp = synth.make_inputs(T, 384, 1280, 80, name=f"repeat{T}{weights}", weight_dtype=weights)
+    layer = make_layer(inp, flags=flags)
+    x = bf16_tensor(inp.x)
+    outs = [torch.empty_like(x) for _ in range(40)]
+    for o in outs:
+        layer.forward(x, out=o)
+    torch.cuda.synchronize()
+    layer.sync_status()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert_values(outs[0].float().cpu().numpy().astype(np.float64), oracle.moe_tokens(inp).y, inp.name)
     layer.close()
