@@ -233,6 +233,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest `value` over all ranks (the slowest replica sets the job's
+    step time); `value` itself when not distributed."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world, tokens_per_rank, seconds_per_step):
+    """Token throughput of the whole job: every rank runs its own replica on
+    `tokens_per_rank` tokens per step (weak scaling, no exchange), and the step
+    ends when the slowest rank ends."""
+    return world * tokens_per_rank / seconds_per_step
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import synth
@@ -300,12 +318,8 @@ def run_ours(args, rank, world, local_rank):
     prof = layer.profile_read(reset=True)
     layer.set_profiling(False)
 
-    ms_step = ms_total / args.steps
-    if dist:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * inp.T / (ms_step / 1e3)
+    ms_step = max_over_ranks(ms_total / args.steps, dist, "cuda")
+    value = whole_job_tokens_per_s(world, inp.T, ms_step / 1e3)
 
     # end to end through the host-buffer entry point (pinned memory, copies inside)
     xh = x_host.pin_memory()
@@ -318,12 +332,8 @@ def run_ours(args, rank, world, local_rank):
     t1 = time.perf_counter()
     for _ in range(e2e_steps):
         layer.forward_host(xh, oh)
-    e2e_s = (time.perf_counter() - t1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * inp.T / e2e_s
+    e2e_s = max_over_ranks((time.perf_counter() - t1) / e2e_steps, dist, "cuda")
+    e2e_value = whole_job_tokens_per_s(world, inp.T, e2e_s)
 
     # kernels: average device time per launch, dominant kernel's roofline
     pk, peak_kind = peaks()
@@ -424,13 +434,15 @@ def run_reference(args):
     inp = make_workload(args.workload)
     cores = oracle.max_threads()
     rng_base = 100
-    # each step: routing of a 512-token slice + the full layer on one sampled token
+    # each step: routing of a slice of up to 512 tokens + the full layer on one sampled token
+    n_slice = min(512, inp.T)
+
     def step(i):
-        lo = (i * 512) % inp.T
-        sub = synth.MoeInputs(**{**inp.__dict__, "T": 512, "x": np.ascontiguousarray(inp.x[lo:lo + 512])})
+        lo = (i * n_slice) % (inp.T - n_slice + 1)
+        sub = synth.MoeInputs(**{**inp.__dict__, "T": n_slice, "x": np.ascontiguousarray(inp.x[lo:lo + n_slice])})
         t0 = time.perf_counter()
         oracle.route(sub)
-        tr = (time.perf_counter() - t0) / 512
+        tr = (time.perf_counter() - t0) / n_slice
         t0 = time.perf_counter()
         oracle.moe_tokens(inp, oracle_token_sample(inp, 1, seed=rng_base + i))
         tl = time.perf_counter() - t0
@@ -446,7 +458,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)", "config": config_block(inp),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "per step: routing of a 512-token slice + full layer on one seeded token; "
+                         "sample": f"per step: routing of a {n_slice}-token slice + full layer on one seeded token; "
                                    "fp64 C oracle on the host cores"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
