@@ -12,6 +12,7 @@ marshals numpy arrays into it.
 Functions
 ---------
 route(inp)                       -> Route (xn, p, idx, w) for all T tokens
+routing_stats(p)                 -> mean probability per expert, routing entropy, collapse index
 moe_tokens(inp, tokens)          -> Layer (y, m, idx, w, p) for a token subset
 expert_ffn(inp, xn, e)           -> (h, v, a, o) of one expert on one vector
 dequant(q, scale, scale_E, scale_G) -> fp32 [E, N, K] dequantised weights
@@ -65,6 +66,8 @@ def _load():
         lib.oracle_expert_ffn.restype = None
         lib.oracle_expert_ffn.argtypes = [i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                           vp, vp, vp, vp]
+        lib.oracle_routing_stats.restype = None
+        lib.oracle_routing_stats.argtypes = [i64, i64, vp, vp]
         lib.oracle_moe_tokens.restype = None
         lib.oracle_moe_tokens.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, dbl, i32, vp, vp, vp,
                                           vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
@@ -140,6 +143,17 @@ def route(inp, keep_xn: bool = False) -> Route:
     _load().oracle_route(T, d, E, _p(inp.x), _p(inp.gate), _p(inp.bias), _p(inp.s_pre), inp.eps, _p(xn), _p(p),
                          _p(idx), _p(w))
     return Route(xn, p, idx, w)
+
+
+def routing_stats(p: np.ndarray) -> dict:
+    """Routing diagnostics of router probabilities p [T, E] (float64): the mean
+    probability of each expert, the routing entropy of that mean distribution in
+    nats, and the collapse index 1 - entropy / ln E."""
+    p = np.ascontiguousarray(p, np.float64)
+    T, E = p.shape
+    out = np.empty(E + 2, np.float64)
+    _load().oracle_routing_stats(T, E, _p(p), _p(out))
+    return {"mean_prob": out[:E].copy(), "entropy": float(out[E]), "collapse": float(out[E + 1])}
 
 
 def expert_ffn(inp, xn: np.ndarray, e: int):

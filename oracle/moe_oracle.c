@@ -179,6 +179,28 @@ void oracle_route(int64_t T, int64_t d, int64_t E, const uint16_t* x, const floa
   }
 }
 
+/* Routing diagnostics over T tokens ("Jah-yee/grok" README, list "New metrics
+ * track MoE-specific grokking signals" (routing entropy, collapse index) and the
+ * --demo block "[3] MoE routing (layer 0)", which prints one weight per expert
+ * and the routing entropy against its maximum):
+ *   out[e]     = (1/T) sum_t p[t, e]              mean router probability of expert e
+ *   out[E]     = -sum_e out[e] ln out[e]          routing entropy in nats (max ln E)
+ *   out[E + 1] = 1 - out[E] / ln E                collapse index (reading: 0 uniform,
+ *                                                 1 when one expert takes all)
+ * Terms with out[e] == 0 contribute 0 to the entropy. */
+void oracle_routing_stats(int64_t T, int64_t E, const double* p, double* out) {
+  for (int64_t e = 0; e < E; ++e) {
+    double s = 0.0;
+    for (int64_t t = 0; t < T; ++t) s += p[t * E + e];
+    out[e] = s / (double)T;
+  }
+  double h = 0.0;
+  for (int64_t e = 0; e < E; ++e)
+    if (out[e] > 0.0) h -= out[e] * log(out[e]);
+  out[E] = h;
+  out[E + 1] = 1.0 - h / log((double)E);
+}
+
 /* One GeGLU expert on one token ("Jah-yee/grok" README: GELU(x W) (*) (x Wv),
  * then the output projection; shapes from the model card's weight listing).
  *   h_n = sum_k W[e,n,k] xn_k,  v_n = sum_k Wv[e,n,k] xn_k,  a_n = GELU(h_n) v_n,

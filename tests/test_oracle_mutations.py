@@ -27,6 +27,8 @@ MUTANTS = {
     "gelu_constant": ("0.044715 * u * u * u", "0.0447 * u * u * u"),
     "int8_scale_not_per_expert": ("int64_t es = (W->scale_E > 1) ? e : 0;", "int64_t es = 0;"),
     "bias_sign": ("l[e] = acc + (bias ? (double)bias[e] : 0.0)", "l[e] = acc - (bias ? (double)bias[e] : 0.0)"),
+    "entropy_in_bits": ("if (out[e] > 0.0) h -= out[e] * log(out[e]);", "if (out[e] > 0.0) h -= out[e] * log2(out[e]);"),
+    "stats_sum_not_mean": ("out[e] = s / (double)T;", "out[e] = s;"),
 }
 
 

@@ -121,6 +121,50 @@ def test_uniform_router_matches_page_demo():
     assert np.all(r.w == 0.125)
 
 
+def test_routing_stats_uniform_router_matches_page_demo():
+    """The README demo's untrained router: 0.125 per expert, entropy 2.079 of 2.079."""
+    g = _golden("uniform_router.txt")
+    inp = synth.make_inputs(24, 256, 512, 9, norm_scales="ones")
+    inp.gate[:] = 0.0
+    s = oracle.routing_stats(oracle.route(inp).p)
+    assert np.all(np.round(s["mean_prob"], 3) == g["expert_weight"])
+    assert round(s["entropy"], 3) == g["routing_entropy"] == round(math.log(g["num_experts"]), 3)
+    assert abs(s["entropy"] - math.log(8)) < 1e-12 and abs(s["collapse"]) < 1e-12
+
+
+@pytest.mark.parametrize("hot,entropy", [
+    ((5,), 0.0),                  # one expert takes every token: entropy 0, collapse 1
+    ((2, 6), math.log(2)),        # two experts share every token equally: ln 2
+    ((0, 3, 7, 1), math.log(4)),  # four equal experts: ln 4
+])
+def test_routing_stats_closed_forms(hot, entropy):
+    inp = synth.make_inputs(20, 256, 512, 10, norm_scales="ones")
+    inp.gate[:] = 0.0
+    b = np.full(8, -1e4, np.float32)
+    b[list(hot)] = 0.0
+    inp.bias = b
+    s = oracle.routing_stats(oracle.route(inp).p)
+    expect = np.zeros(8)
+    expect[list(hot)] = 1.0 / len(hot)
+    np.testing.assert_allclose(s["mean_prob"], expect, atol=1e-12)
+    assert abs(s["entropy"] - entropy) < 1e-9
+    assert abs(s["collapse"] - (1.0 - entropy / math.log(8))) < 1e-9
+
+
+def test_routing_stats_invariants():
+    inp = synth.make_inputs(300, 256, 512, 11, bias=synth.SKEW_BIAS)
+    r = oracle.route(inp)
+    s = oracle.routing_stats(r.p)
+    assert abs(s["mean_prob"].sum() - 1.0) < 1e-12
+    assert 0.0 < s["entropy"] < math.log(8)
+    # the skew bias favours expert 0 and disfavours expert 7
+    assert s["mean_prob"].argmax() == 0 and s["mean_prob"].argmin() == 7
+    # token order does not matter
+    perm = np.random.default_rng(3).permutation(inp.T)
+    s2 = oracle.routing_stats(r.p[perm])
+    np.testing.assert_allclose(s2["mean_prob"], s["mean_prob"], rtol=1e-13)
+
+
 @pytest.mark.parametrize("bias,expect", [
     ([0, 0, 0, 5, 0, 5, 0, 0], (3, 5)),
     ([1, 2, 2, 0, 0, 0, 0, 0], (1, 2)),
