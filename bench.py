@@ -291,6 +291,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     layer.sync_status()
     _, _, _, counts = layer.forward(x, out, routing=True)
+    rstats = layer.router_stats().cpu().numpy()
     counts = counts.cpu().numpy()
     torch.cuda.synchronize()
 
@@ -381,6 +382,8 @@ def run_ours(args, rank, world, local_rank):
         "layer_hbm_frac": round(layer_hbm_frac, 4),
         "kernels": kernels,
         "expert_counts": [int(c) for c in counts],
+        "router_stats": {"mean_prob": [round(float(v), 5) for v in rstats[:8]],
+                         "entropy_nats": round(float(rstats[8]), 5), "collapse_index": round(float(rstats[9]), 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(inp.T * inp.d * 2),
                 "d2h_bytes_per_step": int(inp.T * inp.d * 2), "ms_per_step": round(e2e_s * 1e3, 3),
                 "entry_point": "moe_layer_forward_host (pinned host buffers)"},

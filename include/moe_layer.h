@@ -149,6 +149,22 @@ const char* moe_status_string(moe_status_t status);
 /* One-line detail of the last error returned on this thread ("" if none). */
 const char* moe_last_error_message(void);
 
+/*
+ * Routing diagnostics of the last forward enqueued on this handle ("Jah-yee/grok"
+ * README: list "New metrics track MoE-specific grokking signals" and the --demo
+ * block "[3] MoE routing (layer 0)", which prints a weight per expert and the
+ * routing entropy against its maximum).  Enqueued on `stream` (one small kernel);
+ * issue it on the forward's stream, after the forward, and before the next
+ * forward on this handle (it reads the router's per-CTA partial sums).
+ *   stats  DEVICE [10] fp32, written:
+ *          stats[0..7] mean router probability of each expert over the T tokens
+ *          stats[8]    routing entropy of that mean distribution, in nats (uniform: ln 8 = 2.079)
+ *          stats[9]    collapse index 1 - stats[8] / ln 8 (0 uniform, 1 one expert takes all)
+ * Token counts per expert come from moe_layer_forward's expert_counts.  Errors:
+ * MOE_ERR_INVALID_ARG (null or misaligned pointer, no forward with T > 0 yet).
+ */
+moe_status_t moe_layer_router_stats(moe_layer_t* layer, float* stats, void* stream);
+
 /* ----------------------------------------------------------- measurement */
 
 /* Kernels of one forward, in launch order (indices of the profiling arrays). */

@@ -78,6 +78,8 @@ def lib():
         L.moe_layer_set_profiling.argtypes = [vp, i32]
         L.moe_layer_profile_read.restype = i32
         L.moe_layer_profile_read.argtypes = [vp, vp, vp, i32]
+        L.moe_layer_router_stats.restype = i32
+        L.moe_layer_router_stats.argtypes = [vp, vp, vp]
         L.moe_layer_gemm_grid.restype = i32
         L.moe_layer_gemm_grid.argtypes = [vp, vp]
         L.moe_layer_launch_count.restype = i64
@@ -200,6 +202,15 @@ class MoeLayer:
                                             _stream_handle(stream), _ptr(idx), _ptr(prob), _ptr(counts)),
                "moe_layer_forward_host")
         return (out_host, idx, prob, counts) if routing else out_host
+
+    def router_stats(self, stream=None):
+        """Routing diagnostics of the last forward, as a CUDA fp32 tensor [10]:
+        mean router probability of experts 0-7, routing entropy (nats), collapse
+        index 1 - entropy / ln 8.  Enqueued on `stream` (default: current)."""
+        import torch
+        out = torch.empty(10, dtype=torch.float32, device=torch.device("cuda", self._dev))
+        _check(lib().moe_layer_router_stats(self._h, out.data_ptr(), _stream_handle(stream)), "moe_layer_router_stats")
+        return out
 
     def sync_status(self, stream=None):
         _check(lib().moe_layer_sync_status(self._h, _stream_handle(stream)), "moe_layer_sync_status")

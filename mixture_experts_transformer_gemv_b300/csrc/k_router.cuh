@@ -26,9 +26,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const __nv_bfloat16* __restrict__ x, int T, int d, const float* __restrict__ gate,
     const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
     __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
-    int32_t* __restrict__ user_idx, float* __restrict__ user_prob) {
+    int32_t* __restrict__ user_idx, float* __restrict__ user_prob, float* __restrict__ p_part) {
   __shared__ float red[kRouterThreads / 32][kRouterTok * kNumExperts];
   __shared__ float rnorm[kRouterTok];
+  __shared__ float s_p[kRouterTok][kNumExperts];
   const int t0 = blockIdx.x * kRouterTok;
   const int ntok = min(kRouterTok, T - t0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,6 +183,49 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
       user_prob[2 * t] = b0;
       user_prob[2 * t + 1] = b1;
     }
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) s_p[i][e] = p[e];
+  } else if (threadIdx.x < kRouterTok) {
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) s_p[threadIdx.x][e] = 0.f;
+  }
+  // this CTA's sum of the router probabilities, per expert, in token order
+  // (the routing diagnostics reduce these partial sums in block order)
+  __syncthreads();
+  if (threadIdx.x < kNumExperts) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRouterTok; ++i) s += s_p[i][threadIdx.x];
+    p_part[blockIdx.x * kNumExperts + threadIdx.x] = s;
+  }
+}
+
+// Routing diagnostics of the last forward ("Jah-yee/grok" README, list "New
+// metrics track MoE-specific grokking signals" and the --demo block "[3] MoE
+// routing (layer 0)"):
+//   stats[e]  = (1/T) sum_t p_t,e                mean router probability of expert e
+//   stats[8]  = -sum_e stats[e] ln stats[e]      routing entropy, nats (max ln 8 = 2.079)
+//   stats[9]  = 1 - stats[8] / ln 8              collapse index (0 uniform, 1 one expert)
+// One CTA; warp e sums the per-CTA partial sums of expert e in a fixed order.
+__global__ void __launch_bounds__(32 * kNumExperts) router_stats_kernel(const float* __restrict__ p_part,
+                                                                       int n_part, int T, float* __restrict__ stats) {
+  __shared__ float mean[kNumExperts];
+  const int e = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int b = lane; b < n_part; b += 32) s += p_part[b * kNumExperts + e];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) mean[e] = s / (float)T;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float h = 0.f;
+#pragma unroll
+    for (int q = 0; q < kNumExperts; ++q) {
+      stats[q] = mean[q];
+      if (mean[q] > 0.f) h -= mean[q] * logf(mean[q]);
+    }
+    stats[kNumExperts] = h;
+    stats[kNumExperts + 1] = 1.0f - h / logf((float)kNumExperts);
   }
 }
 

@@ -159,6 +159,8 @@ struct moe_layer {
   __nv_bfloat16* act = nullptr;
   float* y_rows = nullptr;
   float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
+  float* p_part = nullptr;  // [ceil(max_T / kRouterTok)][E] per-router-CTA sums of p
+  int last_T = 0;           // tokens of the last forward enqueued (routing diagnostics)
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
@@ -232,7 +234,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   mark(0);
   router_kernel<<<(T + kRouterTok - 1) / kRouterTok, kRouterThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
-      L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob);
+      L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
   mark(1);
   permute_kernel<<<1, kPermuteThreads, 0, st>>>(L->idx, L->prob, T, L->sched, L->row_of_slot, L->token_of_row,
                                                L->prob_of_row, counts, (int)L->rows_cap, checks, L->err);
@@ -355,6 +357,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
         L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks, L->err, static_cast<__nv_bfloat16*>(out));
   mark(6);
   L->launches += MOE_K_COUNT;
+  L->last_T = T;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
   return ok();
@@ -434,12 +437,13 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   const int64_t R = L->rows_cap;
 
   // one workspace block, every buffer 1 KB aligned
-  size_t offs[12], total = 0;
-  const size_t sizes[12] = {(size_t)(T * d * 2), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
+  size_t offs[13], total = 0;
+  const size_t sizes[13] = {(size_t)(T * d * 2), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
                             (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
                             (size_t)(R * F * 2), (size_t)(R * d * 4), 256,
-                            (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4};
-  for (int i = 0; i < 12; ++i) {
+                            (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4,
+                            (size_t)((T + kRouterTok - 1) / kRouterTok) * kNumExperts * 4};
+  for (int i = 0; i < 13; ++i) {
     offs[i] = total;
     total = align_up(total + sizes[i], 1024);
   }
@@ -462,6 +466,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   L->y_rows = reinterpret_cast<float*>(b + offs[9]);
   L->err = reinterpret_cast<uint32_t*>(b + offs[10]);
   L->part = reinterpret_cast<float*>(b + offs[11]);
+  L->p_part = reinterpret_cast<float*>(b + offs[12]);
   // decode-path split of the F reduction: up to kDecMaxSplit chunks of whole 64-wide blocks
   L->ksplit = kDecMaxSplit;
   while (L->ksplit > 1 && (F / kDecBK) % L->ksplit) L->ksplit /= 2;
@@ -650,6 +655,21 @@ moe_status_t moe_layer_profile_read(moe_layer_t* L, double* ms_total, int64_t* l
       L->prof_ms[k] = 0.0;
       L->prof_n[k] = 0;
     }
+  return ok();
+}
+
+moe_status_t moe_layer_router_stats(moe_layer_t* L, float* stats, void* stream) {
+  if (!L || !stats) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  if (!aligned4(stats)) return fail(MOE_ERR_INVALID_ARG, "stats not 4-byte aligned");
+  if (L->last_T < 1) return fail(MOE_ERR_INVALID_ARG, "no forward with T > 0 has been enqueued on this handle");
+  DeviceGuard g(L->device);
+  if (!g.ok) return fail(MOE_ERR_CUDA, "cannot select device %d", L->device);
+  const int n_part = (L->last_T + kRouterTok - 1) / kRouterTok;
+  router_stats_kernel<<<1, 32 * kNumExperts, 0, static_cast<cudaStream_t>(stream)>>>(L->p_part, n_part, L->last_T,
+                                                                                      stats);
+  L->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -101,6 +101,8 @@ def test_null_handle_calls(lib):
     assert lib.moe_layer_destroy(None) == moe.MOE_OK
     assert lib.moe_layer_launch_count(None) == 0
     assert lib.moe_layer_set_profiling(None, 1) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_router_stats(None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_gemm_grid(None, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

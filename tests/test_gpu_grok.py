@@ -26,8 +26,9 @@ def grok(request):
     weights = device_weights(inp)
     layer = make_layer(inp, weights=weights)
     y, idx, prob, counts = run(layer, inp)
+    stats = layer.router_stats().cpu().numpy().astype(np.float64)
     ref_route = oracle.route(inp)
-    yield {"inp": inp, "y": y, "idx": idx, "prob": prob, "counts": counts, "route": ref_route}
+    yield {"inp": inp, "y": y, "idx": idx, "prob": prob, "counts": counts, "route": ref_route, "stats": stats}
     layer.close()
     del weights
     torch.cuda.empty_cache()
@@ -44,6 +45,15 @@ def test_values_on_token_sample(grok):
     ref = oracle.moe_tokens(inp, toks)
     rep = assert_values(grok["y"][toks], ref.y, inp.name)
     print(inp.name, "tokens", len(toks), "values", rep)
+
+
+def test_router_stats_full_shape(grok):
+    """Routing diagnostics of the full-shape forward against the oracle's."""
+    s = grok["stats"]
+    ref = oracle.routing_stats(grok["route"].p)
+    np.testing.assert_allclose(s[:8], ref["mean_prob"], atol=2e-6)
+    assert abs(s[8] - ref["entropy"]) < 2e-5
+    print(grok["inp"].name, "router stats", np.round(s, 5).tolist())
 
 
 def test_skew_shares_reported(grok):

@@ -312,3 +312,51 @@ def test_back_to_back_forwards_are_deterministic(T, weights, flags):
         assert torch.equal(o, outs[0])
     assert_values(outs[0].float().cpu().numpy().astype(np.float64), oracle.moe_tokens(inp).y, inp.name)
     layer.close()
+
+
+
+# ----------------------------------------------------------- routing diagnostics
+
+def _stats_case(name):
+    if name == "uniform":
+        inp = synth.make_inputs(64, 256, 512, 81, norm_scales="ones", name=name)
+        inp.gate[:] = 0.0
+    elif name == "onehot":
+        inp = synth.make_inputs(40, 256, 512, 82, name=name)
+        b = np.zeros(8, np.float32)
+        b[4] = 1e4
+        inp.bias = b
+    elif name == "skew":
+        inp = synth.make_inputs(1001, 256, 512, 83, bias=synth.SKEW_BIAS, name=name)
+    elif name == "decode":
+        inp = synth.make_inputs(7, 384, 640, 84, name=name)
+    else:
+        inp = synth.workload("tiny")
+    return inp
+
+
+@pytest.mark.parametrize("name", ["tiny", "skew", "uniform", "onehot", "decode"])
+def test_router_stats_match_oracle(name):
+    """moe_layer_router_stats after a forward: mean probability per expert,
+    routing entropy and collapse index against the oracle's (fp32 sums of T
+    probabilities: 2e-6 absolute)."""
+    inp = _stats_case(name)
+    layer = make_layer(inp)
+    run(layer, inp)
+    s = layer.router_stats().cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    ref = oracle.routing_stats(oracle.route(inp).p)
+    np.testing.assert_allclose(s[:8], ref["mean_prob"], atol=2e-6)
+    assert abs(s[8] - ref["entropy"]) < 2e-5 and abs(s[9] - ref["collapse"]) < 2e-5
+    if name == "uniform":
+        assert round(float(s[8]), 3) == 2.079 and np.all(np.round(s[:8], 3) == 0.125)
+    layer.close()
+
+
+def test_router_stats_needs_a_forward():
+    inp = synth.workload("tiny")
+    layer = make_layer(inp)
+    with pytest.raises(moe.MoeError) as ei:
+        layer.router_stats()
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    layer.close()
