@@ -15,18 +15,21 @@
 
 namespace moe {
 
-constexpr int kCombineThreads = 256;
-constexpr int kCombineVec = 16;  // float4 per thread kept in registers: d <= 16384
+constexpr int kCombineThreads = 256;  // per token for large T; 1024 for T below the SM count
+constexpr int kCombineVec = 16;       // largest float4 count per thread kept in registers: d <= 16384
 
 // kSplit = false: Y rows of the grouped GEMM path, Y[row] = p * o.
 // kSplit = true:  decode path, o split over `ksplit` reduction chunks:
 //                 part[kc][e][s][:], s = row - row_offset[e]; summed in kc order.
-template <bool kSplit>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+// THREADS per token (256, or 1024 when there are fewer tokens than SMs); VEC =
+// ceil(d / (4 THREADS)) float4 of m per thread, sized to d so that registers (and
+// so the number of CTAs per SM) follow the row length.
+template <bool kSplit, int THREADS, int VEC>
+__global__ void __launch_bounds__(THREADS) combine_kernel(
     const float* __restrict__ y_rows, const int32_t* __restrict__ row_of_slot, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ sched, int ksplit, const __nv_bfloat16* x, const float* __restrict__ s_post,
     float eps, int d, int rows_valid_cap, int checks, uint32_t* __restrict__ err, __nv_bfloat16* out) {
-  __shared__ float red[kCombineThreads / 32];
+  __shared__ float red[THREADS / 32];
   const int t = blockIdx.x;
   int r0 = row_of_slot[2 * t], r1 = row_of_slot[2 * t + 1];
   if (checks && (r0 < 0 || r0 >= rows_valid_cap || r1 < 0 || r1 >= rows_valid_cap)) {
@@ -52,11 +55,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     y1 = reinterpret_cast<const float4*>(y_rows + (size_t)r1 * d);
   }
   const int nv = d >> 2;
-  float4 m[kCombineVec];
+  float4 m[VEC];
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < kCombineVec; ++i) {
-    const int c = threadIdx.x + i * kCombineThreads;
+  for (int i = 0; i < VEC; ++i) {
+    const int c = threadIdx.x + i * THREADS;
     if (c < nv) {
       float4 a = y0[c], b = y1[c];
       if (kSplit) {
@@ -79,14 +82,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   __syncthreads();
   float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < kCombineThreads / 32; ++w) tot += red[w];
+  for (int w = 0; w < THREADS / 32; ++w) tot += red[w];
   const float rr = 1.0f / sqrtf(tot / (float)d + eps);
 
   const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d);
   uint2* orow = reinterpret_cast<uint2*>(out + (size_t)t * d);
 #pragma unroll
-  for (int i = 0; i < kCombineVec; ++i) {
-    const int c = threadIdx.x + i * kCombineThreads;
+  for (int i = 0; i < VEC; ++i) {
+    const int c = threadIdx.x + i * THREADS;
     if (c < nv) {
       const float4 s = reinterpret_cast<const float4*>(s_post)[c];
       const uint2 xv = xr[c];  // read before the (possibly aliasing) write below
@@ -96,6 +99,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
       orow[c] = o;
     }
   }
+}
+
+// Launch of combine_kernel<kSplit, THREADS, VEC> for a row length d (multiple of
+// 128, <= 16384): VEC is the smallest count of float4 per thread that covers d/4.
+template <bool kSplit, int THREADS, int VEC = 1>
+inline void launch_combine(int T, cudaStream_t st, const float* y_rows, const int32_t* row_of_slot,
+                           const int32_t* idx, const int32_t* sched, int ksplit, const __nv_bfloat16* x,
+                           const float* s_post, float eps, int d, int rows_valid_cap, int checks, uint32_t* err,
+                           __nv_bfloat16* out) {
+  if constexpr (VEC * THREADS * 4 < kCombineVec * kCombineThreads * 4) {
+    if (d > VEC * THREADS * 4) {
+      launch_combine<kSplit, THREADS, VEC + 1>(T, st, y_rows, row_of_slot, idx, sched, ksplit, x, s_post, eps, d,
+                                               rows_valid_cap, checks, err, out);
+      return;
+    }
+  }
+  combine_kernel<kSplit, THREADS, VEC><<<T, THREADS, 0, st>>>(y_rows, row_of_slot, idx, sched, ksplit, x, s_post,
+                                                              eps, d, rows_valid_cap, checks, err, out);
 }
 
 }  // namespace moe

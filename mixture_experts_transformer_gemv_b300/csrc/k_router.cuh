@@ -10,9 +10,10 @@
 //   p      = softmax(l)                      (max-subtracted, fp32)
 //   i0, i1 = two largest p, ties to the lower index; weights p_i0, p_i1
 //
-// One CTA of 256 threads handles kRouterTok tokens: every gate value it loads
-// feeds all of them (the gate is [8, d] fp32 and is read from L2 once per CTA,
-// not once per token).  x rows are read with 16-byte loads, twice (the second
+// One CTA of 256 threads handles kRouterTok tokens (4 for large T, 1 for small
+// T, where more CTAs hide latency better): every gate value it loads feeds all
+// of them (the gate is [8, d] fp32 and is read from L2 once per CTA, not once
+// per token).  x rows are read with 16-byte loads, twice (the second
 // pass hits L1/L2).
 #pragma once
 #include "common.cuh"
@@ -20,9 +21,10 @@
 namespace moe {
 
 constexpr int kRouterThreads = 256;
-constexpr int kRouterTok = 4;
+constexpr int kRouterTokMax = 4;  // tokens per CTA for large T; 1 for small T (more CTAs)
 
-__global__ void __launch_bounds__(kRouterThreads) router_kernel(
+template <int kRouterTok>
+__global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
     const __nv_bfloat16* __restrict__ x, int T, int d, const float* __restrict__ gate,
     const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
     __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
@@ -82,36 +84,40 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const float4 sa = *reinterpret_cast<const float4*>(s_pre + c * 8);
     const float4 sb = *reinterpret_cast<const float4*>(s_pre + c * 8 + 4);
     const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-    float g[kNumExperts][8];
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) {
-      const float4 ga = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8);
-      const float4 gb = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8 + 4);
-      g[e][0] = ga.x; g[e][1] = ga.y; g[e][2] = ga.z; g[e][3] = ga.w;
-      g[e][4] = gb.x; g[e][5] = gb.y; g[e][6] = gb.z; g[e][7] = gb.w;
-    }
+    // the normed values of this chunk for every token (and their bf16 copy out)
+    float xn[kRouterTok][8];
 #pragma unroll
     for (int i = 0; i < kRouterTok; ++i) {
       if (i < ntok) {
         uint4 v = ld_nc_v4(x + (size_t)(t0 + i) * d + c * 8);
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float xn[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          xn[2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
-          xn[2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
+          xn[i][2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
+          xn[i][2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
         }
         uint4 o;
-        o.x = pack_bf16x2(xn[0], xn[1]);
-        o.y = pack_bf16x2(xn[2], xn[3]);
-        o.z = pack_bf16x2(xn[4], xn[5]);
-        o.w = pack_bf16x2(xn[6], xn[7]);
+        o.x = pack_bf16x2(xn[i][0], xn[i][1]);
+        o.y = pack_bf16x2(xn[i][2], xn[i][3]);
+        o.z = pack_bf16x2(xn[i][4], xn[i][5]);
+        o.w = pack_bf16x2(xn[i][6], xn[i][7]);
         *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
+      } else {
 #pragma unroll
-        for (int e = 0; e < kNumExperts; ++e)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xn[j], g[e][j], lg[i][e]);
+        for (int j = 0; j < 8; ++j) xn[i][j] = 0.f;
       }
+    }
+    // one expert's 8 gate values at a time, used by every token (registers stay
+    // low enough for two CTAs per SM)
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) {
+      const float4 ga = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8);
+      const float4 gb = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8 + 4);
+      const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+      for (int i = 0; i < kRouterTok; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xn[i][j], g[j], lg[i][e]);
     }
   }
   // block reduction of the kRouterTok x 8 partial logits

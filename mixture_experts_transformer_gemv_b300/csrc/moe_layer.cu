@@ -159,8 +159,9 @@ struct moe_layer {
   __nv_bfloat16* act = nullptr;
   float* y_rows = nullptr;
   float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
-  float* p_part = nullptr;  // [ceil(max_T / kRouterTok)][E] per-router-CTA sums of p
+  float* p_part = nullptr;  // [router CTAs (<= max_T)][E] per-router-CTA sums of p
   int last_T = 0;           // tokens of the last forward enqueued (routing diagnostics)
+  int last_router_ctas = 0; // router CTAs of that forward
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
@@ -232,9 +233,17 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
   const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) || (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
   mark(0);
-  router_kernel<<<(T + kRouterTok - 1) / kRouterTok, kRouterThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
-      L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
+  // 4 tokens per router CTA once there are enough CTAs to fill the GPU twice over
+  const int rtok = (T >= 2 * kRouterTokMax * L->num_sms) ? kRouterTokMax : 1;
+  L->last_router_ctas = (T + rtok - 1) / rtok;
+  if (rtok == kRouterTokMax)
+    router_kernel<kRouterTokMax><<<L->last_router_ctas, kRouterThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
+        L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
+  else
+    router_kernel<1><<<L->last_router_ctas, kRouterThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
+        L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
   mark(1);
   permute_kernel<<<1, kPermuteThreads, 0, st>>>(L->idx, L->prob, T, L->sched, L->row_of_slot, L->token_of_row,
                                                L->prob_of_row, counts, (int)L->rows_cap, checks, L->err);
@@ -346,15 +355,28 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
           L->tm_act, L->tm_w1_128, L->tm_w1_128, p);
   }
   mark(5);
-  if (decode)
-    combine_kernel<true><<<T, kCombineThreads, 0, st>>>(
-        L->part, L->row_of_slot, L->idx, L->sched, int8 ? L->ksplit_i8 : L->ksplit,
-        static_cast<const __nv_bfloat16*>(hidden),
-        L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks, L->err, static_cast<__nv_bfloat16*>(out));
-  else
-    combine_kernel<false><<<T, kCombineThreads, 0, st>>>(
-        L->y_rows, L->row_of_slot, L->idx, L->sched, 1, static_cast<const __nv_bfloat16*>(hidden),
-        L->w.post_norm_scale, L->cfg.eps, d, (int)L->rows_cap, checks, L->err, static_cast<__nv_bfloat16*>(out));
+  {
+    const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+    const int rc = (int)L->rows_cap;
+    const bool wide = T < L->num_sms;  // few tokens: more threads per token hide latency
+    if (decode) {
+      const int ks = int8 ? L->ksplit_i8 : L->ksplit;
+      if (wide)
+        launch_combine<true, 1024>(T, st, L->part, L->row_of_slot, L->idx, L->sched, ks, xh, L->w.post_norm_scale,
+                                   L->cfg.eps, d, rc, checks, L->err, o);
+      else
+        launch_combine<true, kCombineThreads>(T, st, L->part, L->row_of_slot, L->idx, L->sched, ks, xh,
+                                              L->w.post_norm_scale, L->cfg.eps, d, rc, checks, L->err, o);
+    } else {
+      if (wide)
+        launch_combine<false, 1024>(T, st, L->y_rows, L->row_of_slot, L->idx, L->sched, 1, xh,
+                                    L->w.post_norm_scale, L->cfg.eps, d, rc, checks, L->err, o);
+      else
+        launch_combine<false, kCombineThreads>(T, st, L->y_rows, L->row_of_slot, L->idx, L->sched, 1, xh,
+                                               L->w.post_norm_scale, L->cfg.eps, d, rc, checks, L->err, o);
+    }
+  }
   mark(6);
   L->launches += MOE_K_COUNT;
   L->last_T = T;
@@ -442,7 +464,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
                             (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
                             (size_t)(R * F * 2), (size_t)(R * d * 4), 256,
                             (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4,
-                            (size_t)((T + kRouterTok - 1) / kRouterTok) * kNumExperts * 4};
+                            (size_t)T * kNumExperts * 4};
   for (int i = 0; i < 13; ++i) {
     offs[i] = total;
     total = align_up(total + sizes[i], 1024);
@@ -664,9 +686,8 @@ moe_status_t moe_layer_router_stats(moe_layer_t* L, float* stats, void* stream) 
   if (L->last_T < 1) return fail(MOE_ERR_INVALID_ARG, "no forward with T > 0 has been enqueued on this handle");
   DeviceGuard g(L->device);
   if (!g.ok) return fail(MOE_ERR_CUDA, "cannot select device %d", L->device);
-  const int n_part = (L->last_T + kRouterTok - 1) / kRouterTok;
-  router_stats_kernel<<<1, 32 * kNumExperts, 0, static_cast<cudaStream_t>(stream)>>>(L->p_part, n_part, L->last_T,
-                                                                                      stats);
+  router_stats_kernel<<<1, 32 * kNumExperts, 0, static_cast<cudaStream_t>(stream)>>>(L->p_part, L->last_router_ctas,
+                                                                                      L->last_T, stats);
   L->launches += 1;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));

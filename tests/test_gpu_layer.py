@@ -41,6 +41,7 @@ def test_tiny_workload_all_tokens():
     (1000, 256, 640, 32),    # two row blocks per expert, F/128 = 5
     (200, 384, 512, 33),     # d = 384: the last down-projection tile is half outside d
     (7, 256, 512, 34),       # fewer slots than a tile in every expert
+    (1500, 256, 512, 36),    # enough tokens for the 4-tokens-per-CTA router
 ])
 def test_mid_shapes(T, d, F, seed):
     _full_check(synth.make_inputs(T, d, F, seed, name=f"mid{T}x{d}x{F}"))
