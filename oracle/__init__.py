@@ -130,8 +130,9 @@ class Route:
 def _weight_args(inp):
     if inp.weight_dtype == "bf16":
         return W_BF16, inp.w, inp.wv, inp.w1, None, None, None, 1, 1, 1
-    # per expert, per output channel: logical (E, 1, N)
-    return (W_INT8, inp.w, inp.wv, inp.w1, inp.w_scale, inp.wv_scale, inp.w1_scale, inp.E, 1, 1)
+    # logical scale shape (E_s, G, N): G groups along each weight's input dimension
+    return (W_INT8, inp.w, inp.wv, inp.w1, inp.w_scale, inp.wv_scale, inp.w1_scale, inp.scale_experts,
+            inp.scale_groups, inp.scale_groups)
 
 
 def route(inp, keep_xn: bool = False) -> Route:

@@ -145,9 +145,11 @@ class MoeInputs:
     w: np.ndarray  # [E, F, d] bf16 bits or int8
     wv: np.ndarray  # [E, F, d]
     w1: np.ndarray  # [E, d, F]
-    w_scale: Optional[np.ndarray] = None  # [E, F] bf16 bits (int8 only)
-    wv_scale: Optional[np.ndarray] = None  # [E, F]
-    w1_scale: Optional[np.ndarray] = None  # [E, d]
+    w_scale: Optional[np.ndarray] = None  # [E_s, G, F] bf16 bits (int8 only)
+    wv_scale: Optional[np.ndarray] = None  # [E_s, G, F]
+    w1_scale: Optional[np.ndarray] = None  # [E_s, G, d]
+    scale_experts: int = 8  # E_s: 8 = one scale set per expert, 1 = shared by all experts
+    scale_groups: int = 1   # G: groups along each weight's input dimension
     notes: dict = field(default_factory=dict)
 
 
@@ -166,7 +168,13 @@ def make_inputs(
     bias=None,
     eps: float = 1e-5,
     int8_scale_range=(1e-4, 3e-4),
+    int8_scale_shape=(8, 1),
 ) -> MoeInputs:
+    """int8_scale_shape = (E_s, G): the logical scale shape (E_s, G, N) of every
+    int8 weight ("TevunahAi/Grok-1-BF16", "Conversion Details" lists (8,1,N),
+    (8,8,N), (1,N) and (8,N), the last two read as (1,1,N) and (1,8,N)); scale set
+    es is drawn from the stream of expert es, so (8, 1) gives the same values
+    whatever else changes."""
     x = normal_bf16(seed, TID_X, (T, d))
     gstd = (1.0 / np.sqrt(d)) if gate_std is None else gate_std
     gate = normal_f32(seed, TID_GATE, (E, d), std=gstd)
@@ -190,22 +198,27 @@ def make_inputs(
         w = np.empty((E, F, d), np.int8)
         wv = np.empty((E, F, d), np.int8)
         w1 = np.empty((E, d, F), np.int8)
-        sw = np.empty((E, F), np.uint16)
-        swv = np.empty((E, F), np.uint16)
-        sw1 = np.empty((E, d), np.uint16)
+        es_n, g_n = int8_scale_shape
+        assert es_n in (1, E) and d % g_n == 0 and F % g_n == 0
+        sw = np.empty((es_n, g_n, F), np.uint16)
+        swv = np.empty((es_n, g_n, F), np.uint16)
+        sw1 = np.empty((es_n, g_n, d), np.uint16)
         lo, hi = int8_scale_range
         for e in range(E):
             uniform_int8(seed, TID_W + e, None, -127, 127, out=w[e])
             uniform_int8(seed, TID_WV + e, None, -127, 127, out=wv[e])
             uniform_int8(seed, TID_W1 + e, None, -127, 127, out=w1[e])
-            uniform_bf16(seed, TID_SW + e, None, lo, hi, out=sw[e])
-            uniform_bf16(seed, TID_SWV + e, None, lo, hi, out=swv[e])
-            uniform_bf16(seed, TID_SW1 + e, None, lo, hi, out=sw1[e])
+        for es in range(es_n):
+            uniform_bf16(seed, TID_SW + es, None, lo, hi, out=sw[es])
+            uniform_bf16(seed, TID_SWV + es, None, lo, hi, out=swv[es])
+            uniform_bf16(seed, TID_SW1 + es, None, lo, hi, out=sw1[es])
     else:
         raise ValueError(weight_dtype)
     return MoeInputs(name=name, seed=seed, T=T, d=d, F=F, E=E, top_k=2, eps=eps, weight_dtype=weight_dtype,
                      x=x, gate=gate, bias=b, s_pre=s_pre, s_post=s_post, w=w, wv=wv, w1=w1,
-                     w_scale=sw, wv_scale=swv, w1_scale=sw1)
+                     w_scale=sw, wv_scale=swv, w1_scale=sw1,
+                     scale_experts=int8_scale_shape[0] if weight_dtype == "int8" else E,
+                     scale_groups=int8_scale_shape[1] if weight_dtype == "int8" else 1)
 
 
 GROK_D, GROK_F = 6144, 32768

@@ -40,12 +40,16 @@ def _weights_f64(inp):
     """Dense fp64 weights, dequantised by an independent numpy broadcast."""
     if inp.weight_dtype == "bf16":
         return _f64(inp.w), _f64(inp.wv), _f64(inp.w1)
-    sw = synth.bf16_bits_to_f32(inp.w_scale)[:, :, None]
-    swv = synth.bf16_bits_to_f32(inp.wv_scale)[:, :, None]
-    sw1 = synth.bf16_bits_to_f32(inp.w1_scale)[:, :, None]
-    return (torch.from_numpy((inp.w.astype(np.float32) * sw).astype(np.float64)),
-            torch.from_numpy((inp.wv.astype(np.float32) * swv).astype(np.float64)),
-            torch.from_numpy((inp.w1.astype(np.float32) * sw1).astype(np.float64)))
+
+    def full(scale, q):
+        # scale [E_s, G, N] -> [E, N, K]: group g covers inputs [g K/G, (g+1) K/G)
+        E, N, K = q.shape
+        s = synth.bf16_bits_to_f32(scale)
+        s = np.repeat(np.transpose(s, (0, 2, 1)), K // s.shape[1], axis=2)
+        return np.broadcast_to(s, (E, N, K))
+
+    return tuple(torch.from_numpy((q.astype(np.float32) * full(s, q)).astype(np.float64))
+                 for q, s in ((inp.w, inp.w_scale), (inp.wv, inp.wv_scale), (inp.w1, inp.w1_scale)))
 
 
 def _torch_layer_dense(inp):
@@ -196,7 +200,7 @@ def test_routing_invariants():
 
 # ------------------------------------------------------------- whole layer
 
-@pytest.mark.parametrize("which", ["tiny", "mid", "tiny_int8", "tiny_bias"])
+@pytest.mark.parametrize("which", ["tiny", "mid", "tiny_int8", "int8_8x8", "int8_1x1", "int8_1x8", "tiny_bias"])
 def test_layer_equals_dense_bruteforce(which):
     if which == "tiny":
         inp = synth.workload("tiny")
@@ -204,6 +208,10 @@ def test_layer_equals_dense_bruteforce(which):
         inp = synth.make_inputs(24, 384, 640, 11)
     elif which == "tiny_int8":
         inp = synth.make_inputs(32, 256, 512, 12, weight_dtype="int8", int8_scale_range=(1e-3, 3e-3))
+    elif which.startswith("int8_"):  # grouped / shared scale shapes (8,8,N), (1,N), (8,N)
+        es, g = (int(v) for v in which[5:].split("x"))
+        inp = synth.make_inputs(32, 256, 512, 14, weight_dtype="int8", int8_scale_range=(1e-3, 3e-3),
+                                int8_scale_shape=(es, g))
     else:
         inp = synth.make_inputs(32, 256, 512, 13, bias=synth.SKEW_BIAS)
     y_ref, m_ref, idx_ref, w_ref, p_ref = _torch_layer_dense(inp)
