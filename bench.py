@@ -282,7 +282,8 @@ def run_ours(args, rank, world, local_rank):
             weights[k] = torch.from_numpy(getattr(inp, k).view(np.int16)).view(torch.bfloat16).cuda()
     x = x_host.cuda()
     out = torch.empty_like(x)
-    layer = moe.MoeLayer(inp.d, inp.F, inp.T, weights, eps=inp.eps, weight_dtype=inp.weight_dtype)
+    layer = moe.MoeLayer(inp.d, inp.F, inp.T, weights, eps=inp.eps, weight_dtype=inp.weight_dtype,
+                         scale_shape=(inp.scale_experts, inp.scale_groups))
     stream = torch.cuda.current_stream()
 
     # warm-up

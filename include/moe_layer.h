@@ -71,6 +71,18 @@ typedef struct {
   float eps;            /* RMSNorm epsilon (Grok-1 configs: 1e-5) */
   int32_t weight_dtype; /* moe_weight_dtype_t */
   uint32_t flags;       /* MOE_FLAG_* */
+  /* int8 only: logical scale shape (scale_experts, scale_groups, N) of every
+   * expert weight ("TevunahAi/Grok-1-BF16", "Conversion Details": (8,1,N),
+   * (8,8,N), (1,N), (8,N); the last two read as (1,1,N) and (1,8,N)).
+   * scale_experts: 8 = one scale set per expert, 1 = one set shared by all
+   * experts (0 means 8).  scale_groups: G groups along each weight's input
+   * dimension, group g covering inputs [g K/G, (g+1) K/G) (0 means 1).  G > 1
+   * needs d and F to be multiples of 128 G.  With G == 1 the scale multiplies
+   * the fp32 result of the reduction (exact); with G > 1 it multiplies each
+   * weight as it is converted on chip, rounded once to bf16 (fp16 on the T <= 16
+   * path). */
+  int32_t scale_experts;
+  int32_t scale_groups;
 } moe_config_t;
 
 /*
@@ -85,10 +97,10 @@ typedef struct {
   const void* w;                /* [E, F, d] bf16 or int8: GELU branch ("linear") */
   const void* wv;               /* [E, F, d] bf16 or int8: linear branch ("linear_v") */
   const void* w1;               /* [E, d, F] bf16 or int8: down projection ("linear_1") */
-  const uint16_t* w_scale;      /* int8 only: bf16 bits [E, F], one scale per expert and output
-                                   channel (the logical (8, 1, N) scale shape); NULL for bf16 */
-  const uint16_t* wv_scale;     /* int8 only: bf16 bits [E, F] */
-  const uint16_t* w1_scale;     /* int8 only: bf16 bits [E, d] */
+  const uint16_t* w_scale;      /* int8 only: bf16 bits [scale_experts, scale_groups, F] (per expert,
+                                   group and output channel); NULL for bf16 */
+  const uint16_t* wv_scale;     /* int8 only: bf16 bits [scale_experts, scale_groups, F] */
+  const uint16_t* w1_scale;     /* int8 only: bf16 bits [scale_experts, scale_groups, d] */
   const float* pre_norm_scale;  /* [d] fp32 (pre_moe_norm.scale) */
   const float* post_norm_scale; /* [d] fp32 (post_moe_norm.scale) */
 } moe_weights_t;
@@ -100,9 +112,10 @@ typedef struct moe_layer moe_layer_t;
  * allocate the workspace for cfg->max_tokens tokens on the current device.
  * Launches no kernel.  On success *out receives the handle (owned by the caller,
  * freed by moe_layer_destroy).  Errors: MOE_ERR_INVALID_ARG (null / misaligned
- * pointer, max_tokens < 1, eps <= 0), MOE_ERR_UNSUPPORTED (E != 8, top_k != 2,
- * d or F not a multiple of 128, d > 16384, int8 without scales, device not
- * sm_103 / sm_100 class), MOE_ERR_OOM, MOE_ERR_CUDA.
+ * pointer, max_tokens < 1, eps <= 0, int8 without scales, scale_experts not in
+ * {0, 1, 8}), MOE_ERR_UNSUPPORTED (E != 8, top_k != 2, d or F not a multiple of
+ * 128, d > 16384, scale_groups > 1 with d or F not a multiple of 128 G, device
+ * not sm_103), MOE_ERR_OOM, MOE_ERR_CUDA.
  */
 moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weights, moe_layer_t** out);
 

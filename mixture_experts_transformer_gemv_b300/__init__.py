@@ -34,7 +34,8 @@ class MoeError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ffn", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("eps", ctypes.c_float),
-                ("weight_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("weight_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32), ("scale_experts", ctypes.c_int32),
+                ("scale_groups", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -142,17 +143,20 @@ class MoeLayer:
 
     weights: dict of CUDA tensors, contiguous:
       gate [E, d] fp32, gate_bias [E] fp32 or None, w / wv [E, F, d] and
-      w1 [E, d, F] (bf16, or int8 with w_scale / wv_scale [E, F] and w1_scale
-      [E, d] bf16), pre_norm_scale / post_norm_scale [d] fp32.
+      w1 [E, d, F] (bf16, or int8 with w_scale / wv_scale [E_s, G, F] and
+      w1_scale [E_s, G, d] bf16, scale_shape = (E_s, G)), pre_norm_scale /
+      post_norm_scale [d] fp32.
     """
 
     def __init__(self, d_model: int, d_ffn: int, max_tokens: int, weights: dict, eps: float = 1e-5,
-                 weight_dtype: str = "bf16", flags: int = 0, num_experts: int = 8, top_k: int = 2):
+                 weight_dtype: str = "bf16", flags: int = 0, num_experts: int = 8, top_k: int = 2,
+                 scale_shape=(8, 1)):
         import torch
         self.d, self.F, self.max_tokens = d_model, d_ffn, max_tokens
         self._weights = dict(weights)  # keep the borrowed tensors alive
         cfg = Config(d_model, d_ffn, num_experts, top_k, max_tokens, eps,
-                     MOE_WEIGHT_INT8 if weight_dtype == "int8" else MOE_WEIGHT_BF16, flags)
+                     MOE_WEIGHT_INT8 if weight_dtype == "int8" else MOE_WEIGHT_BF16, flags,
+                     int(scale_shape[0]), int(scale_shape[1]))
         w = Weights()
         for name, _ in Weights._fields_:
             t = weights.get(name)

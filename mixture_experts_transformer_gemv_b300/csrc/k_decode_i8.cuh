@@ -29,7 +29,9 @@
 // projection's epilogue writes the GeGLU activations as fp16, saturating at
 // +-65504; fp16 carries 3 more mantissa bits than bf16 within that range.
 // The per-channel scales factor out of the reduction and are applied in fp32 in
-// the epilogue (one scale per thread: its TMEM lane is one weight row).
+// the epilogue (one scale per thread: its TMEM lane is one weight row); scales
+// that also vary along k (G > 1 groups) multiply the converted weights instead
+// (f16x2, one rounding).
 //
 // Warps: 0 TMA producer; 1 TMEM allocation + MMA issuer; 2-5 epilogue;
 // 6-21 converters, each converting a quarter of every k-block.  Every wait is
@@ -87,6 +89,12 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   hi = f16x2_sub(__byte_perm(u, 0x64u, 0x4342), 0x64806480u);
 }
 
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint16_t f16_sat(float v) {
   uint16_t r;
   asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(r) : "f"(v));
@@ -101,8 +109,11 @@ struct DecI8Params {
   int ksplit;                 // K4q: chunks of the reduction (1 for K3q)
   void* out;                  // act [rows_cap, F] fp16 or part [ksplit][E][16][d] fp32
   const float* row_scale;     // K4q: combine weight of each permuted row
-  const uint16_t* scale0;     // bf16 bits [E, rows_per_expert]: scale of W (K3q) or W1 (K4q)
-  const uint16_t* scale1;     // K3q: bf16 bits [E, F], scale of Wv
+  const uint16_t* scale0;     // bf16 bits [E_s, G, rows_per_expert]: scale of W (K3q) or W1 (K4q)
+  const uint16_t* scale1;     // K3q: bf16 bits [E_s, G, F], scale of Wv
+  int scale_experts;          // E_s: 8 (per expert) or 1 (shared)
+  int scale_groups;           // G groups along the reduction; 1 = per output channel only
+  int group_kb;               // G > 1: k-blocks of 128 per group
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -296,14 +307,16 @@ __global__ void __launch_bounds__(DecI8Cfg<EPI>::kThreads, 1)
       tc_fence_after_sync();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
       const int n = d.blk * kDecBM + q * 32 + lane;  // weight row = output column
-      const size_t si = (size_t)d.e * p.rows_per_expert + n;
+      // per-output-channel scales (G == 1); grouped scales were applied in conversion
+      const size_t si = (size_t)(p.scale_experts > 1 ? d.e : 0) * p.rows_per_expert + n;
+      const bool chan = p.scale_groups == 1;
       if (EPI == kEpiGeglu) {
         uint32_t h[16], v[16];
         tmem_ld_32x32b_x16(tb, h);       // columns [0, 16): W branch
         tmem_ld_32x32b_x16(tb + 32, v);  // columns [32, 48): Wv branch
         tmem_ld_wait();
-        const float sw = __uint_as_float((uint32_t)p.scale0[si] << 16);
-        const float sv = __uint_as_float((uint32_t)p.scale1[si] << 16);
+        const float sw = chan ? __uint_as_float((uint32_t)p.scale0[si] << 16) : 1.0f;
+        const float sv = chan ? __uint_as_float((uint32_t)p.scale1[si] << 16) : 1.0f;
         uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
         for (int s = 0; s < kDecNS; ++s)
@@ -314,7 +327,7 @@ __global__ void __launch_bounds__(DecI8Cfg<EPI>::kThreads, 1)
         uint32_t y[16];
         tmem_ld_32x32b_x16(tb, y);
         tmem_ld_wait();
-        const float s1 = __uint_as_float((uint32_t)p.scale0[si] << 16);
+        const float s1 = chan ? __uint_as_float((uint32_t)p.scale0[si] << 16) : 1.0f;
         float* out = static_cast<float*>(p.out) + ((size_t)(d.kc * kNumExperts + d.e) * kDecNS) * p.n_out;
 #pragma unroll
         for (int s = 0; s < kDecNS; ++s)
@@ -343,7 +356,19 @@ __global__ void __launch_bounds__(DecI8Cfg<EPI>::kThreads, 1)
     uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const DecUnit du = unit_of(u);
+      const int n = du.blk * kDecBM + r;  // this thread's weight row
+      const size_t gsc_e = (size_t)(p.scale_experts > 1 ? du.e : 0) * p.scale_groups;
       for (int i = 0; i < kb_per_unit; ++i) {
+        // grouped scales (G > 1): this row's scale for the k-block's group, as fp16
+        __half2 gs2 = __float2half2_rn(1.0f);
+        if (p.scale_groups > 1) {
+          const size_t gi = (gsc_e + (du.kc * kb_per_unit + i) / p.group_kb) * p.rows_per_expert + n;
+          const float s0 = __uint_as_float((uint32_t)p.scale0[gi] << 16);
+          gs2 = __float2half2_rn(s0);
+          if (EPI == kEpiGeglu && (part >> 1) == 1) gs2 = __float2half2_rn(__uint_as_float((uint32_t)p.scale1[gi] << 16));
+        }
+        const uint32_t gsu = *reinterpret_cast<uint32_t*>(&gs2);
         ok = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
                                          wait_bounded(aempty_bar(astage), aphase ^ 1u, abort_flag, p.timeout_ns));
         if (!ok) break;
@@ -363,6 +388,10 @@ __global__ void __launch_bounds__(DecI8Cfg<EPI>::kThreads, 1)
             i8x4_to_f16x4(v.z, a[8 * cc + 4], a[8 * cc + 5]);
             i8x4_to_f16x4(v.w, a[8 * cc + 6], a[8 * cc + 7]);
           }
+          if (p.scale_groups > 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = f16x2_mul(a[j], gsu);
+          }
           tmem_st_32x32b_x32(acol + mat * 64 + hh * 32, a);
         } else {  // K [32 part, 32 part + 32) of the W1 row -> 16 columns
           const uint8_t* row = sb + r * 128;
@@ -375,6 +404,10 @@ __global__ void __launch_bounds__(DecI8Cfg<EPI>::kThreads, 1)
             i8x4_to_f16x4(v.y, a[8 * cc + 2], a[8 * cc + 3]);
             i8x4_to_f16x4(v.z, a[8 * cc + 4], a[8 * cc + 5]);
             i8x4_to_f16x4(v.w, a[8 * cc + 6], a[8 * cc + 7]);
+          }
+          if (p.scale_groups > 1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a[j] = f16x2_mul(a[j], gsu);
           }
           tmem_st_32x32b_x16(acol + part * 16, a);
         }

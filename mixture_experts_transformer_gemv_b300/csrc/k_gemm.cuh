@@ -45,7 +45,9 @@
 // the MMA reads (|q| <= 127 is exact in bf16), make it visible to the tensor
 // core's async proxy and tell the even CTA's MMA warp.  Because the scale
 // belongs to an output channel it factors out of the reduction and is applied
-// in fp32 in the epilogue: sum_k a_k (q_nk s_n) = s_n sum_k a_k q_nk.
+// in fp32 in the epilogue: sum_k a_k (q_nk s_n) = s_n sum_k a_k q_nk.  Scales that
+// also vary along k (G > 1 groups) do not factor out; the converters then
+// multiply each converted weight by its group's scale (bf16x2, one rounding).
 //
 // Every wait is bounded (wait_bounded).  A role that times out raises its CTA's
 // abort flag and the device error word; the others stop at their next wait
@@ -53,6 +55,8 @@
 // (bounded) for its own TMA copies in flight, the MMA issuer for its own MMAs,
 // and both CTAs meet at a cluster barrier before TMEM is freed and they exit.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 #include "ptx_pair.cuh"
@@ -104,8 +108,11 @@ struct GemmParams {
   int n_out;                     // output columns / leading dimension: F (act) or d (Y)
   void* out;                     // act [rows_cap, F] bf16 or Y [rows_cap, d] fp32
   const float* row_scale;        // down: combine weight of each permuted row
-  const uint16_t* scale0;        // int8: bf16 bits [E, n_out], scale of W (up) or W1 (down)
-  const uint16_t* scale1;        // int8 up: bf16 bits [E, F], scale of Wv
+  const uint16_t* scale0;        // int8: bf16 bits [E_s, G, n_out], scale of W (up) or W1 (down)
+  const uint16_t* scale1;        // int8 up: bf16 bits [E_s, G, F], scale of Wv
+  int scale_experts;             // int8: E_s, 8 (per expert) or 1 (shared)
+  int scale_groups;              // int8: G groups along the reduction; 1 = per output channel only
+  int group_kb;                  // int8, G > 1: k-blocks of 64 per group
   uint32_t* err;                 // device error word
   uint64_t timeout_ns;           // limit of every wait
 };
@@ -139,6 +146,11 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExp
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -372,8 +384,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           tmem_ld_32x32b_x32(tbase + c * 32, h);
           tmem_ld_32x32b_x32(tbase + kGemmHalfN + c * 32, v);
           tmem_ld_wait();
-          if (WQ) {  // per-output-channel scales of W and Wv (same for every row)
-            const size_t so = (size_t)tc.e * p.n_out + n0 + c * 32;
+          if (WQ && p.scale_groups == 1) {  // per-output-channel scales of W and Wv (same for every row)
+            const size_t so = (size_t)(p.scale_experts > 1 ? tc.e : 0) * p.n_out + n0 + c * 32;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               float sw[8], sv[8];
@@ -410,8 +422,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           float sc[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) sc[j] = ps;
-          if (WQ) {  // per-output-channel scale of W1
-            const size_t so = (size_t)tc.e * p.n_out + col0;
+          if (WQ && p.scale_groups == 1) {  // per-output-channel scale of W1
+            const size_t so = (size_t)(p.scale_experts > 1 ? tc.e : 0) * p.n_out + col0;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               float s8[8];
@@ -449,6 +461,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
     uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
     bool ok = true;
     for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      // grouped scales (G > 1): this CTA's B rows are weight rows nb + r
+      const TileCoord tc = decode_tile(t, off, p.n_tiles);
+      const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN : tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
+      const uint16_t* gsc = (EPI == kEpiGeglu && !leader) ? p.scale1 : p.scale0;
+      const size_t gsc_e = (size_t)(p.scale_experts > 1 ? tc.e : 0) * p.scale_groups;
       for (int kb = 0; kb < kb_count; ++kb) {
         const bool got = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
                                                      wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag,
@@ -456,20 +473,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         if (got) {
           const uint8_t* src = sB8 + stage * kB8TileBytes;
           uint8_t* dst = sB + bstage * kBTileBytes;
+          // one 16-byte unit: row u / 4, int8 columns [16 (u % 4), +16), optionally times
+          // this row's group scale (bf16 bits in both halves of s2)
+          auto convert = [&](auto with_scale) {
 #pragma unroll
-          for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
-            const int u = ct + i * kConvThreads;  // 16-byte unit: row u / 4, int8 columns [16 (u % 4), +16)
-            const int r = u >> 2, c = u & 3;
-            const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
-            uint4 o0, o1;
-            i8x4_to_bf16x4(qv.x, o0.x, o0.y);
-            i8x4_to_bf16x4(qv.y, o0.z, o0.w);
-            i8x4_to_bf16x4(qv.z, o1.x, o1.y);
-            i8x4_to_bf16x4(qv.w, o1.z, o1.w);
-            uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
-            *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = o0;
-            *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
-          }
+            for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
+              const int u = ct + i * kConvThreads;
+              const int r = u >> 2, c = u & 3;
+              const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
+              uint4 o0, o1;
+              i8x4_to_bf16x4(qv.x, o0.x, o0.y);
+              i8x4_to_bf16x4(qv.y, o0.z, o0.w);
+              i8x4_to_bf16x4(qv.z, o1.x, o1.y);
+              i8x4_to_bf16x4(qv.w, o1.z, o1.w);
+              if constexpr (decltype(with_scale)::value) {
+                const int n = nb + r;
+                const uint32_t s = n < p.n_out ? gsc[(gsc_e + kb / p.group_kb) * p.n_out + n] : 0u;
+                const uint32_t s2 = s | (s << 16);
+                o0 = make_uint4(bf16x2_mul(o0.x, s2), bf16x2_mul(o0.y, s2), bf16x2_mul(o0.z, s2),
+                                bf16x2_mul(o0.w, s2));
+                o1 = make_uint4(bf16x2_mul(o1.x, s2), bf16x2_mul(o1.y, s2), bf16x2_mul(o1.z, s2),
+                                bf16x2_mul(o1.w, s2));
+              }
+              uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
+              *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = o0;
+              *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+            }
+          };
+          if (p.scale_groups > 1)
+            convert(std::true_type{});
+          else
+            convert(std::false_type{});
           fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
         }
         // Every converter warp of this CTA reaches this barrier each k-block and

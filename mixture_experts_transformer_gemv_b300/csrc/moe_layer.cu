@@ -267,6 +267,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.row_scale = nullptr;
     p.scale0 = L->w.w_scale;
     p.scale1 = L->w.wv_scale;
+    p.scale_experts = L->cfg.scale_experts;
+    p.scale_groups = L->cfg.scale_groups;
+    p.group_kb = d / L->cfg.scale_groups / kDq8BK;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     decode_gemm_i8_kernel<kEpiGeglu><<<L->num_sms, DecI8Cfg<kEpiGeglu>::kThreads, DecI8Cfg<kEpiGeglu>::kSmemBytes,
@@ -295,6 +298,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.row_scale = nullptr;
     p.scale0 = L->w.w_scale;
     p.scale1 = L->w.wv_scale;
+    p.scale_experts = L->cfg.scale_experts;
+    p.scale_groups = L->cfg.scale_groups;
+    p.group_kb = d / L->cfg.scale_groups / kGemmBK;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     if (int8)
@@ -317,6 +323,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.row_scale = L->prob_of_row;
     p.scale0 = L->w.w1_scale;
     p.scale1 = nullptr;
+    p.scale_experts = L->cfg.scale_experts;
+    p.scale_groups = L->cfg.scale_groups;
+    p.group_kb = F / L->cfg.scale_groups / kDq8BK;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     decode_gemm_i8_kernel<kEpiDown><<<L->num_sms, DecI8Cfg<kEpiDown>::kThreads, DecI8Cfg<kEpiDown>::kSmemBytes,
@@ -345,6 +354,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.row_scale = L->prob_of_row;
     p.scale0 = L->w.w1_scale;
     p.scale1 = nullptr;
+    p.scale_experts = L->cfg.scale_experts;
+    p.scale_groups = L->cfg.scale_groups;
+    p.group_kb = F / L->cfg.scale_groups / kGemmBK;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     if (int8)
@@ -421,6 +433,13 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (!(c.eps > 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be > 0");
   if (c.weight_dtype != MOE_WEIGHT_BF16 && c.weight_dtype != MOE_WEIGHT_INT8)
     return fail(MOE_ERR_INVALID_ARG, "unknown weight_dtype %d", c.weight_dtype);
+  if (c.scale_experts != 0 && c.scale_experts != 1 && c.scale_experts != kNumExperts)
+    return fail(MOE_ERR_INVALID_ARG, "scale_experts must be 0, 1 or 8 (got %d)", c.scale_experts);
+  if (c.scale_groups < 0) return fail(MOE_ERR_INVALID_ARG, "scale_groups < 0");
+  if (c.weight_dtype == MOE_WEIGHT_INT8 && c.scale_groups > 1 &&
+      (c.d_model % (128 * c.scale_groups) || c.d_ffn % (128 * c.scale_groups)))
+    return fail(MOE_ERR_UNSUPPORTED, "scale_groups = %d needs d_model and d_ffn to be multiples of %d",
+                c.scale_groups, 128 * c.scale_groups);
   if ((c.flags & MOE_FLAG_FORCE_GEMV) && (c.flags & MOE_FLAG_FORCE_TC))
     return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_FORCE_GEMV and MOE_FLAG_FORCE_TC are exclusive");
   const void* req[] = {w->gate, w->w, w->wv, w->w1, w->pre_norm_scale, w->post_norm_scale};
@@ -451,6 +470,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   auto* L = new (std::nothrow) moe_layer();
   if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
   L->cfg = c;
+  if (L->cfg.scale_experts == 0) L->cfg.scale_experts = kNumExperts;
+  if (L->cfg.scale_groups == 0) L->cfg.scale_groups = 1;
   L->w = *w;
   L->device = dev;
   L->num_sms = prop.multiProcessorCount;

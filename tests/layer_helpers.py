@@ -48,7 +48,7 @@ def device_weights(inp) -> dict:
 def make_layer(inp, max_tokens=None, flags=0, weights=None):
     weights = device_weights(inp) if weights is None else weights
     return moe.MoeLayer(inp.d, inp.F, max_tokens or inp.T, weights, eps=inp.eps, weight_dtype=inp.weight_dtype,
-                        flags=flags)
+                        flags=flags, scale_shape=(inp.scale_experts, inp.scale_groups))
 
 
 def run(layer, inp, x_dev=None):

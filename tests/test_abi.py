@@ -77,6 +77,9 @@ def _create(lib, cfg, w):
     (dict(weight_dtype=1), moe.MOE_ERR_INVALID_ARG),  # int8 weights without their scales
     (dict(weight_dtype=1, flags=moe.MOE_FLAG_FORCE_GEMV), moe.MOE_ERR_INVALID_ARG),  # no scales
     (dict(flags=moe.MOE_FLAG_FORCE_GEMV | moe.MOE_FLAG_FORCE_TC), moe.MOE_ERR_INVALID_ARG),
+    (dict(weight_dtype=1, scale_experts=3), moe.MOE_ERR_INVALID_ARG),
+    (dict(weight_dtype=1, scale_groups=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(weight_dtype=1, scale_groups=4), moe.MOE_ERR_UNSUPPORTED),  # d = 256 is not a multiple of 128 x 4
 ])
 def test_create_rejects_bad_config(lib, kw, status):
     s, h = _create(lib, _cfg(**kw), _fake_weights())

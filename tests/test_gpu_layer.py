@@ -361,3 +361,18 @@ def test_router_stats_needs_a_forward():
         layer.router_stats()
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG
     layer.close()
+
+
+
+# ------------------------------------------------------- int8 scale shapes
+# The model card lists scale shapes (8,1,N), (8,8,N), (1,N) and (8,N) ("Conversion
+# Details"); read as (E_s, G, N) = (8,1), (8,8), (1,1), (1,8).  G > 1 scales vary
+# along the reduction and are applied to the weights as they are converted (one
+# bf16 or fp16 rounding); G == 1 scales multiply the fp32 result.
+
+@pytest.mark.parametrize("shape", [(8, 8), (1, 1), (1, 8), (8, 2)])
+@pytest.mark.parametrize("T,flags", [(200, 0), (8, 0), (8, moe.MOE_FLAG_FORCE_TC)])
+def test_int8_scale_shapes(shape, T, flags):
+    inp = synth.make_inputs(T, 1024, 1024, 90 + shape[0] + shape[1], name=f"int8_scales_{shape}",
+                            weight_dtype="int8", int8_scale_shape=shape)
+    _full_check(inp, flags=flags)
