@@ -376,3 +376,32 @@ def test_int8_scale_shapes(shape, T, flags):
     inp = synth.make_inputs(T, 1024, 1024, 90 + shape[0] + shape[1], name=f"int8_scales_{shape}",
                             weight_dtype="int8", int8_scale_shape=shape)
     _full_check(inp, flags=flags)
+
+
+def test_forward_captured_in_a_cuda_graph():
+    """moe_layer_forward reads nothing back to the host, so it can be captured in
+    a CUDA graph: replaying the graph on new inputs must give what direct calls give."""
+    inp = synth.make_inputs(64, 256, 512, 95, name="graph")
+    layer = make_layer(inp)
+    x = bf16_tensor(inp.x)
+    x_static = x.clone()
+    out_static = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x_static, out=out_static, stream=s)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(x_static, out=out_static, stream=s)
+    x2 = torch.roll(x, shifts=5, dims=0).contiguous()
+    for xin in (x, x2):
+        x_static.copy_(xin)
+        g.replay()
+        torch.cuda.synchronize()
+        layer.sync_status()
+        direct = layer.forward(xin)
+        torch.cuda.synchronize()
+        assert torch.equal(out_static, direct)
+    layer.close()
