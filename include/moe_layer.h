@@ -216,8 +216,8 @@ typedef struct {
   int32_t* counts;      /* [E] tokens per expert */
   int32_t* row_offset;  /* [E + 1] first permuted row of each expert (multiples of 128) */
   int32_t* row_of_slot; /* [max_tokens, 2] permuted row of (token, rank) */
-  void* xn_perm;        /* [rows_cap, d] bf16: normed rows in expert order */
-  void* act;            /* [rows_cap, F] bf16: GELU(h) * v per permuted row */
+  void* xn_perm;        /* [rows_cap, d] bf16 (fp16 for int8 weights): normed rows in expert order */
+  void* act;            /* [rows_cap, F] bf16 (fp16 for int8 weights): GELU(h) * v per permuted row */
   float* y_rows;        /* [rows_cap, d] fp32: p * (W1 act) per permuted row */
   int64_t rows_cap;     /* capacity in permuted rows */
 } moe_workspace_view_t;

@@ -75,26 +75,6 @@ struct DecI8Cfg {
 constexpr uint32_t kDq8Idesc = (1u << 4) | (static_cast<uint32_t>(kDecNS >> 3) << 17) |
                                (static_cast<uint32_t>(kDecBM >> 4) << 24);
 
-// 4 int8 (one 32-bit word, element i in byte i) -> 4 fp16 in two words, exact:
-// u = q + 128 (sign bit flipped) in the low byte of the fp16 pattern 0x64uu is
-// 1024 + u, and subtracting 1152 leaves q.
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  lo = f16x2_sub(__byte_perm(u, 0x64u, 0x4140), 0x64806480u);
-  hi = f16x2_sub(__byte_perm(u, 0x64u, 0x4342), 0x64806480u);
-}
-
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 __device__ __forceinline__ uint16_t f16_sat(float v) {
   uint16_t r;
   asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(r) : "f"(v));

@@ -29,7 +29,7 @@
 //               of its own TMA stages to the even CTA's barrier.
 //   warps 2-5   epilogue of the CTA's 128 rows: tcgen05.ld, GeGLU or scaling,
 //               stores; then tell the even CTA's MMA warp the accumulator is free
-//   warps 6-13  int8 weights only: int8 -> bf16 conversion of the CTA's B half
+//   warps 6-13  int8 weights only: int8 -> fp16 conversion of the CTA's B half
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap the
 // mainloop of tile i+1.
 //
@@ -41,13 +41,17 @@
 // int8 weights ("TevunahAi/Grok-1-BF16", "Conversion Details": int8 values
 // with bf16 scales, one per expert and output channel for the (8, 1, N) scale
 // shape): TMA brings the CTA's raw int8 B half into a staging buffer; the
-// converter warps rewrite it as bf16 in the 128-byte-swizzled K-major layout
-// the MMA reads (|q| <= 127 is exact in bf16), make it visible to the tensor
-// core's async proxy and tell the even CTA's MMA warp.  Because the scale
+// converter warps rewrite it as fp16 in the 128-byte-swizzled K-major layout
+// the MMA reads (exact: one byte shuffle and one subtraction per pair), make it
+// visible to the tensor core's async proxy and tell the even CTA's MMA warp.
+// The MMA then runs on fp16 operands, so an int8 layer carries its activation
+// rows in fp16 (the gather writes them, the up projection's epilogue writes the
+// GeGLU activations, saturating at +-65504); fp16 has 3 more mantissa bits than
+// bf16, and its conversion takes half the integer work, which set the rate.  Because the scale
 // belongs to an output channel it factors out of the reduction and is applied
 // in fp32 in the epilogue: sum_k a_k (q_nk s_n) = s_n sum_k a_k q_nk.  Scales that
 // also vary along k (G > 1 groups) do not factor out; the converters then
-// multiply each converted weight by its group's scale (bf16x2, one rounding).
+// multiply each converted weight by its group's scale (f16x2, one rounding).
 //
 // Every wait is bounded (wait_bounded).  A role that times out raises its CTA's
 // abort flag and the device error word; the others stop at their next wait
@@ -78,6 +82,9 @@ constexpr int kBTileBytes = kGemmHalfN * kGemmBK * 2;   // 16 KB (bf16, swizzled
 constexpr int kB8TileBytes = kGemmHalfN * kGemmBK;      // 8 KB (int8 staging, dense rows of 64 B)
 constexpr uint32_t kTmemCols = 2 * kGemmBN;              // two fp32 accumulators of 128 x 256 per CTA
 constexpr uint32_t kGemmIdesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+// int8 weights: the same MMA with fp16 A and B (format 0 in bits 7-9 and 10-12)
+constexpr uint32_t kGemmIdescF16 = (1u << 4) | (static_cast<uint32_t>(kGemmBN >> 3) << 17) |
+                                   (static_cast<uint32_t>(kGemmBM >> 4) << 24);
 static_assert(kGemmBM == kRowTile, "expert row blocks are whole tiles");
 
 // Per weight type:
@@ -137,27 +144,24 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExp
   return c;
 }
 
-// 4 int8 (one 32-bit word, element i in byte i) -> 4 bf16 in two words, exact,
-// with integer byte shuffles and one bf16x2 subtraction per pair.  For the
-// two's-complement byte q = m - 128 s (m = low 7 bits, s = sign bit), the bf16
-// with high byte 0x43 and low byte m is 128 + m, and with low byte 0x80 s it is
-// 128 + 128 s; their difference is q, exactly representable, so the
-// subtraction is exact.
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+// 4 int8 (one 32-bit word, element i in byte i) -> 4 fp16 in two words, exact:
+// u = q + 128 (sign bit flipped) in the low byte of the fp16 pattern 0x64uu is
+// 1024 + u, and subtracting 1152 leaves q.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   uint32_t r;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = f16x2_sub(__byte_perm(u, 0x64u, 0x4140), 0x64806480u);
+  hi = f16x2_sub(__byte_perm(u, 0x64u, 0x4342), 0x64806480u);
 }
-__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t m = w & 0x7F7F7F7Fu;
-  const uint32_t s = w & 0x80808080u;
-  lo = bf16x2_sub(__byte_perm(m, 0x43u, 0x4140), __byte_perm(s, 0x43u, 0x4140));
-  hi = bf16x2_sub(__byte_perm(m, 0x43u, 0x4342), __byte_perm(s, 0x43u, 0x4342));
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // 8 bf16 scales (16 bytes of bf16 bits) -> fp32.
@@ -313,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sB + (WQ ? bstage : stage) * kBTileBytes));
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
-            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kGemmIdesc, (kb | kk) != 0);
+            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, WQ ? kGemmIdescF16 : kGemmIdesc, (kb | kk) != 0);
           umma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == (uint32_t)C::kStages) {
             stage = 0;
@@ -403,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           for (int j = 0; j < 16; ++j) {
             const float a0 = gelu_tanh(__uint_as_float(h[2 * j])) * __uint_as_float(v[2 * j]);
             const float a1 = gelu_tanh(__uint_as_float(h[2 * j + 1])) * __uint_as_float(v[2 * j + 1]);
-            pk[j] = pack_bf16x2(a0, a1);
+            pk[j] = WQ ? pack_f16x2_sat(a0, a1) : pack_bf16x2(a0, a1);  // int8 layers carry fp16 rows
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -453,9 +457,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       if (acc == 0) acc_phase ^= 1u;
     }
   } else if (WQ) {
-    // -------------------------------------------------- int8 -> bf16 converter
+    // -------------------------------------------------- int8 -> fp16 converter
     // Staging tile: 128 rows x 64 int8, row r at byte 64 r.  MMA tile: 128 rows x
-    // 64 bf16 in 128-byte swizzle atoms of 8 rows: element (r, k) at
+    // 64 fp16 in 128-byte swizzle atoms of 8 rows: element (r, k) at
     // (r / 8) * 1024 + (r % 8) * 128 + ((k / 8) ^ (r % 8)) * 16 + (k % 8) * 2.
     const int ct = threadIdx.x - kConvWarp0 * 32;
     uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
@@ -482,18 +486,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
               const int r = u >> 2, c = u & 3;
               const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
               uint4 o0, o1;
-              i8x4_to_bf16x4(qv.x, o0.x, o0.y);
-              i8x4_to_bf16x4(qv.y, o0.z, o0.w);
-              i8x4_to_bf16x4(qv.z, o1.x, o1.y);
-              i8x4_to_bf16x4(qv.w, o1.z, o1.w);
+              i8x4_to_f16x4(qv.x, o0.x, o0.y);
+              i8x4_to_f16x4(qv.y, o0.z, o0.w);
+              i8x4_to_f16x4(qv.z, o1.x, o1.y);
+              i8x4_to_f16x4(qv.w, o1.z, o1.w);
               if constexpr (decltype(with_scale)::value) {
                 const int n = nb + r;
-                const uint32_t s = n < p.n_out ? gsc[(gsc_e + kb / p.group_kb) * p.n_out + n] : 0u;
-                const uint32_t s2 = s | (s << 16);
-                o0 = make_uint4(bf16x2_mul(o0.x, s2), bf16x2_mul(o0.y, s2), bf16x2_mul(o0.z, s2),
-                                bf16x2_mul(o0.w, s2));
-                o1 = make_uint4(bf16x2_mul(o1.x, s2), bf16x2_mul(o1.y, s2), bf16x2_mul(o1.z, s2),
-                                bf16x2_mul(o1.w, s2));
+                const uint32_t sb = n < p.n_out ? gsc[(gsc_e + kb / p.group_kb) * p.n_out + n] : 0u;
+                __half2 sh = __float2half2_rn(__uint_as_float(sb << 16));
+                const uint32_t s2 = *reinterpret_cast<uint32_t*>(&sh);
+                o0 = make_uint4(f16x2_mul(o0.x, s2), f16x2_mul(o0.y, s2), f16x2_mul(o0.z, s2), f16x2_mul(o0.w, s2));
+                o1 = make_uint4(f16x2_mul(o1.x, s2), f16x2_mul(o1.y, s2), f16x2_mul(o1.z, s2), f16x2_mul(o1.w, s2));
               }
               uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
               *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = o0;

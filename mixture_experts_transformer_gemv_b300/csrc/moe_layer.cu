@@ -250,10 +250,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   mark(2);
   {
     const int grid = (int)std::min<int64_t>(L->rows_cap, (int64_t)L->num_sms * 8);
-    // the int8 weight-streaming kernels multiply in fp16 (int8 -> fp16 is one
-    // shuffle and one subtraction), so their activation rows are fp16
-    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, decode && int8 ? 1 : 0,
-                                             L->xn_perm);
+    // int8 layers multiply in fp16 (int8 -> fp16 is one shuffle and one
+    // subtraction), so their activation rows are fp16
+    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, int8 ? 1 : 0, L->xn_perm);
   }
   mark(3);
   if (decode && int8) {

@@ -274,7 +274,7 @@ def test_int8_intermediates_match_oracle():
     layer = make_layer(inp)
     run(layer, inp)
     ws = layer.workspace()
-    act = read_device(ws.act, (ws.rows_cap, inp.F), torch.bfloat16)
+    act = read_device(ws.act, (ws.rows_cap, inp.F), torch.float16)  # int8 layers carry fp16 rows
     yr = read_device(ws.y_rows, (ws.rows_cap, inp.d), torch.float32)
     ros = read_device(ws.row_of_slot, (inp.T, 2), torch.int32)
     r = oracle.route(inp, keep_xn=True)
