@@ -148,6 +148,26 @@ moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* hidden_host,
                                     void* stream, int32_t* topk_idx_host, float* topk_prob_host,
                                     int32_t* expert_counts_host);
 
+/*
+ * Same as moe_layer_forward_host, but asynchronous, so that a caller serving a
+ * stream of batches overlaps the copies of one call with the layer of another.
+ * The input copy runs on an internal copy stream, the layer on `stream` (after
+ * the input landed), and the output copies on a second internal copy stream.
+ * Two device staging slots are used in turn (allocated with the copy streams
+ * on the first call): a call reuses a slot only after the output copies of the
+ * call two before it finished.  The host buffers must stay untouched until
+ * moe_layer_host_wait returns (pinned memory is needed for the copies to
+ * overlap anything).  Argument errors return at once; device errors are
+ * reported by moe_layer_host_wait.
+ */
+moe_status_t moe_layer_forward_host_async(moe_layer_t* layer, const void* hidden_host, void* out_host, int32_t T,
+                                          void* stream, int32_t* topk_idx_host, float* topk_prob_host,
+                                          int32_t* expert_counts_host);
+
+/* Wait for every moe_layer_forward_host_async call on this handle (their output
+ * copies) and for `stream`; then as moe_layer_sync_status. */
+moe_status_t moe_layer_host_wait(moe_layer_t* layer, void* stream);
+
 /* Wait for `stream`, then return (and clear) the first device-side error any
  * earlier forward on this handle latched: MOE_OK, MOE_ERR_TIMEOUT,
  * MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */

@@ -67,6 +67,10 @@ def lib():
         L.moe_layer_forward.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp]
         L.moe_layer_forward_host.restype = i32
         L.moe_layer_forward_host.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp]
+        L.moe_layer_forward_host_async.restype = i32
+        L.moe_layer_forward_host_async.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp]
+        L.moe_layer_host_wait.restype = i32
+        L.moe_layer_host_wait.argtypes = [vp, vp]
         L.moe_layer_sync_status.restype = i32
         L.moe_layer_sync_status.argtypes = [vp, vp]
         L.moe_layer_destroy.restype = i32
@@ -215,6 +219,21 @@ class MoeLayer:
         out = torch.empty(10, dtype=torch.float32, device=torch.device("cuda", self._dev))
         _check(lib().moe_layer_router_stats(self._h, out.data_ptr(), _stream_handle(stream)), "moe_layer_router_stats")
         return out
+
+    def forward_host_async(self, hidden_host, out_host, stream=None):
+        """moe_layer_forward_host_async: enqueue the layer on HOST tensors (pinned)
+        and return at once; call host_wait() before touching the buffers."""
+        import torch
+        if hidden_host.is_cuda or hidden_host.dtype != torch.bfloat16 or not hidden_host.is_contiguous():
+            raise ValueError("hidden_host must be a contiguous CPU bf16 tensor")
+        if out_host.is_cuda or out_host.dtype != torch.bfloat16 or not out_host.is_contiguous():
+            raise ValueError("out_host must be a contiguous CPU bf16 tensor")
+        _check(lib().moe_layer_forward_host_async(self._h, hidden_host.data_ptr(), out_host.data_ptr(),
+                                                  hidden_host.shape[0], _stream_handle(stream), None, None, None),
+               "moe_layer_forward_host_async")
+
+    def host_wait(self, stream=None):
+        _check(lib().moe_layer_host_wait(self._h, _stream_handle(stream)), "moe_layer_host_wait")
 
     def sync_status(self, stream=None):
         _check(lib().moe_layer_sync_status(self._h, _stream_handle(stream)), "moe_layer_sync_status")

@@ -174,6 +174,13 @@ struct moe_layer {
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
   size_t host_stage_bytes = 0;
 
+  // moe_layer_forward_host_async: two device staging slots, copy streams and events
+  void* async_stage[2] = {nullptr, nullptr};
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t in_ready[2] = {}, fwd_done[2] = {}, slot_free[2] = {};
+  int async_slot = 0;
+  bool async_pending = false;
+
   bool profiling = false;
   std::vector<std::array<cudaEvent_t, MOE_K_COUNT + 1>> ring;
   std::vector<bool> pending;
@@ -603,6 +610,14 @@ moe_status_t moe_layer_destroy(moe_layer_t* L) {
       if (ev) cudaEventDestroy(ev);
   if (L->ws) cudaFree(L->ws);
   if (L->host_stage) cudaFree(L->host_stage);
+  for (int i = 0; i < 2; ++i) {
+    if (L->async_stage[i]) cudaFree(L->async_stage[i]);
+    if (L->in_ready[i]) cudaEventDestroy(L->in_ready[i]);
+    if (L->fwd_done[i]) cudaEventDestroy(L->fwd_done[i]);
+    if (L->slot_free[i]) cudaEventDestroy(L->slot_free[i]);
+  }
+  if (L->copy_in) cudaStreamDestroy(L->copy_in);
+  if (L->copy_out) cudaStreamDestroy(L->copy_out);
   delete L;
   return ok();
 }
@@ -675,6 +690,77 @@ moe_status_t moe_layer_forward_host(moe_layer_t* L, const void* hidden_host, voi
     MOE_CUDA_TRY(cudaMemcpyAsync(topk_prob_host, ps, (size_t)T * 8, cudaMemcpyDeviceToHost, st));
   if (expert_counts_host)
     MOE_CUDA_TRY(cudaMemcpyAsync(expert_counts_host, cs, kNumExperts * 4, cudaMemcpyDeviceToHost, st));
+  return moe_layer_sync_status(L, stream);
+}
+
+// Device staging of one asynchronous host call: x [max_T, d] bf16 (in place),
+// topk_idx, topk_prob [max_T, 2], counts [E].
+static size_t async_slot_bytes(const moe_layer* L, size_t* x_bytes, size_t* ip_bytes) {
+  const size_t d = (size_t)L->cfg.d_model, maxT = (size_t)L->cfg.max_tokens;
+  *x_bytes = align_up(maxT * d * 2, 1024);
+  *ip_bytes = align_up(maxT * 2 * 4, 1024);
+  return *x_bytes + 2 * *ip_bytes + 1024;
+}
+
+moe_status_t moe_layer_forward_host_async(moe_layer_t* L, const void* hidden_host, void* out_host, int32_t T,
+                                          void* stream, int32_t* topk_idx_host, float* topk_prob_host,
+                                          int32_t* expert_counts_host) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  if (T < 0 || T > L->cfg.max_tokens) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, L->cfg.max_tokens);
+  if (T == 0) return ok();
+  if (!hidden_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "null host buffer");
+  DeviceGuard g(L->device);
+  if (!g.ok) return fail(MOE_ERR_CUDA, "cannot select device %d", L->device);
+  size_t x_bytes = 0, ip_bytes = 0;
+  const size_t need = async_slot_bytes(L, &x_bytes, &ip_bytes);
+  if (!L->copy_in) {  // first call: two staging slots, two copy streams, events
+    for (int i = 0; i < 2; ++i) {
+      MOE_CUDA_TRY(cudaMalloc(&L->async_stage[i], need));
+      MOE_CUDA_TRY(cudaEventCreateWithFlags(&L->in_ready[i], cudaEventDisableTiming));
+      MOE_CUDA_TRY(cudaEventCreateWithFlags(&L->fwd_done[i], cudaEventDisableTiming));
+      MOE_CUDA_TRY(cudaEventCreateWithFlags(&L->slot_free[i], cudaEventDisableTiming));
+    }
+    MOE_CUDA_TRY(cudaStreamCreateWithFlags(&L->copy_out, cudaStreamNonBlocking));
+    MOE_CUDA_TRY(cudaStreamCreateWithFlags(&L->copy_in, cudaStreamNonBlocking));
+  }
+  const int slot = L->async_slot;
+  L->async_slot ^= 1;
+  char* b = static_cast<char*>(L->async_stage[slot]);
+  void* xs = b;
+  int32_t* is = reinterpret_cast<int32_t*>(b + x_bytes);
+  float* ps = reinterpret_cast<float*>(b + x_bytes + ip_bytes);
+  int32_t* cs = reinterpret_cast<int32_t*>(b + x_bytes + 2 * ip_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t nb = (size_t)T * L->cfg.d_model * 2;
+  // input copy once this slot's previous output copy is done (slot_free), the
+  // forward on the caller's stream once the input landed, the output copy once
+  // the forward is done; consecutive calls overlap one's copies with the
+  // other's forward
+  if (L->async_pending) MOE_CUDA_TRY(cudaStreamWaitEvent(L->copy_in, L->slot_free[slot], 0));
+  MOE_CUDA_TRY(cudaMemcpyAsync(xs, hidden_host, nb, cudaMemcpyHostToDevice, L->copy_in));
+  MOE_CUDA_TRY(cudaEventRecord(L->in_ready[slot], L->copy_in));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(st, L->in_ready[slot], 0));
+  moe_status_t s = enqueue_forward(L, xs, xs, T, st, topk_idx_host ? is : nullptr, topk_prob_host ? ps : nullptr,
+                                   expert_counts_host ? cs : nullptr);
+  if (s != MOE_OK) return s;
+  MOE_CUDA_TRY(cudaEventRecord(L->fwd_done[slot], st));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(L->copy_out, L->fwd_done[slot], 0));
+  MOE_CUDA_TRY(cudaMemcpyAsync(out_host, xs, nb, cudaMemcpyDeviceToHost, L->copy_out));
+  if (topk_idx_host)
+    MOE_CUDA_TRY(cudaMemcpyAsync(topk_idx_host, is, (size_t)T * 8, cudaMemcpyDeviceToHost, L->copy_out));
+  if (topk_prob_host)
+    MOE_CUDA_TRY(cudaMemcpyAsync(topk_prob_host, ps, (size_t)T * 8, cudaMemcpyDeviceToHost, L->copy_out));
+  if (expert_counts_host)
+    MOE_CUDA_TRY(cudaMemcpyAsync(expert_counts_host, cs, kNumExperts * 4, cudaMemcpyDeviceToHost, L->copy_out));
+  MOE_CUDA_TRY(cudaEventRecord(L->slot_free[slot], L->copy_out));
+  L->async_pending = true;
+  return ok();
+}
+
+moe_status_t moe_layer_host_wait(moe_layer_t* L, void* stream) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "null layer");
+  DeviceGuard g(L->device);
+  if (L->copy_out) MOE_CUDA_TRY(cudaStreamSynchronize(L->copy_out));
   return moe_layer_sync_status(L, stream);
 }
 

@@ -107,6 +107,25 @@ def test_in_place_and_host_entry_point():
     assert counts.sum().item() == 2 * inp.T
 
 
+def test_async_host_calls_match_device_calls():
+    """Four moe_layer_forward_host_async calls in flight on alternating staging
+    slots: each output equals a device-buffer forward of the same input."""
+    inp = synth.make_inputs(96, 256, 512, 96, name="async")
+    layer = make_layer(inp)
+    x = bf16_tensor(inp.x)
+    xs = [torch.roll(x, shifts=7 * i, dims=0).contiguous() for i in range(4)]
+    xh = [t.cpu().pin_memory() for t in xs]
+    oh = [torch.empty_like(h).pin_memory() for h in xh]
+    for h, o in zip(xh, oh):
+        layer.forward_host_async(h, o)
+    layer.host_wait()
+    for t, o in zip(xs, oh):
+        direct = layer.forward(t)
+        torch.cuda.synchronize()
+        assert torch.equal(o, direct.cpu())
+    layer.close()
+
+
 def test_token_permutation():
     inp = synth.make_inputs(400, 256, 512, 40, name="perm")
     layer = make_layer(inp)
