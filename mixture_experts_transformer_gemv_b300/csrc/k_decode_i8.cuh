@@ -14,9 +14,10 @@
 // Data path per k-block of 128: TMA brings the int8 weight tile(s) (128 x 128,
 // 128-byte swizzle: whole 128-byte rows, the granule the bf16 kernels stream at
 // full HBM speed; 64-byte rows measured at two thirds of it) and the slot rows
-// (16 x 128, two 128-byte-swizzled boxes) into a deep shared-memory ring; sixteen converter warps turn each weight row into 64 fp16
-// and store them straight into Tensor Memory with tcgen05.st, where the MMA
-// reads its A operand (tcgen05.mma with A in TMEM).  The converted weights never
+// (16 x 128, two 128-byte-swizzled boxes) into a deep shared-memory ring;
+// sixteen converter warps turn each weight row into fp16 and store it straight
+// into Tensor Memory with tcgen05.st, where the MMA reads its A operand
+// (tcgen05.mma with A in TMEM).  The converted weights never
 // go back through shared memory, so shared memory carries only the int8 bytes
 // and the slot rows.
 //
