@@ -15,6 +15,8 @@ route(inp)                       -> Route (xn, p, idx, w) for all T tokens
 routing_stats(p)                 -> mean probability per expert, routing entropy, collapse index
 moe_tokens(inp, tokens)          -> Layer (y, m, idx, w, p) for a token subset
 expert_ffn(inp, xn, e)           -> (h, v, a, o) of one expert on one vector
+attn_tokens(inp, tokens)         -> (y, ctx) of the attention block for a token subset
+rope(v, pos, base)               -> rotary embedding of one head vector
 dequant(q, scale, scale_E, scale_G) -> fp32 [E, N, K] dequantised weights
 gelu_tanh(u), rmsnorm(v, s, eps)
 """
@@ -71,6 +73,11 @@ def _load():
         lib.oracle_moe_tokens.restype = None
         lib.oracle_moe_tokens.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, dbl, i32, vp, vp, vp,
                                           vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.oracle_rope.restype = None
+        lib.oracle_rope.argtypes = [i64, vp, i64, dbl]
+        lib.oracle_attn_tokens.restype = None
+        lib.oracle_attn_tokens.argtypes = [i64, vp, i64, i64, i64, i64, i64, vp, vp, vp, dbl, vp, vp, vp, vp,
+                                           dbl, dbl, vp, vp]
         _lib = lib
     return _lib
 
@@ -212,3 +219,26 @@ def near_order_tie_tokens(p: np.ndarray, band: float = 1e-6) -> np.ndarray:
     rank order is compared as a set only)."""
     s = -np.sort(-p, axis=1)
     return (s[:, 0] - s[:, 1]) < band
+
+
+def rope(v: np.ndarray, pos: int, base: float = 10000.0) -> np.ndarray:
+    """Rotary embedding of one head vector (pairs (2i, 2i + 1)) at position pos."""
+    out = np.array(v, dtype=np.float64, copy=True, order="C")
+    _load().oracle_rope(out.size, _p(out), int(pos), float(base))
+    return out
+
+
+def attn_tokens(inp, tokens: Optional[Sequence[int]] = None, want_ctx: bool = False):
+    """Attention block y = x + RMSNorm_post(Wo attn(RMSNorm_pre(x))) of one causal
+    sequence, for a subset of its tokens (all when None).  Returns (tok, y, ctx);
+    ctx [n, Hq Dh] is the attention output before Wo (None unless asked for)."""
+    tok = np.arange(inp.T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    n = tok.size
+    assert n == 0 or (tok.min() >= 0 and tok.max() < inp.T)
+    y = np.empty((n, inp.d), np.float64)
+    ctx = np.empty((n, inp.Hq * inp.Dh), np.float64) if want_ctx else None
+    if n:
+        _load().oracle_attn_tokens(n, _p(tok), inp.T, inp.d, inp.Hq, inp.Hkv, inp.Dh, _p(inp.x), _p(inp.s_pre),
+                                   _p(inp.s_post), inp.eps, _p(inp.wq), _p(inp.wk), _p(inp.wv), _p(inp.wo),
+                                   inp.rope_base, inp.clamp, _p(y), _p(ctx))
+    return tok, y, ctx

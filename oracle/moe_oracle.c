@@ -286,3 +286,139 @@ void oracle_moe_tokens(int64_t n_tok, const int64_t* tok, int64_t d, int64_t F, 
       y[i * d + j] = (double)bf16_bits_to_float(x_row[j]) + m[j] * rr * (double)s_post[j];
   }
 }
+
+/* ===================================================================== */
+/* Attention half of a Grok-1 decoder layer (the block before the MoE one).
+ *
+ * Sources (page title, section): "Jah-yee/grok" README, architecture diagram
+ * (GQA with 48 query and 8 key/value heads, rotary position embeddings,
+ * RMSNorm) and references (Su et al., "RoFormer: Enhanced Transformer with
+ * Rotary Position Embedding"); "TevunahAi/Grok-1-BF16" model card, "Grok-1
+ * Specific Behaviors" (attention logits hard-clamped to [-30, 30] before the
+ * softmax; pre- and post-attention norms) and "Weight Verification" (q_proj
+ * [6144, 6144], k_proj and v_proj [1024, 6144], o_proj [6144, 6144] in
+ * PyTorch [out, in] order, so the head dimension is 6144 / 48 = 128).
+ *
+ * For one causal sequence x [T, d] and every requested token t:
+ *   xn_t  = RMSNorm_pre(x_t)
+ *   q_t   = RoPE_t(Wq xn_t),  k_j = RoPE_j(Wk xn_j),  v_j = Wv xn_j   (per head)
+ *   s_hj  = clamp(<q_t,h, k_j,g(h)> / sqrt(Dh), -c, c),  j = 0..t,  g(h) = h / (Hq / Hkv)
+ *   ctx_h = sum_j softmax_j(s_h) v_j,g(h)
+ *   y_t   = x_t + RMSNorm_post(Wo ctx_t)
+ * Readings where the pages are silent: RoPE as in RoFormer, rotating the
+ * pairs (2i, 2i + 1) of each head by angle pos * base^(-2i / Dh), base 10000;
+ * logits scaled by 1/sqrt(Dh) before the clamp; a causal mask; query head h
+ * uses key/value head h / (Hq / Hkv); head h is rows [Dh h, Dh (h + 1)) of the
+ * projection; the residual around the post-norm as in the MoE half. */
+
+/* RoPE of one head vector v [Dh] at position pos, in place. */
+void oracle_rope(int64_t Dh, double* v, int64_t pos, double base) {
+  for (int64_t i = 0; i < Dh / 2; ++i) {
+    const double theta = pow(base, -2.0 * (double)i / (double)Dh);
+    const double a = (double)pos * theta;
+    const double c = cos(a), s = sin(a);
+    const double x0 = v[2 * i], x1 = v[2 * i + 1];
+    v[2 * i] = x0 * c - x1 * s;
+    v[2 * i + 1] = x0 * s + x1 * c;
+  }
+}
+
+/* xn = x_row / sqrt(mean(x_row^2) + eps) * s  (x_row bf16 bits) */
+static void rmsnorm_bf16_row(int64_t d, const uint16_t* x_row, const float* s, double eps, double* xn) {
+  double ss = 0.0;
+  for (int64_t j = 0; j < d; ++j) {
+    const double v = (double)bf16_bits_to_float(x_row[j]);
+    ss += v * v;
+  }
+  const double r = 1.0 / sqrt(ss / (double)d + eps);
+  for (int64_t j = 0; j < d; ++j) xn[j] = (double)bf16_bits_to_float(x_row[j]) * r * (double)s[j];
+}
+
+/* out[n] = sum_k W[n, k] v[k] for a bf16 matrix W [N, K] */
+static void matvec_bf16(int64_t N, int64_t K, const uint16_t* W, const double* v, double* out) {
+  for (int64_t n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) acc += (double)bf16_bits_to_float(W[n * K + k]) * v[k];
+    out[n] = acc;
+  }
+}
+
+/* y [n_tok, d] of the attention block for the tokens tok[] of the sequence x [T, d];
+ * ctx_out [n_tok, Hq Dh] (attention output before o_proj) may be NULL. */
+void oracle_attn_tokens(int64_t n_tok, const int64_t* tok, int64_t T, int64_t d, int64_t Hq, int64_t Hkv,
+                        int64_t Dh, const uint16_t* x, const float* s_pre, const float* s_post, double eps,
+                        const uint16_t* wq, const uint16_t* wk, const uint16_t* wv, const uint16_t* wo,
+                        double rope_base, double clamp_c, double* y, double* ctx_out) {
+  (void)T;
+  int64_t tmax = 0;
+  for (int64_t i = 0; i < n_tok; ++i)
+    if (tok[i] > tmax) tmax = tok[i];
+  const int64_t nk = tmax + 1, kvw = Hkv * Dh, qw = Hq * Dh, group = Hq / Hkv;
+  double* K = (double*)malloc((size_t)(nk * kvw) * sizeof(double));
+  double* V = (double*)malloc((size_t)(nk * kvw) * sizeof(double));
+#pragma omp parallel
+  {
+    double* xn = (double*)malloc((size_t)d * sizeof(double));
+#pragma omp for schedule(static)
+    for (int64_t t = 0; t < nk; ++t) {
+      rmsnorm_bf16_row(d, x + t * d, s_pre, eps, xn);
+      matvec_bf16(kvw, d, wk, xn, K + t * kvw);
+      matvec_bf16(kvw, d, wv, xn, V + t * kvw);
+      for (int64_t g = 0; g < Hkv; ++g) oracle_rope(Dh, K + t * kvw + g * Dh, t, rope_base);
+    }
+    free(xn);
+  }
+#pragma omp parallel
+  {
+    double* xn = (double*)malloc((size_t)d * sizeof(double));
+    double* q = (double*)malloc((size_t)qw * sizeof(double));
+    double* ctx = (double*)malloc((size_t)qw * sizeof(double));
+    double* sc = (double*)malloc((size_t)nk * sizeof(double));
+    double* o = (double*)malloc((size_t)d * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_tok; ++i) {
+      const int64_t t = tok[i];
+      rmsnorm_bf16_row(d, x + t * d, s_pre, eps, xn);
+      matvec_bf16(qw, d, wq, xn, q);
+      for (int64_t h = 0; h < Hq; ++h) oracle_rope(Dh, q + h * Dh, t, rope_base);
+      for (int64_t h = 0; h < Hq; ++h) {
+        const int64_t g = h / group;
+        double mx = -INFINITY;
+        for (int64_t j = 0; j <= t; ++j) {
+          double s = 0.0;
+          for (int64_t c = 0; c < Dh; ++c) s += q[h * Dh + c] * K[j * kvw + g * Dh + c];
+          s /= sqrt((double)Dh);
+          if (s > clamp_c) s = clamp_c;
+          if (s < -clamp_c) s = -clamp_c;
+          sc[j] = s;
+          if (s > mx) mx = s;
+        }
+        double z = 0.0;
+        for (int64_t j = 0; j <= t; ++j) {
+          sc[j] = exp(sc[j] - mx);
+          z += sc[j];
+        }
+        for (int64_t c = 0; c < Dh; ++c) {
+          double acc = 0.0;
+          for (int64_t j = 0; j <= t; ++j) acc += sc[j] * V[j * kvw + g * Dh + c];
+          ctx[h * Dh + c] = acc / z;
+        }
+      }
+      if (ctx_out)
+        for (int64_t c = 0; c < qw; ++c) ctx_out[i * qw + c] = ctx[c];
+      matvec_bf16(d, qw, wo, ctx, o);
+      double ss = 0.0;
+      for (int64_t n = 0; n < d; ++n) ss += o[n] * o[n];
+      const double rr = 1.0 / sqrt(ss / (double)d + eps);
+      for (int64_t n = 0; n < d; ++n)
+        y[i * d + n] = (double)bf16_bits_to_float(x[t * d + n]) + o[n] * rr * (double)s_post[n];
+    }
+    free(xn);
+    free(q);
+    free(ctx);
+    free(sc);
+    free(o);
+  }
+  free(K);
+  free(V);
+}

@@ -244,3 +244,74 @@ def workload(name: str, T: Optional[int] = None) -> MoeInputs:
     if name == "skew":
         return make_inputs(T or 4096, GROK_D, GROK_F, seed, name=name, bias=SKEW_BIAS)
     raise KeyError(name)
+
+
+# ----------------------------------------------------------------------------
+# Attention half of the decoder layer (GQA with rotary embeddings, logit clamp).
+# Shapes from "TevunahAi/Grok-1-BF16", "Weight Verification": q_proj [Hq Dh, d],
+# k_proj and v_proj [Hkv Dh, d], o_proj [d, Hq Dh] in PyTorch [out, in] order,
+# pre/post-attention norm scales [d]; 48 query and 8 key/value heads of 128 at
+# d = 6144 ("Jah-yee/grok" README).
+
+TID_WQ, TID_WK, TID_WVA, TID_WO, TID_SPRE_A, TID_SPOST_A = 700, 701, 702, 703, 704, 705
+
+
+@dataclass
+class AttnInputs:
+    """One attention block's inputs for a causal sequence of T tokens at
+    positions 0..T-1. bf16 arrays hold uint16 bit patterns."""
+
+    name: str
+    seed: int
+    T: int
+    d: int
+    Hq: int
+    Hkv: int
+    Dh: int
+    eps: float
+    rope_base: float
+    clamp: float
+    x: np.ndarray  # [T, d] bf16 bits
+    s_pre: np.ndarray  # [d] float32 (bf16-representable)
+    s_post: np.ndarray  # [d] float32
+    wq: np.ndarray  # [Hq Dh, d] bf16 bits
+    wk: np.ndarray  # [Hkv Dh, d]
+    wv: np.ndarray  # [Hkv Dh, d]
+    wo: np.ndarray  # [d, Hq Dh]
+
+
+def make_attn_inputs(T: int, d: int, Hq: int, Hkv: int, seed: int, *, name: str = "custom", Dh: int = 128,
+                     qk_gain: float = 1.6, eps: float = 1e-5, rope_base: float = 10000.0,
+                     clamp: float = 30.0) -> AttnInputs:
+    """x ~ N(0, 1); Wq, Wk ~ N(0, qk_gain / sqrt(d)) (1.6 gives attention logits
+    of standard deviation about 2.5, 5 pushes most of them past the clamp);
+    Wv ~ N(0, 1 / sqrt(d)); Wo ~ N(0, 1 / sqrt(Hq Dh)); norm scales U(0.5, 1.5)
+    rounded to bf16."""
+    x = normal_bf16(seed, TID_X, (T, d))
+    s_pre = bf16_bits_to_f32(uniform_bf16(seed, TID_SPRE_A, (d,), 0.5, 1.5))
+    s_post = bf16_bits_to_f32(uniform_bf16(seed, TID_SPOST_A, (d,), 0.5, 1.5))
+    wq = normal_bf16(seed, TID_WQ, (Hq * Dh, d), std=qk_gain / np.sqrt(d))
+    wk = normal_bf16(seed, TID_WK, (Hkv * Dh, d), std=qk_gain / np.sqrt(d))
+    wv = normal_bf16(seed, TID_WVA, (Hkv * Dh, d), std=1.0 / np.sqrt(d))
+    wo = normal_bf16(seed, TID_WO, (d, Hq * Dh), std=1.0 / np.sqrt(Hq * Dh))
+    return AttnInputs(name=name, seed=seed, T=T, d=d, Hq=Hq, Hkv=Hkv, Dh=Dh, eps=eps, rope_base=rope_base,
+                      clamp=clamp, x=x, s_pre=s_pre, s_post=s_post, wq=wq, wk=wk, wv=wv, wo=wo)
+
+
+# Attention workloads; their seeds are 2000 + position.
+ATTN_WORKLOADS = ("attn_tiny", "attn_clamp", "attn_prefill")
+
+
+def attn_workload(name: str, T: Optional[int] = None) -> AttnInputs:
+    """attn_tiny: T=200, d=768, 6 query heads on 1 key/value head (the 6:1 ratio
+    of 48:8); attn_clamp: the same with Wq, Wk gain 5 so the +-30 clamp binds;
+    attn_prefill: T=8192 at d=6144, 48/8 heads.  ``T`` overrides the length
+    (the first rows of x do not depend on it)."""
+    seed = 2000 + ATTN_WORKLOADS.index(name)
+    if name == "attn_tiny":
+        return make_attn_inputs(T or 200, 768, 6, 1, seed, name=name)
+    if name == "attn_clamp":
+        return make_attn_inputs(T or 200, 768, 6, 1, seed, name=name, qk_gain=5.0)
+    if name == "attn_prefill":
+        return make_attn_inputs(T or 8192, GROK_D, 48, 8, seed, name=name)
+    raise KeyError(name)

@@ -31,6 +31,26 @@ MUTANTS = {
     "stats_sum_not_mean": ("out[e] = s / (double)T;", "out[e] = s;"),
 }
 
+# planted in the attention block; checked by its own pin file
+ATTN_MUTANTS = {
+    "rope_sign": ("v[2 * i] = x0 * c - x1 * s;", "v[2 * i] = x0 * c + x1 * s;"),
+    "rope_frequency": ("pow(base, -2.0 * (double)i / (double)Dh)", "pow(base, -1.0 * (double)i / (double)Dh)"),
+    "rope_half_split_pairs": ("const double x0 = v[2 * i], x1 = v[2 * i + 1];",
+                              "const double x0 = v[i], x1 = v[i + Dh / 2];"),
+    "keys_not_rotated": ("for (int64_t g = 0; g < Hkv; ++g) oracle_rope(", "for (int64_t g = 0; g < 0; ++g) oracle_rope("),
+    "logit_scale_dropped": ("s /= sqrt((double)Dh);", ""),
+    "clamp_dropped": ("if (s > clamp_c) s = clamp_c;", ""),
+    "gqa_heads_interleaved": ("const int64_t g = h / group;", "const int64_t g = h % Hkv;"),
+    "values_from_key_weights": ("matvec_bf16(kvw, d, wv, xn, V + t * kvw);", "matvec_bf16(kvw, d, wk, xn, V + t * kvw);"),
+    "attn_residual_dropped": ("(double)bf16_bits_to_float(x[t * d + n]) + o[n] * rr", "o[n] * rr"),
+    "attn_post_norm_scale_dropped": ("o[n] * rr * (double)s_post[n]", "o[n] * rr"),
+    "attn_softmax_unnormalised": ("ctx[h * Dh + c] = acc / z;", "ctx[h * Dh + c] = acc;"),
+}
+
+PIN_FILE = {name: "test_oracle_pins.py" for name in MUTANTS}
+PIN_FILE.update({name: "test_oracle_attn_pins.py" for name in ATTN_MUTANTS})
+MUTANTS.update(ATTN_MUTANTS)
+
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, tmp_path):
@@ -43,7 +63,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", str(lib), str(mut), "-lm"])
     env = dict(os.environ, MOE_ORACLE_LIB_OVERRIDE=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", PIN_FILE[name])],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout
