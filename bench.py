@@ -16,6 +16,11 @@ layer is token-parallel with no exchange, so scaling is weak and value = N * T
 
 --impl reference times the CPU oracle (fp64, OpenMP) on the host cores, one
 bounded token sample per step, and prints the same metric.
+
+--workload attn_prefill times the attention half of the decoder layer instead
+(pre-norm, q/k/v projection, RoPE, causal GQA attention 48/8 with the +-30
+logit clamp, output projection, post-norm, residual) on one causal sequence of
+T = 8192 tokens at d = 6144 (seed 2002); a step is one attn_block_forward.
 """
 from __future__ import annotations
 
@@ -251,6 +256,180 @@ def whole_job_tokens_per_s(world, tokens_per_rank, seconds_per_step):
     return world * tokens_per_rank / seconds_per_step
 
 
+ATTN_METRIC = "Grok-1 attention block tokens/s (T=8192 causal, GQA 48/8, bf16); % of bf16 TC roofline"
+
+
+def attn_work(inp):
+    """Algorithmic flops of each tensor-core kernel of the attention block and
+    bytes of the others, per launch.  Causal attention counts the T(T+1)/2
+    query-key pairs of each query head, 4 Dh flops each (Q K^T and P V)."""
+    T, d, Hq, Hkv, Dh = inp.T, inp.d, inp.Hq, inp.Hkv, inp.Dh
+    nqkv = (Hq + 2 * Hkv) * Dh
+    pairs = T * (T + 1) // 2
+    return {
+        "prenorm": ("hbm", T * d * 2 * 2),
+        "qkv": ("tensor", 2.0 * T * d * nqkv),
+        "rope": ("hbm", T * nqkv * 4 + T * nqkv * 2),
+        "attn": ("tensor", 4.0 * Dh * Hq * pairs),
+        "oproj": ("tensor", 2.0 * T * Hq * Dh * d),
+        "post": ("hbm", T * d * 4 + T * d * 2 * 2),
+    }
+
+
+def attn_cpu_baseline(inp, budget_s=20.0, seed=7):
+    """The attention oracle on this host: keys and values of the whole sequence
+    once, then a seeded sample of query tokens; tokens/s = T / (key/value time +
+    T * per-query time)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attn_tokens(inp, [inp.T - 1])
+    t_first = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    n = 4
+    toks = np.sort(rng.choice(inp.T, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle.attn_tokens(inp, np.concatenate([toks, [inp.T - 1]]))
+    t_n = time.perf_counter() - t0
+    per_query = max(t_n - t_first, 0.0) / n
+    t_kv = max(t_first - per_query, 0.0)
+    per_token = t_kv / inp.T + per_query
+    return {"value": round(1.0 / per_token, 4), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"keys/values of all {inp.T} tokens + queries {', '.join(str(int(t)) for t in toks)} and "
+                      f"{inp.T - 1} ({t_first + t_n:.1f} s); fp64 C oracle, OpenMP over rows",
+            "seconds_per_token": round(per_token, 6)}
+
+
+def run_attn(args, rank, world, local_rank):
+    import torch
+    import synth
+    import mixture_experts_transformer_gemv_b300 as moe
+    from mixture_experts_transformer_gemv_b300 import build as moe_build
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    moe_build.build()
+    inp = synth.attn_workload(args.workload)
+
+    def bf(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    weights = {"wq": bf(inp.wq).cuda(), "wk": bf(inp.wk).cuda(), "wv": bf(inp.wv).cuda(), "wo": bf(inp.wo).cuda(),
+               "s_pre": torch.from_numpy(inp.s_pre).cuda(), "s_post": torch.from_numpy(inp.s_post).cuda()}
+    x_host = bf(inp.x)
+    x = x_host.cuda()
+    out = torch.empty_like(x)
+    blk = moe.AttnBlock(inp.d, inp.Hq, inp.Hkv, inp.T, weights, eps=inp.eps, rope_base=inp.rope_base,
+                        logit_clamp=inp.clamp)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        blk.forward(x, out)
+    torch.cuda.synchronize()
+    blk.sync_status()
+
+    blk.set_profiling(True)
+    blk.profile_read(reset=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        blk.forward(x, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    blk.sync_status()
+    prof = blk.profile_read(reset=True)
+    blk.set_profiling(False)
+    ms_step = max_over_ranks(ms_total / args.steps, dist, "cuda")
+    value = whole_job_tokens_per_s(world, inp.T, ms_step / 1e3)
+
+    # end to end: pinned host x -> device, the block, y -> pinned host, every step
+    xh = x_host.pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        x.copy_(xh, non_blocking=True)
+        blk.forward(x, out)
+        yh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t1 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x.copy_(xh, non_blocking=True)
+        blk.forward(x, out)
+        yh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t1) / e2e_steps, dist, "cuda")
+
+    pk, peak_kind = peaks()
+    work = attn_work(inp)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        b, a = work[name]
+        per = ms / max(n, 1)
+        kernels[name] = {"ms_per_launch": round(per, 4), "launches": n,
+                         "achieved": round(a / (per / 1e3) / (1e12 if b == "tensor" else 1e9), 1) if per > 0 else None,
+                         "unit": "TFLOP/s" if b == "tensor" else "GB/s"}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
+    bound, amount = work[dom]
+    dur_s = kernels[dom]["ms_per_launch"] / 1e3
+    if bound == "tensor":
+        achieved = amount / dur_s / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
+                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4)}
+    else:
+        achieved = amount / dur_s / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})"}
+    roof["kernel"] = dom
+    roof["algorithmic_per_launch"] = amount
+    roof["kernel_function"] = {"attn": "attn_kernel", "qkv": "grouped_gemm_kernel<1, 0>",
+                               "oproj": "grouped_gemm_kernel<1, 0>"}.get(dom, dom)
+    roof["traffic"] = None
+    tc_flops = sum(a for b, a in work.values() if b == "tensor")
+    result = {
+        "metric": ATTN_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)",
+        "config": {"workload": f"grok1_attention_block T={inp.T} d={inp.d} Hq={inp.Hq} Hkv={inp.Hkv} Dh={inp.Dh} "
+                               f"causal, clamp +-{inp.clamp:g}, RoPE base {inp.rope_base:g} (seed {inp.seed})",
+                   "T": inp.T, "d_model": inp.d, "global_batch_tokens": inp.T,
+                   "parallelism": "sequence replicas, no exchange",
+                   "l2": "no flush: the step reads 0.2 GB of weights and writes/reads 1.3 GB of activations "
+                         "(larger than L2) between the same kernels every step"},
+        "roofline": roof,
+        "block_tc_frac": round(tc_flops / (ms_step / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 4),
+        "kernels": kernels,
+        "e2e": {"value": round(whole_job_tokens_per_s(world, inp.T, e2e_s), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(inp.T * inp.d * 2), "d2h_bytes_per_step": int(inp.T * inp.d * 2),
+                "ms_per_step": round(e2e_s * 1e3, 3),
+                "entry_point": "pinned host x copied in, attn_block_forward, y copied out (one stream)"},
+        "gpu_launches": int(blk.launch_count() * args.steps),
+        "clocks": clk,
+    }
+    blk.close()
+    del weights
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = attn_cpu_baseline(inp, budget_s=args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import synth
@@ -484,6 +663,27 @@ def run_reference(args):
     }
 
 
+def run_attn_reference(args):
+    import synth
+    inp = synth.attn_workload(args.workload)
+    cb = None
+    vals = []  # the oracle keeps no state between calls: no warm-up step is needed
+    for i in range(args.steps):
+        cb = attn_cpu_baseline(inp, seed=100 + i)
+        vals.append(1.0 / cb["seconds_per_token"])
+    value = float(np.mean(vals))
+    cb = dict(cb, value=round(value, 4))
+    return {
+        "impl": "reference", "metric": ATTN_METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(inp.T / value * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)",
+        "config": {"workload": f"grok1_attention_block T={inp.T} d={inp.d} Hq={inp.Hq} Hkv={inp.Hkv}"},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,7 +691,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["prefill", "decode", "skew", "int8", "int8_decode", "tiny", *PROFILE_CASES],
+                    choices=["prefill", "decode", "skew", "int8", "int8_decode", "tiny", *PROFILE_CASES,
+                             "attn_prefill", "attn_tiny"],
                     help="prefill (T=8192) is the headline workload")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -501,12 +702,13 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    attn = args.workload.startswith("attn_")
     if args.impl == "reference":
         if rank != 0:
             return 0
-        res = run_reference(args)
+        res = run_attn_reference(args) if attn else run_reference(args)
     else:
-        res = run_ours(args, rank, world, local_rank)
+        res = run_attn(args, rank, world, local_rank) if attn else run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
     return 0

@@ -1,7 +1,7 @@
 """Grok-1 top-2-of-8 MoE feed-forward layer on B300 (sm_103a): Python binding.
 
-A thin ctypes layer over the C ABI in ``include/moe_layer.h`` (library
-``libmoe_layer.so`` in this directory).  It only checks and marshals
+A thin ctypes layer over the C ABI in ``include/moe_layer.h`` and
+``include/attn_block.h`` (library ``libmoe_layer.so`` in this directory).  It only checks and marshals
 arguments: every step of the layer runs in the library's CUDA kernels.  PyTorch
 is used for device memory and streams.  There is no CPU fallback: when the
 library is missing or the device is not an sm_103 part, calls raise.
@@ -17,12 +17,14 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_PKG)
 LIB_PATH = os.path.join(_PKG, "libmoe_layer.so")
 HEADER_PATH = os.path.join(_ROOT, "include", "moe_layer.h")
+ATTN_HEADER_PATH = os.path.join(_ROOT, "include", "attn_block.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_TIMEOUT = 4, 5, 6
 MOE_WEIGHT_BF16, MOE_WEIGHT_INT8 = 0, 1
 MOE_FLAG_DEVICE_CHECKS, MOE_FLAG_FORCE_TC, MOE_FLAG_FORCE_GEMV = 0x1, 0x2, 0x4
 KERNEL_NAMES = ("router", "permute", "gather", "up_geglu", "down", "combine")
+ATTN_KERNEL_NAMES = ("prenorm", "qkv", "rope", "attn", "oproj", "post")
 
 
 class MoeError(RuntimeError):
@@ -41,6 +43,16 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("gate", "gate_bias", "w", "wv", "w1", "w_scale", "wv_scale",
                                                 "w1_scale", "pre_norm_scale", "post_norm_scale")]
+
+
+class AttnConfig(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float), ("logit_clamp", ctypes.c_float)]
+
+
+class AttnWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("wq", "wk", "wv", "wo", "s_pre", "s_post")]
 
 
 class WorkspaceView(ctypes.Structure):
@@ -93,6 +105,20 @@ def lib():
         L.moe_layer_workspace.argtypes = [vp, ctypes.POINTER(WorkspaceView)]
         L.moe_group_slots_noalloc.restype = i32
         L.moe_group_slots_noalloc.argtypes = [vp, vp, i32, vp, vp, vp]
+        L.attn_block_create.restype = i32
+        L.attn_block_create.argtypes = [ctypes.POINTER(AttnConfig), ctypes.POINTER(AttnWeights), ctypes.POINTER(vp)]
+        L.attn_block_forward.restype = i32
+        L.attn_block_forward.argtypes = [vp, vp, vp, i32, vp]
+        L.attn_block_sync_status.restype = i32
+        L.attn_block_sync_status.argtypes = [vp, vp]
+        L.attn_block_set_profiling.restype = i32
+        L.attn_block_set_profiling.argtypes = [vp, i32]
+        L.attn_block_profile_read.restype = i32
+        L.attn_block_profile_read.argtypes = [vp, vp, vp, i32]
+        L.attn_block_launch_count.restype = i32
+        L.attn_block_launch_count.argtypes = [vp]
+        L.attn_block_destroy.restype = i32
+        L.attn_block_destroy.argtypes = [vp]
         _lib_handle = L
     return _lib_handle
 
@@ -110,9 +136,10 @@ def _check(status: int, where: str):
 
 
 def declared_functions():
-    """Names of the functions include/moe_layer.h declares."""
-    text = open(HEADER_PATH).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?(moe_[a-z_0-9]+)\s*\(", text, re.M)))
+    """Names of the functions include/moe_layer.h and include/attn_block.h declare."""
+    text = open(HEADER_PATH).read() + open(ATTN_HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?((?:moe|attn)_[a-z_0-9]+)\s*\(", text,
+                                 re.M)))
 
 
 def _ptr(t) -> Optional[int]:
@@ -278,3 +305,68 @@ class MoeLayer:
         if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 2
                 and t.shape[1] == self.d):
             raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [T, {self.d}]")
+
+
+class AttnBlock:
+    """The attention half of a Grok-1 decoder layer bound to device tensors.
+
+    weights: dict of contiguous CUDA tensors: wq [Hq 128, d], wk / wv [Hkv 128, d],
+    wo [d, Hq 128] (bf16), s_pre / s_post [d] (fp32).  wq, wk, wv are copied
+    into the handle; wo and the norm scales are borrowed (kept alive here)."""
+
+    def __init__(self, d_model: int, n_q_heads: int, n_kv_heads: int, max_tokens: int, weights: dict,
+                 eps: float = 1e-5, rope_base: float = 10000.0, logit_clamp: float = 30.0, head_dim: int = 128):
+        import torch
+        self.d, self.max_tokens = d_model, max_tokens
+        self._weights = dict(weights)
+        cfg = AttnConfig(d_model, n_q_heads, n_kv_heads, head_dim, max_tokens, eps, rope_base, logit_clamp)
+        w = AttnWeights()
+        for name, _ in AttnWeights._fields_:
+            t = weights.get(name)
+            if t is not None:
+                if not (t.is_cuda and t.is_contiguous()):
+                    raise ValueError(f"weight {name} must be a contiguous CUDA tensor")
+                setattr(w, name, t.data_ptr())
+        handle = ctypes.c_void_p()
+        _check(lib().attn_block_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(handle)), "attn_block_create")
+        self._h = handle
+
+    def forward(self, x, out=None, stream=None):
+        """x [T, d] bf16 CUDA (one causal sequence) -> y [T, d] bf16."""
+        import torch
+        for t, name in ((x, "x"), (out, "out")):
+            if t is not None and not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 2
+                                      and t.shape[1] == self.d):
+                raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [T, {self.d}]")
+        if out is None:
+            out = torch.empty_like(x)
+        _check(lib().attn_block_forward(self._h, x.data_ptr(), out.data_ptr(), x.shape[0], _stream_handle(stream)),
+               "attn_block_forward")
+        return out
+
+    def sync_status(self, stream=None):
+        _check(lib().attn_block_sync_status(self._h, _stream_handle(stream)), "attn_block_sync_status")
+
+    def launch_count(self) -> int:
+        return int(lib().attn_block_launch_count(self._h))
+
+    def set_profiling(self, on: bool):
+        _check(lib().attn_block_set_profiling(self._h, int(bool(on))), "attn_block_set_profiling")
+
+    def profile_read(self, reset: bool = False) -> dict:
+        """{kernel: (total ms, timed launches)} since the last reset."""
+        ms = (ctypes.c_double * len(ATTN_KERNEL_NAMES))()
+        n = (ctypes.c_int64 * len(ATTN_KERNEL_NAMES))()
+        _check(lib().attn_block_profile_read(self._h, ms, n, int(reset)), "attn_block_profile_read")
+        return {k: (ms[i], n[i]) for i, k in enumerate(ATTN_KERNEL_NAMES)}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(lib().attn_block_destroy(self._h), "attn_block_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

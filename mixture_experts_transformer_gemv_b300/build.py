@@ -1,7 +1,8 @@
 """Build the CUDA library in-tree: libmoe_layer.so next to this file.
 
-nvcc -gencode arch=compute_103a,code=sm_103a, one translation unit
-(csrc/moe_layer.cu), static CUDA runtime, no libcuda link (the driver's
+nvcc -gencode arch=compute_103a,code=sm_103a, two translation units
+(csrc/moe_layer.cu: the MoE layer; csrc/attn_block.cu: the attention block),
+static CUDA runtime, no libcuda link (the driver's
 tensor-map encoder is fetched at run time).  Usage: python -m
 mixture_experts_transformer_gemv_b300.build [--force] [--verbose]
 """
@@ -29,7 +30,7 @@ def nvcc() -> str:
 
 def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
-                  [os.path.join(INCLUDE, "moe_layer.h")])
+                  glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def stale() -> bool:
@@ -44,7 +45,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-I", INCLUDE,
-           "-I", CSRC, "-o", tmp, os.path.join(CSRC, "moe_layer.cu")]
+           "-I", CSRC, "-o", tmp, os.path.join(CSRC, "moe_layer.cu"), os.path.join(CSRC, "attn_block.cu")]
     if verbose:
         cmd.insert(1, "-Xptxas")
         cmd.insert(2, "-v")

@@ -1,0 +1,481 @@
+// Kernels of the attention half of a Grok-1 decoder layer (sm_103a).
+//
+// Per causal sequence x [T, d] ("Jah-yee/grok" README, architecture diagram:
+// grouped-query attention, 48 query and 8 key/value heads, rotary embeddings,
+// RMSNorm; "TevunahAi/Grok-1-BF16", "Grok-1 Specific Behaviors": logits
+// hard-clamped to [-30, 30] before the softmax, pre- and post-attention norms;
+// "Weight Verification": q_proj [6144, 6144], k_proj / v_proj [1024, 6144],
+// o_proj [6144, 6144], so heads of 128):
+//
+//   A1 attn_prenorm_kernel   xn = fp16(RMSNorm_pre(x)) and the one-group GEMM schedule
+//   A2 grouped_gemm<down>    qkv = xn [Wq; Wk; Wv]^T, fp16 operands, fp32 out (tcgen05, CTA pairs)
+//   A3 rope_layout_kernel    Q, K rotated (RoFormer pairs (2i, 2i + 1)) in fp16, V transposed in bf16
+//   A4 attn_kernel           ctx = softmax(clamp(Q K^T / sqrt(128))) V, causal (tcgen05)
+//   A5 grouped_gemm<down>    o = ctx Wo^T, fp32                           (tcgen05, CTA pairs)
+//   A6 attn_post_kernel      y = x + RMSNorm_post(o)
+//
+// A4 needs no running maximum: every clamped logit lies in [-c, c], so
+// exp(s - c) lies in [exp(-2c), 1] (normal in fp32 and bf16 for c <= 40) and
+// the softmax is sum_j exp(s_j - c) v_j / sum_j exp(s_j - c) exactly, without
+// the rescaling of the accumulator a flash-attention kernel does when the
+// maximum grows.
+//
+// Precision: the logits are the sensitive part (their error scales with |q||k|),
+// so the path that feeds them (xn, Wq, Wk, q, k) is carried in fp16, 3 mantissa
+// bits more than bf16 at the same tensor-core rate, with saturation at +-65504.
+// The softmax weights, V and ctx stay bf16: the weights go down to exp(-2c) =
+// 8.8e-27, below fp16's range, and both operands of one MMA share a type.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "ptx_tmem.cuh"
+
+namespace moe {
+
+constexpr int kAttnDh = 128;                         // head dimension
+constexpr int kAttnBM = 128;                         // queries of one CTA (TMEM lanes)
+constexpr int kAttnBN = 128;                         // keys of one block
+constexpr int kAttnStages = 3;                       // K/V blocks in flight
+constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 bf16, two 64-column boxes
+constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 bf16, 128-byte swizzle
+constexpr int kAttnThreads = 192;                    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax + epilogue
+constexpr int kAttnNumBars = 1 + 2 * kAttnStages + 6 + 2;
+constexpr size_t kAttnSmemBytes = 1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + 8 * kAttnNumBars + 16;
+constexpr uint32_t kAttnTmemCols = 512;              // O | S0 | S1 | P0 | P1
+constexpr uint32_t kAttnColS = 128, kAttnColP = 384;
+constexpr uint32_t kAttnIdesc = idesc_bf16_f32(kAttnBM, kAttnBN);  // P V: bf16 x bf16
+// Q K^T: fp16 x fp16 (format 0 in bits 7-9 and 10-12), fp32 accumulator
+constexpr uint32_t kAttnIdescF16 = (1u << 4) | (static_cast<uint32_t>(kAttnBN >> 3) << 17) |
+                                   (static_cast<uint32_t>(kAttnBM >> 4) << 24);
+static_assert(kAttnBN == kAttnDh, "S and O share the instruction shape");
+static_assert(kAttnSmemBytes <= 232448, "fits one CTA per SM");
+
+struct AttnParams {
+  int T;               // sequence length
+  int t_stride;        // rows per head of Q and K, columns of Vt (multiple of 128)
+  int n_q_heads;       // query heads
+  int group;           // query heads per key/value head
+  int n_qtiles;        // ceil(T / 128)
+  float scale_log2;    // log2(e) / sqrt(128)
+  float clamp_log2;    // c log2(e)
+  __nv_bfloat16* ctx;  // [rows, n_q_heads * 128]
+  int ctx_ld;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One CTA: 128 queries of one head against the key blocks 0..(query tile).
+// Warp 0 streams Q once and K / V^T blocks through a 3-stage ring (TMA), warp 1
+// issues S_j = Q K_j^T into a double-buffered TMEM S and O += P_j V_j with P
+// read from TMEM, warps 2-5 turn S_j into P_j (one query row per thread) and
+// finally write ctx = O / l.
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                // [128 x 128] bf16
+  uint8_t* sKV = smem + kAttnTile;   // stage s: K at 2s tiles, V^T at 2s + 1 tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (1 + 2 * kAttnStages));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const uint32_t b0 = smem_addr(bars);
+  const uint32_t q_full = b0;
+  auto kv_full = [&](int s) { return b0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return b0 + 8u * (1 + kAttnStages + s); };
+  auto s_full = [&](int b) { return b0 + 8u * (1 + 2 * kAttnStages + b); };
+  auto p_full = [&](int b) { return b0 + 8u * (3 + 2 * kAttnStages + b); };
+  auto p_free = [&](int b) { return b0 + 8u * (5 + 2 * kAttnStages + b); };
+  const uint32_t o_full = b0 + 8u * (7 + 2 * kAttnStages);
+  const uint32_t drain = o_full + 8u;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.x / p.n_q_heads;  // longest query tiles first
+  const int h = (int)blockIdx.x % p.n_q_heads;
+  const int g = h / p.group;
+  const int nblk = qt + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(p_full(b), 128);  // every softmax thread
+      mbar_init(p_free(b), 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_vt);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kAttnTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      bool ok = true;
+      int n_issued = 0;
+      mbar_arrive_expect_tx(q_full, kAttnTile);
+      const int qrow0 = h * p.t_stride + qt * kAttnBM;
+      tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
+      tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kAttnStages;
+        if (j >= kAttnStages &&
+            !wait_bounded(kv_empty(s), (uint32_t)((j / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = kv_full(s);
+        mbar_arrive_expect_tx(fb, 2 * kAttnTile);
+        uint8_t* sk = sKV + (size_t)(2 * s) * kAttnTile;
+        uint8_t* sv = sk + kAttnTile;
+        const int krow = g * p.t_stride + j * kAttnBN;
+        tma_load_2d(smem_addr(sk), &tm_k, fb, 0, krow);
+        tma_load_2d(smem_addr(sk + kAttnHalf), &tm_k, fb, 64, krow);
+        tma_load_2d(smem_addr(sv), &tm_vt, fb, j * kAttnBN, g * kAttnDh);
+        tma_load_2d(smem_addr(sv + kAttnHalf), &tm_vt, fb, j * kAttnBN + 64, g * kAttnDh);
+        n_issued = j + 1;
+      }
+      // every release of a stage by the MMA issuer has landed before exit
+      for (int j = (nblk > kAttnStages ? nblk - kAttnStages : 0); j < nblk && ok; ++j)
+        if (!wait_bounded(kv_empty(j % kAttnStages), (uint32_t)(j / kAttnStages) & 1u, abort_flag, p.timeout_ns))
+          ok = false;
+      if (!ok) {
+        raise_abort(abort_flag, p.err);
+        // this role's copies still in flight land before the CTA exits
+        wait_bounded(q_full, 0, nullptr, p.timeout_ns);
+        for (int j = (n_issued > kAttnStages ? n_issued - kAttnStages : 0); j < n_issued; ++j)
+          wait_bounded(kv_full(j % kAttnStages), (uint32_t)(j / kAttnStages) & 1u, nullptr, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t tO = tmem_base, tS = tmem_base + kAttnColS, tP = tmem_base + kAttnColP;
+      const uint32_t qa = smem_addr(sQ);
+      bool ok = wait_bounded(q_full, 0, abort_flag, p.timeout_ns);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % kAttnStages;
+        if (!wait_bounded(kv_full(s), (uint32_t)(j / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
+        tc_fence_after_sync();
+        const uint32_t kb = smem_addr(sKV + (size_t)(2 * s) * kAttnTile);
+#pragma unroll
+        for (int kk = 0; kk < kAttnDh / 16; ++kk)  // K = 16 along the head dimension
+          umma_bf16(tS + (uint32_t)(j & 1) * kAttnBN, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
+                    smem_desc_k_sw128(kb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdescF16, kk != 0);
+        umma_commit(s_full(j & 1));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nblk && ok; ++j) {
+        // S_{j+1} runs on the tensor cores while the softmax warps work on S_j
+        if (j + 1 < nblk && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        const int b = j & 1;
+        if (!wait_bounded(p_full(b), (uint32_t)(j >> 1) & 1u, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t vb = smem_addr(sKV + (size_t)(2 * (j % kAttnStages) + 1) * kAttnTile);
+#pragma unroll
+        for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
+          umma_bf16_tmem_a(tO, tP + (uint32_t)b * (kAttnBN / 2) + 8 * kk,
+                           smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc, (j | kk) != 0);
+        umma_commit(kv_empty(j % kAttnStages));
+        umma_commit(p_free(b));
+      }
+      if (ok) umma_commit(o_full);
+      // all MMAs issued by this thread are complete before TMEM is freed
+      umma_commit(drain);
+      if (!wait_bounded(drain, 0, nullptr, p.timeout_ns)) ok = false;
+      if (!ok) raise_abort(abort_flag, p.err);
+    }
+  } else {
+    // ------------------------------------------------- softmax + epilogue
+    const int q4 = warp & 3;  // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int qrow = qt * kAttnBM + r;
+    const float sc = p.scale_log2, cl = p.clamp_log2;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nblk; ++j) {
+      const int b = j & 1;
+      bool got = wait_bounded(s_full(b), (uint32_t)(j >> 1) & 1u, abort_flag, p.timeout_ns);
+      // P_b was last read by the MMA of block j - 2
+      if (got && j >= 2) got = wait_bounded(p_free(b), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const bool diag = (j == qt);  // the only block with keys after some queries
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t s0[32], s1[32];
+        const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)b * kAttnBN + hh * 64;
+        tmem_ld_32x32b_x32(ts, s0);
+        tmem_ld_32x32b_x32(ts + 32, s1);
+        tmem_ld_wait();
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
+          const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+          float p0 = ex2_approx(fminf(fmaxf(__uint_as_float(u0) * sc, -cl), cl) - cl);
+          float p1 = ex2_approx(fminf(fmaxf(__uint_as_float(u1) * sc, -cl), cl) - cl);
+          if (diag) {
+            const int key = hh * 64 + 2 * c;
+            if (key > r) p0 = 0.f;
+            if (key + 1 > r) p1 = 0.f;
+          }
+          pk[c] = pack_bf16x2(p0, p1);
+          l += bf16_lo(pk[c]) + bf16_hi(pk[c]);  // the weights the MMA multiplies
+        }
+        tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)b * (kAttnBN / 2) + hh * 32, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(p_full(b));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_full, 0, abort_flag, p.timeout_ns));
+    if (ok) {
+      tc_fence_after_sync();
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh;
+#pragma unroll 1
+      for (int c = 0; c < kAttnDh / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem_base + lane_off + c * 32, o);
+        tmem_ld_wait();
+        if (qrow < p.T) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+    } else if (lane == 0) {
+      raise_abort(abort_flag, p.err);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kAttnTmemCols);
+  }
+}
+
+// A1: xn[t] = fp16(x[t] / sqrt(mean(x[t]^2) + eps) * s) for t < T, zero rows for
+// T <= t < rows_pad; block 0 also writes the schedule that makes the grouped
+// GEMM one dense GEMM (group 0 holds rows [0, rows_pad), the others none).
+// One block of 256 threads per row; d a multiple of 8.
+__global__ void __launch_bounds__(256) attn_prenorm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           const float* __restrict__ s, float eps, int T,
+                                                           int rows_pad, int d, __half* __restrict__ xn,
+                                                           int32_t* __restrict__ sched) {
+  const int t = blockIdx.x;
+  if (t == 0 && threadIdx.x < kSchedInts)
+    sched[threadIdx.x] = threadIdx.x == 0 ? T : (threadIdx.x < kNumExperts ? 0 : (threadIdx.x == kNumExperts ? 0 : rows_pad));
+  uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)t * d);
+  const int nv = d / 8;
+  if (t >= T) {
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = bf16_lo(w[k]), b = bf16_hi(w[k]);
+      ss = fmaf(a, a, fmaf(b, b, ss));
+    }
+  }
+  __shared__ float red[8];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float rr = rsqrtf(tot / (float)d + eps);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const float4 s0 = reinterpret_cast<const float4*>(s)[2 * i];
+    const float4 s1 = reinterpret_cast<const float4*>(s)[2 * i + 1];
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      o[k] = pack_f16x2_sat(bf16_lo(w[k]) * rr * sv[2 * k], bf16_hi(w[k]) * rr * sv[2 * k + 1]);
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// In-place bf16 -> fp16 of n values (round to nearest, saturating; values
+// below 2^-14 in magnitude become fp16 subnormals).
+__global__ void bf16_to_f16_kernel(uint32_t* p, int64_t n_pairs) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_pairs; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t u = p[i];
+    p[i] = pack_f16x2_sat(bf16_lo(u), bf16_hi(u));
+  }
+}
+
+// Rotation table: cs[t * 64 + i] = (cos, sin)(t * base^(-2i / 128)), angles in fp64.
+__global__ void rope_table_kernel(float2* cs, int n_pos, double base) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_pos * (kAttnDh / 2)) return;
+  const int t = idx / (kAttnDh / 2), i = idx % (kAttnDh / 2);
+  const double a = (double)t * pow(base, -2.0 * (double)i / (double)kAttnDh);
+  double sn, cn;
+  sincos(a, &sn, &cn);
+  cs[idx] = make_float2((float)cn, (float)sn);
+}
+
+__global__ void fill_f32_kernel(float* p, float v, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+// A3: from qkv fp32 [T, ld] (query heads, then key heads, then value heads, 128
+// columns each) write Q [Hq][t_stride][128] and K [Hkv][t_stride][128] rotated
+// (pair (2i, 2i + 1) of each head turned by t * base^(-2i/128)) in fp16
+// (saturating) and Vt [Hkv][128][t_stride] (V transposed: keys along rows) in bf16; token rows
+// T <= t < gridDim.x * 32 are written as zeros.  Grid (ceil(T / 128) * 4,
+// Hq + 2 Hkv), 256 threads: 32 tokens x one head per block.
+__global__ void __launch_bounds__(256) rope_layout_kernel(const float* __restrict__ qkv, int ld,
+                                                          const float2* __restrict__ cs, int T, int t_stride, int Hq,
+                                                          int Hkv, __half* __restrict__ Q,
+                                                          __half* __restrict__ K,
+                                                          __nv_bfloat16* __restrict__ Vt) {
+  __shared__ float vt[kAttnDh][33];
+  const int t0 = blockIdx.x * 32, col = blockIdx.y;
+  const int tl = threadIdx.x >> 3, part = threadIdx.x & 7;  // token of the block, 16 columns of the head
+  const int t = t0 + tl;
+  float v[16];
+  if (t < T) {
+    const float4* src = reinterpret_cast<const float4*>(qkv + (size_t)t * ld + (size_t)col * kAttnDh + part * 16);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 a = src[k];
+      v[4 * k] = a.x;
+      v[4 * k + 1] = a.y;
+      v[4 * k + 2] = a.z;
+      v[4 * k + 3] = a.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = 0.f;
+  }
+  if (col < Hq + Hkv) {
+    if (t < T) {
+      const float2* c = cs + (size_t)t * (kAttnDh / 2) + part * 8;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 e = c[k];
+        const float x0 = v[2 * k], x1 = v[2 * k + 1];
+        v[2 * k] = x0 * e.x - x1 * e.y;
+        v[2 * k + 1] = x0 * e.y + x1 * e.x;
+      }
+    }
+    __half* dst = col < Hq ? Q + ((size_t)col * t_stride + t) * kAttnDh
+                           : K + ((size_t)(col - Hq) * t_stride + t) * kAttnDh;
+    uint32_t pk[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pk[k] = pack_f16x2_sat(v[2 * k], v[2 * k + 1]);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + part * 16);
+    d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  } else {
+    const int gv = col - Hq - Hkv;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) vt[part * 16 + k][tl] = v[k];
+    __syncthreads();
+    const int c = threadIdx.x >> 1, hh = threadIdx.x & 1;  // row of Vt, 16 of the block's 32 tokens
+    uint32_t pk[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(vt[c][hh * 16 + 2 * k], vt[c][hh * 16 + 2 * k + 1]);
+    uint4* d4 = reinterpret_cast<uint4*>(Vt + ((size_t)gv * kAttnDh + c) * t_stride + t0 + hh * 16);
+    d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  }
+}
+
+// A6: y[t] = bf16(x[t] + o[t] / sqrt(mean(o[t]^2) + eps) * s), o fp32 [T, ld].
+// One block of 256 threads per row; d a multiple of 8.
+__global__ void __launch_bounds__(256) attn_post_kernel(const __nv_bfloat16* __restrict__ x,
+                                                        const float* __restrict__ o, int ld,
+                                                        const float* __restrict__ s, float eps, int d,
+                                                        __nv_bfloat16* __restrict__ y) {
+  const int t = blockIdx.x;
+  const float4* orow = reinterpret_cast<const float4*>(o + (size_t)t * ld);
+  const int nv = d / 8;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const float4 a = orow[2 * i], b = orow[2 * i + 1];
+    ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+  }
+  __shared__ float red[8];
+#pragma unroll
+  for (int k = 16; k > 0; k >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, k);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float rr = rsqrtf(tot / (float)d + eps);
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)t * d);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const float4 a = orow[2 * i], b = orow[2 * i + 1];
+    const float4 s0 = reinterpret_cast<const float4*>(s)[2 * i];
+    const float4 s1 = reinterpret_cast<const float4*>(s)[2 * i + 1];
+    const uint4 xv = xr[i];
+    uint4 out;
+    out.x = pack_bf16x2(bf16_lo(xv.x) + a.x * rr * s0.x, bf16_hi(xv.x) + a.y * rr * s0.y);
+    out.y = pack_bf16x2(bf16_lo(xv.y) + a.z * rr * s0.z, bf16_hi(xv.y) + a.w * rr * s0.w);
+    out.z = pack_bf16x2(bf16_lo(xv.z) + b.x * rr * s1.x, bf16_hi(xv.z) + b.y * rr * s1.y);
+    out.w = pack_bf16x2(bf16_lo(xv.w) + b.z * rr * s1.z, bf16_hi(xv.w) + b.w * rr * s1.w);
+    yr[i] = out;
+  }
+}
+
+}  // namespace moe

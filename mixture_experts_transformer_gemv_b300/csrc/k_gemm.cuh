@@ -82,7 +82,8 @@ constexpr int kBTileBytes = kGemmHalfN * kGemmBK * 2;   // 16 KB (bf16, swizzled
 constexpr int kB8TileBytes = kGemmHalfN * kGemmBK;      // 8 KB (int8 staging, dense rows of 64 B)
 constexpr uint32_t kTmemCols = 2 * kGemmBN;              // two fp32 accumulators of 128 x 256 per CTA
 constexpr uint32_t kGemmIdesc = idesc_bf16_f32(kGemmBM, kGemmBN);
-// int8 weights: the same MMA with fp16 A and B (format 0 in bits 7-9 and 10-12)
+// fp16 A and B (format 0 in bits 7-9 and 10-12): int8 weights converted to fp16,
+// or fp16 operands on the bf16 path (f16_operands)
 constexpr uint32_t kGemmIdescF16 = (1u << 4) | (static_cast<uint32_t>(kGemmBN >> 3) << 17) |
                                    (static_cast<uint32_t>(kGemmBM >> 4) << 24);
 static_assert(kGemmBM == kRowTile, "expert row blocks are whole tiles");
@@ -120,6 +121,7 @@ struct GemmParams {
   int scale_experts;             // int8: E_s, 8 (per expert) or 1 (shared)
   int scale_groups;              // int8: G groups along the reduction; 1 = per output channel only
   int group_kb;                  // int8, G > 1: k-blocks of 64 per group
+  int f16_operands;              // bf16 path: A and B hold fp16 instead of bf16 (both the same type)
   uint32_t* err;                 // device error word
   uint64_t timeout_ns;           // limit of every wait
 };
@@ -306,6 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kGemmBN;
+        const uint32_t idesc = (WQ || p.f16_operands) ? kGemmIdescF16 : kGemmIdesc;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded_cluster(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
               (WQ && !wait_bounded_cluster(bfull_bar(bstage), bphase, abort_flag, p.timeout_ns))) {
@@ -317,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sB + (WQ ? bstage : stage) * kBTileBytes));
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
-            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, WQ ? kGemmIdescF16 : kGemmIdesc, (kb | kk) != 0);
+            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
           umma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == (uint32_t)C::kStages) {
             stage = 0;

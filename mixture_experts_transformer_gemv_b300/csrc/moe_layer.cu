@@ -29,6 +29,7 @@
 
 #include "moe_layer.h"
 #include "common.cuh"
+#include "host_util.h"
 #include "k_combine.cuh"
 #include "k_decode.cuh"
 #include "k_decode_i8.cuh"
@@ -37,81 +38,11 @@
 #include "k_router.cuh"
 
 using namespace moe;
+using namespace moe_host;
 
 namespace {
 
-thread_local std::string g_last_error;
-
-moe_status_t fail(moe_status_t s, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  g_last_error = buf;
-  return s;
-}
-
-moe_status_t ok() {
-  g_last_error.clear();
-  return MOE_OK;
-}
-
-#define MOE_CUDA_TRY(call)                                                                    \
-  do {                                                                                        \
-    cudaError_t e_ = (call);                                                                  \
-    if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
-  } while (0)
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
-// Restores the caller's current device on scope exit.
-struct DeviceGuard {
-  int prev = -1;
-  bool ok = false;
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev) != cudaSuccess) return;
-    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
-  }
-  ~DeviceGuard() {
-    int cur = -1;
-    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
-  }
-};
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// Row-major 2-D tensor [rows, inner] of 2-byte elements, box [box_rows, 64], 128-byte swizzle.
-moe_status_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  static_assert(kGemmBK == kDecBK, "both GEMM families use 64-element boxes");
-  EncodeTiledFn enc = get_encoder();
-  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return MOE_OK;
-}
+static_assert(kGemmBK == kDecBK && kGemmBK == kTmapBoxInner, "every bf16 GEMM operand box is 64 elements wide");
 
 // Row-major 2-D int8 tensor [rows, inner], box [box_rows, box_inner]: the staging
 // layout the int8 converter warps read; 64-byte rows without swizzle for the
@@ -133,9 +64,6 @@ moe_status_t make_tmap_i8(CUtensorMap* m, const void* base, uint64_t inner, uint
 }
 
 constexpr int kProfRing = 64;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
 
@@ -192,19 +120,8 @@ struct moe_layer {
 
 namespace {
 
-// CTAs of a persistent cluster launch of `kernel`: 2 x the clusters of 2 CTAs
-// that can be resident at once, capped at one CTA per SM.
 moe_status_t gemm_pairs(moe_layer* L, const void* kernel, int threads, size_t smem, int* grid) {
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(2 * (L->num_sms / 2), 1, 1);
-  lc.blockDim = dim3(threads, 1, 1);
-  lc.dynamicSmemBytes = smem;
-  int clusters = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &lc);
-  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
-  if (clusters < 1) return fail(MOE_ERR_UNSUPPORTED, "no CTA pair of the grouped GEMM fits on this device");
-  *grid = 2 * std::min(clusters, L->num_sms / 2);
-  return MOE_OK;
+  return cluster_pair_grid(L->num_sms, kernel, threads, smem, grid);
 }
 
 void harvest(moe_layer* L, int slot) {

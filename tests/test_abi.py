@@ -122,3 +122,45 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text and "moe_oracle" not in text
+
+
+# ------------------------------------------------------------- attention block
+
+def _attn_cfg(**kw):
+    c = dict(d_model=6144, n_q_heads=48, n_kv_heads=8, head_dim=128, max_tokens=8192, eps=1e-5, rope_base=10000.0,
+             logit_clamp=30.0)
+    c.update(kw)
+    return moe.AttnConfig(**c)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), 2),            # only heads of 128
+    (dict(d_model=6000), 2),           # d a multiple of 256
+    (dict(n_kv_heads=7), 1),           # Hkv must divide Hq
+    (dict(max_tokens=0), 1),
+    (dict(max_tokens=70000), 1),
+    (dict(logit_clamp=50.0), 2),       # exp(-2c) must stay a normal float
+    (dict(logit_clamp=0.0), 2),
+    (dict(eps=0.0), 1),
+])
+def test_attn_create_rejects_bad_config(lib, kw, status):
+    cfg = _attn_cfg(**kw)
+    w = moe.AttnWeights(16, 16, 16, 16, 16, 16)  # never dereferenced: validation fails first
+    h = ctypes.c_void_p(1)
+    assert lib.attn_block_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == status
+    assert h.value is None
+    assert lib.moe_last_error_message()
+
+
+def test_attn_null_arguments(lib):
+    cfg = _attn_cfg()
+    h = ctypes.c_void_p()
+    assert lib.attn_block_create(None, None, ctypes.byref(h)) == 1
+    w = moe.AttnWeights(0, 16, 16, 16, 16, 16)
+    assert lib.attn_block_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == 1
+    w = moe.AttnWeights(24, 16, 16, 16, 16, 16)  # misaligned
+    assert lib.attn_block_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == 1
+    assert lib.attn_block_forward(None, 16, 32, 4, None) == 1
+    assert lib.attn_block_sync_status(None, None) == 1
+    assert lib.attn_block_destroy(None) == 0
+    assert lib.attn_block_launch_count(None) == 0

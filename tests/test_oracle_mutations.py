@@ -23,7 +23,7 @@ MUTANTS = {
     "softmax_sign": ("p[e] = exp(l[e] - mx)", "p[e] = exp(mx - l[e])"),
     "tie_to_higher_index": ("if ((float)p[e] > (float)p[i0]) i0", "if ((float)p[e] >= (float)p[i0]) i0"),
     "pre_norm_scale_dropped": ("* r * (double)s_pre[j]", "* r"),
-    "post_norm_eps_dropped": ("double rr = 1.0 / sqrt(ss / (double)d + eps)", "double rr = 1.0 / sqrt(ss / (double)d)"),
+    "post_norm_eps_dropped": ("\n    double rr = 1.0 / sqrt(ss / (double)d + eps)", "\n    double rr = 1.0 / sqrt(ss / (double)d)"),
     "gelu_constant": ("0.044715 * u * u * u", "0.0447 * u * u * u"),
     "int8_scale_not_per_expert": ("int64_t es = (W->scale_E > 1) ? e : 0;", "int64_t es = 0;"),
     "bias_sign": ("l[e] = acc + (bias ? (double)bias[e] : 0.0)", "l[e] = acc - (bias ? (double)bias[e] : 0.0)"),
