@@ -257,6 +257,18 @@ def whole_job_tokens_per_s(world, tokens_per_rank, seconds_per_step):
 
 
 ATTN_METRIC = "Grok-1 attention block tokens/s (T=8192 causal, GQA 48/8, bf16); % of bf16 TC roofline"
+# attention workloads; attn_profile_small (T = 2048, full width: 25 MB of Q,
+# 4 MB of K and V, 0.2 GB of weights) is the ncu capture case
+ATTN_CASES = {"attn_prefill": ("attn_prefill", None), "attn_tiny": ("attn_tiny", None),
+              "attn_profile_small": ("attn_prefill", 2048)}
+
+
+def make_attn_workload(name):
+    import synth
+    base, T = ATTN_CASES[name]
+    inp = synth.attn_workload(base, T=T)
+    inp.name = name
+    return inp
 
 
 def attn_work(inp):
@@ -311,7 +323,7 @@ def run_attn(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     moe_build.build()
-    inp = synth.attn_workload(args.workload)
+    inp = make_attn_workload(args.workload)
 
     def bf(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
@@ -664,8 +676,7 @@ def run_reference(args):
 
 
 def run_attn_reference(args):
-    import synth
-    inp = synth.attn_workload(args.workload)
+    inp = make_attn_workload(args.workload)
     cb = None
     vals = []  # the oracle keeps no state between calls: no warm-up step is needed
     for i in range(args.steps):
@@ -692,7 +703,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["prefill", "decode", "skew", "int8", "int8_decode", "tiny", *PROFILE_CASES,
-                             "attn_prefill", "attn_tiny"],
+                             *ATTN_CASES],
                     help="prefill (T=8192) is the headline workload")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "ptx_pair.cuh"
 #include "ptx_tmem.cuh"
 
 namespace moe {
@@ -42,9 +43,14 @@ constexpr int kAttnBN = 128;                         // keys of one block
 constexpr int kAttnStages = 3;                       // K/V blocks in flight
 constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 bf16, two 64-column boxes
 constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 bf16, 128-byte swizzle
-constexpr int kAttnThreads = 192;                    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax + epilogue
+constexpr int kAttnSoftmaxWarps = 8;                 // two per TMEM lane quarter, 64 keys each
+constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
+constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
 constexpr int kAttnNumBars = 1 + 2 * kAttnStages + 6 + 2;
-constexpr size_t kAttnSmemBytes = 1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + 8 * kAttnNumBars + 16;
+constexpr size_t kAttnBarBytes = 128;                // barriers, TMEM address, abort flag
+constexpr size_t kAttnSmemBytes =
+    1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + kAttnBarBytes + 2 * kAttnBM * sizeof(float);
+static_assert(8 * kAttnNumBars + 8 <= kAttnBarBytes, "barrier block");
 constexpr uint32_t kAttnTmemCols = 512;              // O | S0 | S1 | P0 | P1
 constexpr uint32_t kAttnColS = 128, kAttnColP = 384;
 constexpr uint32_t kAttnIdesc = idesc_bf16_f32(kAttnBM, kAttnBN);  // P V: bf16 x bf16
@@ -77,7 +83,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // One CTA: 128 queries of one head against the key blocks 0..(query tile).
 // Warp 0 streams Q once and K / V^T blocks through a 3-stage ring (TMA), warp 1
 // issues S_j = Q K_j^T into a double-buffered TMEM S and O += P_j V_j with P
-// read from TMEM, warps 2-5 turn S_j into P_j (one query row per thread) and
+// read from TMEM, warps 2-9 turn S_j into P_j (two warps per 32 query rows, 64
+// keys each, so one warp's TMEM loads overlap the other's arithmetic) and
 // finally write ctx = O / l.
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -89,6 +96,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (1 + 2 * kAttnStages));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* l_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kAttnBarBytes);  // [2][128]
   const uint32_t b0 = smem_addr(bars);
   const uint32_t q_full = b0;
   auto kv_full = [&](int s) { return b0 + 8u * (1 + s); };
@@ -113,7 +121,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), 128);  // every softmax thread
+      mbar_init(p_full(b), kAttnSoftmaxThreads);  // every softmax thread
       mbar_init(p_free(b), 1);
     }
     mbar_init(o_full, 1);
@@ -221,7 +229,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
-    const int q4 = warp & 3;  // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
+    const int q4 = warp & 3;                 // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
+    const int half = (warp - 2) >> 2;        // keys [64 half, 64 half + 64) of each block
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int qrow = qt * kAttnBM + r;
@@ -235,52 +244,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (got && j >= 2) got = wait_bounded(p_free(b), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
+        if (lane == 0) raise_abort(abort_flag, p.err);
         break;
       }
       tc_fence_after_sync();
-      const bool diag = (j == qt);  // the only block with keys after some queries
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t s0[32], s1[32];
-        const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)b * kAttnBN + hh * 64;
-        tmem_ld_32x32b_x32(ts, s0);
-        tmem_ld_32x32b_x32(ts + 32, s1);
-        tmem_ld_wait();
-        uint32_t pk[32];
+      uint32_t s0[32], s1[32];
+      const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)b * kAttnBN + half * 64;
+      tmem_ld_32x32b_x32(ts, s0);
+      tmem_ld_32x32b_x32(ts + 32, s1);
+      tmem_ld_wait();
+      // p = 2^(min(max(s log2(e) / sqrt(128), -c'), c') - c'), c' = c log2(e)
+      uint32_t pk[32];
+      if (j == qt) {  // the diagonal block: key (64 half + k) > query r is masked
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
           const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-          float p0 = ex2_approx(fminf(fmaxf(__uint_as_float(u0) * sc, -cl), cl) - cl);
-          float p1 = ex2_approx(fminf(fmaxf(__uint_as_float(u1) * sc, -cl), cl) - cl);
-          if (diag) {
-            const int key = hh * 64 + 2 * c;
-            if (key > r) p0 = 0.f;
-            if (key + 1 > r) p1 = 0.f;
-          }
+          const int key = half * 64 + 2 * c;
+          const float p0 = key > r ? 0.f : ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u0), sc, -cl), -2.f * cl), 0.f));
+          const float p1 =
+              key + 1 > r ? 0.f : ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u1), sc, -cl), -2.f * cl), 0.f));
+          l += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
-          l += bf16_lo(pk[c]) + bf16_hi(pk[c]);  // the weights the MMA multiplies
         }
-        tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)b * (kAttnBN / 2) + hh * 32, pk);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
+          const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+          const float p0 = ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u0), sc, -cl), -2.f * cl), 0.f));
+          const float p1 = ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u1), sc, -cl), -2.f * cl), 0.f));
+          l += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
       }
+      tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)b * (kAttnBN / 2) + half * 32, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(p_full(b));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_full, 0, abort_flag, p.timeout_ns));
+    bool got = ok && __all_sync(0xffffffffu, wait_bounded(o_full, 0, abort_flag, p.timeout_ns));
+    l_part[half * kAttnBM + r] = l;
+    // every softmax thread reaches this barrier exactly once; it also makes the
+    // two halves' row sums visible to each other
+    ok = named_bar_and(1, kAttnSoftmaxThreads, got);
     if (ok) {
       tc_fence_after_sync();
-      const float inv = 1.f / l;
-      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh;
+      const float inv = 1.f / (l_part[r] + l_part[kAttnBM + r]);
+      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < kAttnDh / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_off + c * 32, o);
+        tmem_ld_32x32b_x32(tmem_base + lane_off + half * 64 + c * 32, o);
         tmem_ld_wait();
         if (qrow < p.T) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
