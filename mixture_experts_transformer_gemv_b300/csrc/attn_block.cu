@@ -135,8 +135,8 @@ moe_status_t enqueue(attn_block* B, const void* x, void* y, int T, cudaStream_t 
     p.group = Hq / Hkv;
     p.n_qtiles = t_pad / kAttnBM;
     const double log2e = 1.4426950408889634;
-    p.scale_log2 = (float)(log2e / std::sqrt((double)kAttnDh));
-    p.clamp_log2 = (float)((double)B->cfg.logit_clamp * log2e);
+    p.sat_scale = (float)(1.0 / (2.0 * (double)B->cfg.logit_clamp * std::sqrt((double)kAttnDh)));
+    p.clamp2_log2 = (float)(2.0 * (double)B->cfg.logit_clamp * log2e);
     p.ctx = B->ctx;
     p.ctx_ld = B->n_ctx;
     p.err = B->err;

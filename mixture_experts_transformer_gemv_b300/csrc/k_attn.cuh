@@ -43,7 +43,7 @@ constexpr int kAttnBN = 128;                         // keys of one block
 constexpr int kAttnStages = 3;                       // K/V blocks in flight
 constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 bf16, two 64-column boxes
 constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 bf16, 128-byte swizzle
-constexpr int kAttnSoftmaxWarps = 8;                 // two per TMEM lane quarter, 64 keys each
+constexpr int kAttnSoftmaxWarps = 8;                 // two groups of four: even and odd key blocks
 constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
 constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
 constexpr int kAttnNumBars = 1 + 2 * kAttnStages + 6 + 2;
@@ -66,8 +66,8 @@ struct AttnParams {
   int n_q_heads;       // query heads
   int group;           // query heads per key/value head
   int n_qtiles;        // ceil(T / 128)
-  float scale_log2;    // log2(e) / sqrt(128)
-  float clamp_log2;    // c log2(e)
+  float sat_scale;     // log2(e) / (sqrt(128) 2 c log2(e)) = 1 / (2 c sqrt(128))
+  float clamp2_log2;   // 2 c log2(e)
   __nv_bfloat16* ctx;  // [rows, n_q_heads * 128]
   int ctx_ld;
   uint32_t* err;
@@ -79,13 +79,44 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// a * b + c clamped to [0, 1]
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float r;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// two fp32 in one 64-bit register (lo in the low half) and packed arithmetic on them
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 
 // One CTA: 128 queries of one head against the key blocks 0..(query tile).
 // Warp 0 streams Q once and K / V^T blocks through a 3-stage ring (TMA), warp 1
 // issues S_j = Q K_j^T into a double-buffered TMEM S and O += P_j V_j with P
-// read from TMEM, warps 2-9 turn S_j into P_j (two warps per 32 query rows, 64
-// keys each, so one warp's TMEM loads overlap the other's arithmetic) and
-// finally write ctx = O / l.
+// read from TMEM, warps 2-9 turn S_j into P_j (warps 2-5 the even blocks, 6-9
+// the odd ones, one query row per thread: the two groups work on two blocks at
+// once and the two warps that share a scheduler are out of phase) and finally
+// write ctx = O / l.
+//
+// Softmax weight of a logit s (c' = c log2(e)):
+//   2^(clamp(s log2(e) / sqrt(128), -c', c') - c') = 2^(2c' (u - 1)),
+//   u = saturate(s / (2 c sqrt(128)) + 1/2)
+// one saturating FMA per value, one packed FMA per pair, then ex2.
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
@@ -121,7 +152,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), kAttnSoftmaxThreads);  // every softmax thread
+      mbar_init(p_full(b), kAttnSoftmaxThreads / 2);  // every thread of the group that owns buffer b
       mbar_init(p_free(b), 1);
     }
     mbar_init(o_full, 1);
@@ -230,59 +261,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int q4 = warp & 3;                 // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
-    const int half = (warp - 2) >> 2;        // keys [64 half, 64 half + 64) of each block
+    const int grp = (warp - 2) >> 2;         // key blocks j = grp, grp + 2, ...; S and P buffers grp
+    const int half = grp;                    // epilogue: O columns [64 half, 64 half + 64)
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int qrow = qt * kAttnBM + r;
-    const float sc = p.scale_log2, cl = p.clamp_log2;
-    float l = 0.f;
+    const float ss = p.sat_scale;
+    const uint64_t w2 = f32x2(p.clamp2_log2, p.clamp2_log2), mw2 = f32x2(-p.clamp2_log2, -p.clamp2_log2);
+    uint64_t l2 = f32x2(0.f, 0.f);
     bool ok = true;
-    for (int j = 0; j < nblk; ++j) {
-      const int b = j & 1;
-      bool got = wait_bounded(s_full(b), (uint32_t)(j >> 1) & 1u, abort_flag, p.timeout_ns);
-      // P_b was last read by the MMA of block j - 2
-      if (got && j >= 2) got = wait_bounded(p_free(b), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
+    for (int j = grp; j < nblk; j += 2) {
+      bool got = wait_bounded(s_full(grp), (uint32_t)(j >> 1) & 1u, abort_flag, p.timeout_ns);
+      // P_grp was last read by the MMA of block j - 2
+      if (got && j >= 2) got = wait_bounded(p_free(grp), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         if (lane == 0) raise_abort(abort_flag, p.err);
         break;
       }
       tc_fence_after_sync();
-      uint32_t s0[32], s1[32];
-      const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)b * kAttnBN + half * 64;
-      tmem_ld_32x32b_x32(ts, s0);
-      tmem_ld_32x32b_x32(ts + 32, s1);
-      tmem_ld_wait();
-      // p = 2^(min(max(s log2(e) / sqrt(128), -c'), c') - c'), c' = c log2(e)
-      uint32_t pk[32];
-      if (j == qt) {  // the diagonal block: key (64 half + k) > query r is masked
+      const bool diag = (j == qt);  // the only block with keys after some queries
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t s0[32], s1[32];
+        const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)grp * kAttnBN + hh * 64;
+        tmem_ld_32x32b_x32(ts, s0);
+        tmem_ld_32x32b_x32(ts + 32, s1);
+        tmem_ld_wait();
+        uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
           const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-          const int key = half * 64 + 2 * c;
-          const float p0 = key > r ? 0.f : ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u0), sc, -cl), -2.f * cl), 0.f));
-          const float p1 =
-              key + 1 > r ? 0.f : ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u1), sc, -cl), -2.f * cl), 0.f));
-          l += p0 + p1;
+          const uint64_t t2 = fma_f32x2(f32x2(fma_sat(__uint_as_float(u0), ss, 0.5f), fma_sat(__uint_as_float(u1), ss, 0.5f)),
+                                        w2, mw2);
+          float t0, t1;
+          f32x2_split(t2, t0, t1);
+          float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          if (diag) {
+            const int key = hh * 64 + 2 * c;
+            if (key > r) p0 = 0.f;
+            if (key + 1 > r) p1 = 0.f;
+          }
+          l2 = add_f32x2(l2, f32x2(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
-          const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-          const float p0 = ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u0), sc, -cl), -2.f * cl), 0.f));
-          const float p1 = ex2_approx(fminf(fmaxf(fmaf(__uint_as_float(u1), sc, -cl), -2.f * cl), 0.f));
-          l += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
-        }
+        tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)grp * (kAttnBN / 2) + hh * 32, pk);
       }
-      tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)b * (kAttnBN / 2) + half * 32, pk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(p_full(b));
+      mbar_arrive(p_full(grp));
     }
+    float la, lb;
+    f32x2_split(l2, la, lb);
+    const float l = la + lb;
     bool got = ok && __all_sync(0xffffffffu, wait_bounded(o_full, 0, abort_flag, p.timeout_ns));
     l_part[half * kAttnBM + r] = l;
     // every softmax thread reaches this barrier exactly once; it also makes the
