@@ -141,7 +141,9 @@ moe_status_t enqueue(attn_block* B, const void* x, void* y, int T, cudaStream_t 
     p.ctx_ld = B->n_ctx;
     p.err = B->err;
     p.timeout_ns = kWaitLimitNs;
-    attn_kernel<<<p.n_qtiles * Hq, kAttnThreads, kAttnSmemBytes, st>>>(B->tm_q, B->tm_k, B->tm_vt, p);
+    // persistent: one CTA per SM, each looping over query tiles
+    const int grid = std::min(B->num_sms, p.n_qtiles * Hq);
+    attn_kernel<<<grid, kAttnThreads, kAttnSmemBytes, st>>>(B->tm_q, B->tm_k, B->tm_vt, p);
   }
   mark(ATTN_K_OPROJ);
   {

@@ -46,8 +46,9 @@ constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64
 constexpr int kAttnSoftmaxWarps = 8;                 // two groups of four: even and odd key blocks
 constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
 constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
-constexpr int kAttnNumBars = 1 + 2 * kAttnStages + 6 + 2;
-constexpr size_t kAttnBarBytes = 128;                // barriers, TMEM address, abort flag
+// q_full, q_empty, kv_full[3], kv_empty[3], s_full[2], p_full[2], p_free[2], o_full, o_empty, drain
+constexpr int kAttnNumBars = 2 + 2 * kAttnStages + 6 + 3;
+constexpr size_t kAttnBarBytes = 256;                // barriers, TMEM address, abort flag
 constexpr size_t kAttnSmemBytes =
     1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + kAttnBarBytes + 2 * kAttnBM * sizeof(float);
 static_assert(8 * kAttnNumBars + 8 <= kAttnBarBytes, "barrier block");
@@ -79,6 +80,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Bounded wait that lets the warp sleep: each try_wait may suspend the thread
+// until the phase completes or about 0.5 ms pass, so waiting warps take no
+// issue slots from the working ones.  Gives up (false) after limit_ns or when
+// *abort becomes non-zero, like wait_bounded.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(500000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_sleep(uint32_t bar, uint32_t parity, const volatile uint32_t* abort,
+                                           uint64_t limit_ns) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // a * b + c clamped to [0, 1]
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float r;
@@ -105,13 +132,23 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
-// One CTA: 128 queries of one head against the key blocks 0..(query tile).
-// Warp 0 streams Q once and K / V^T blocks through a 3-stage ring (TMA), warp 1
-// issues S_j = Q K_j^T into a double-buffered TMEM S and O += P_j V_j with P
-// read from TMEM, warps 2-9 turn S_j into P_j (warps 2-5 the even blocks, 6-9
-// the odd ones, one query row per thread: the two groups work on two blocks at
-// once and the two warps that share a scheduler are out of phase) and finally
-// write ctx = O / l.
+// Work item i (heaviest first): query tile qt = n_qtiles - 1 - i / Hq of head
+// h = i % Hq, i.e. 128 queries against the key blocks 0..qt.  The kernel is
+// persistent: CTA c takes items c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (G CTAs,
+// alternating direction so the long and short items even out).
+__device__ __forceinline__ int attn_item_of(int c, int k, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// Per CTA, one item after another: warp 0 streams Q (one buffer, reloaded as
+// soon as the item's last Q K^T product is done) and K / V^T blocks through a
+// 3-stage ring (TMA); warp 1 issues S = Q K^T into a double-buffered TMEM S and
+// O += P V with P read from TMEM; warps 2-9 turn S into P (warps 2-5 the even
+// blocks, 6-9 the odd ones, counted across items; one query row per thread: the
+// two groups work on two blocks at once and the two warps that share a
+// scheduler are out of phase) and at the end of an item write ctx = O / l.
+// Block counters run across items, so ring stages, buffers and barrier phases
+// continue from one item to the next.
 //
 // Softmax weight of a logit s (c' = c log2(e)):
 //   2^(clamp(s log2(e) / sqrt(128), -c', c') - c') = 2^(2c' (u - 1)),
@@ -122,30 +159,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                // [128 x 128] bf16
-  uint8_t* sKV = smem + kAttnTile;   // stage s: K at 2s tiles, V^T at 2s + 1 tiles
+  uint8_t* sQ = smem;                // [128 x 128] fp16
+  uint8_t* sKV = smem + kAttnTile;   // stage s: K (fp16) at 2s tiles, V^T (bf16) at 2s + 1 tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (1 + 2 * kAttnStages));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   float* l_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kAttnBarBytes);  // [2][128]
   const uint32_t b0 = smem_addr(bars);
-  const uint32_t q_full = b0;
-  auto kv_full = [&](int s) { return b0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return b0 + 8u * (1 + kAttnStages + s); };
-  auto s_full = [&](int b) { return b0 + 8u * (1 + 2 * kAttnStages + b); };
-  auto p_full = [&](int b) { return b0 + 8u * (3 + 2 * kAttnStages + b); };
-  auto p_free = [&](int b) { return b0 + 8u * (5 + 2 * kAttnStages + b); };
-  const uint32_t o_full = b0 + 8u * (7 + 2 * kAttnStages);
-  const uint32_t drain = o_full + 8u;
+  const uint32_t q_full = b0, q_empty = b0 + 8u;
+  auto kv_full = [&](int s) { return b0 + 8u * (2 + s); };
+  auto kv_empty = [&](int s) { return b0 + 8u * (2 + kAttnStages + s); };
+  auto s_full = [&](int b) { return b0 + 8u * (2 + 2 * kAttnStages + b); };
+  auto p_full = [&](int b) { return b0 + 8u * (4 + 2 * kAttnStages + b); };
+  auto p_free = [&](int b) { return b0 + 8u * (6 + 2 * kAttnStages + b); };
+  const uint32_t o_full = b0 + 8u * (8 + 2 * kAttnStages);
+  const uint32_t o_empty = o_full + 8u;
+  const uint32_t drain = o_full + 16u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.x / p.n_q_heads;  // longest query tiles first
-  const int h = (int)blockIdx.x % p.n_q_heads;
-  const int g = h / p.group;
-  const int nblk = qt + 1;
+  const int G = (int)gridDim.x, n_items = p.n_qtiles * p.n_q_heads;
+  auto item_qt = [&](int i) { return p.n_qtiles - 1 - i / p.n_q_heads; };
+  auto item_h = [&](int i) { return i % p.n_q_heads; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kAttnStages; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -156,6 +194,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(p_free(b), 1);
     }
     mbar_init(o_full, 1);
+    mbar_init(o_empty, kAttnSoftmaxWarps);  // one arrival per softmax warp
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -178,39 +217,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       bool ok = true;
-      int n_issued = 0;
-      mbar_arrive_expect_tx(q_full, kAttnTile);
-      const int qrow0 = h * p.t_stride + qt * kAttnBM;
-      tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
-      tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
-      for (int j = 0; j < nblk; ++j) {
-        const int s = j % kAttnStages;
-        if (j >= kAttnStages &&
-            !wait_bounded(kv_empty(s), (uint32_t)((j / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
+      int gb = 0, n_q = 0;  // blocks issued (across items), Q tiles issued
+      for (int k = 0; ok; ++k) {
+        const int i = attn_item_of((int)blockIdx.x, k, G);
+        if (i >= n_items) break;
+        const int qt = item_qt(i), h = item_h(i), g = h / p.group;
+        // the previous item's Q K^T products are done with the Q buffer
+        if (k > 0 && !wait_sleep(q_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
-        const uint32_t fb = kv_full(s);
-        mbar_arrive_expect_tx(fb, 2 * kAttnTile);
-        uint8_t* sk = sKV + (size_t)(2 * s) * kAttnTile;
-        uint8_t* sv = sk + kAttnTile;
-        const int krow = g * p.t_stride + j * kAttnBN;
-        tma_load_2d(smem_addr(sk), &tm_k, fb, 0, krow);
-        tma_load_2d(smem_addr(sk + kAttnHalf), &tm_k, fb, 64, krow);
-        tma_load_2d(smem_addr(sv), &tm_vt, fb, j * kAttnBN, g * kAttnDh);
-        tma_load_2d(smem_addr(sv + kAttnHalf), &tm_vt, fb, j * kAttnBN + 64, g * kAttnDh);
-        n_issued = j + 1;
+        mbar_arrive_expect_tx(q_full, kAttnTile);
+        const int qrow0 = h * p.t_stride + qt * kAttnBM;
+        tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
+        tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
+        n_q = k + 1;
+        for (int j = 0; j <= qt; ++j, ++gb) {
+          const int s = gb % kAttnStages;
+          if (gb >= kAttnStages &&
+              !wait_sleep(kv_empty(s), (uint32_t)((gb / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = kv_full(s);
+          mbar_arrive_expect_tx(fb, 2 * kAttnTile);
+          uint8_t* sk = sKV + (size_t)(2 * s) * kAttnTile;
+          uint8_t* sv = sk + kAttnTile;
+          const int krow = g * p.t_stride + j * kAttnBN;
+          tma_load_2d(smem_addr(sk), &tm_k, fb, 0, krow);
+          tma_load_2d(smem_addr(sk + kAttnHalf), &tm_k, fb, 64, krow);
+          tma_load_2d(smem_addr(sv), &tm_vt, fb, j * kAttnBN, g * kAttnDh);
+          tma_load_2d(smem_addr(sv + kAttnHalf), &tm_vt, fb, j * kAttnBN + 64, g * kAttnDh);
+        }
       }
       // every release of a stage by the MMA issuer has landed before exit
-      for (int j = (nblk > kAttnStages ? nblk - kAttnStages : 0); j < nblk && ok; ++j)
-        if (!wait_bounded(kv_empty(j % kAttnStages), (uint32_t)(j / kAttnStages) & 1u, abort_flag, p.timeout_ns))
+      for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb && ok; ++b)
+        if (!wait_sleep(kv_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
           ok = false;
       if (!ok) {
         raise_abort(abort_flag, p.err);
         // this role's copies still in flight land before the CTA exits
-        wait_bounded(q_full, 0, nullptr, p.timeout_ns);
-        for (int j = (n_issued > kAttnStages ? n_issued - kAttnStages : 0); j < n_issued; ++j)
-          wait_bounded(kv_full(j % kAttnStages), (uint32_t)(j / kAttnStages) & 1u, nullptr, p.timeout_ns);
+        if (n_q > 0) wait_sleep(q_full, (uint32_t)(n_q - 1) & 1u, nullptr, p.timeout_ns);
+        for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb; ++b)
+          wait_sleep(kv_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -218,130 +267,157 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       const uint32_t tO = tmem_base, tS = tmem_base + kAttnColS, tP = tmem_base + kAttnColP;
       const uint32_t qa = smem_addr(sQ);
-      bool ok = wait_bounded(q_full, 0, abort_flag, p.timeout_ns);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kAttnStages;
-        if (!wait_bounded(kv_full(s), (uint32_t)(j / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
+      bool ok = true;
+      int gb = 0;  // first block of the current item (across items)
+      auto issue_s = [&](int b) -> bool {
+        const int s = b % kAttnStages;
+        if (!wait_sleep(kv_full(s), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
         tc_fence_after_sync();
         const uint32_t kb = smem_addr(sKV + (size_t)(2 * s) * kAttnTile);
 #pragma unroll
         for (int kk = 0; kk < kAttnDh / 16; ++kk)  // K = 16 along the head dimension
-          umma_bf16(tS + (uint32_t)(j & 1) * kAttnBN, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
+          umma_bf16(tS + (uint32_t)(b & 1) * kAttnBN, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
                     smem_desc_k_sw128(kb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdescF16, kk != 0);
-        umma_commit(s_full(j & 1));
+        umma_commit(s_full(b & 1));
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < nblk && ok; ++j) {
-        // S_{j+1} runs on the tensor cores while the softmax warps work on S_j
-        if (j + 1 < nblk && !issue_s(j + 1)) {
+      for (int k = 0; ok; ++k) {
+        const int i = attn_item_of((int)blockIdx.x, k, G);
+        if (i >= n_items) break;
+        const int nblk = item_qt(i) + 1;
+        if (!wait_sleep(q_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
-        const int b = j & 1;
-        if (!wait_bounded(p_full(b), (uint32_t)(j >> 1) & 1u, abort_flag, p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t vb = smem_addr(sKV + (size_t)(2 * (j % kAttnStages) + 1) * kAttnTile);
+        ok = issue_s(gb);
+        if (ok && nblk == 1) umma_commit(q_empty);
+        for (int j = 0; j < nblk && ok; ++j) {
+          const int b = gb + j;
+          // S_{j+1} runs on the tensor cores while the softmax warps work on S_j
+          if (j + 1 < nblk) {
+            if (!issue_s(b + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 == nblk) umma_commit(q_empty);  // the item's last Q K^T product is issued
+          }
+          if (!wait_sleep(p_full(b & 1), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns) ||
+              (j == 0 && k > 0 && !wait_sleep(o_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t vb = smem_addr(sKV + (size_t)(2 * (b % kAttnStages) + 1) * kAttnTile);
 #pragma unroll
-        for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
-          umma_bf16_tmem_a(tO, tP + (uint32_t)b * (kAttnBN / 2) + 8 * kk,
-                           smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc, (j | kk) != 0);
-        umma_commit(kv_empty(j % kAttnStages));
-        umma_commit(p_free(b));
+          for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
+            umma_bf16_tmem_a(tO, tP + (uint32_t)(b & 1) * (kAttnBN / 2) + 8 * kk,
+                             smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc,
+                             (j | kk) != 0);
+          umma_commit(kv_empty(b % kAttnStages));
+          umma_commit(p_free(b & 1));
+        }
+        if (!ok) break;
+        umma_commit(o_full);
+        gb += nblk;
       }
-      if (ok) umma_commit(o_full);
       // all MMAs issued by this thread are complete before TMEM is freed
       umma_commit(drain);
-      if (!wait_bounded(drain, 0, nullptr, p.timeout_ns)) ok = false;
+      if (!wait_sleep(drain, 0, nullptr, p.timeout_ns)) ok = false;
       if (!ok) raise_abort(abort_flag, p.err);
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int q4 = warp & 3;                 // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
-    const int grp = (warp - 2) >> 2;         // key blocks j = grp, grp + 2, ...; S and P buffers grp
+    const int grp = (warp - 2) >> 2;         // global blocks gb with gb % 2 == grp; S and P buffers grp
     const int half = grp;                    // epilogue: O columns [64 half, 64 half + 64)
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const int qrow = qt * kAttnBM + r;
     const float ss = p.sat_scale;
     const uint64_t w2 = f32x2(p.clamp2_log2, p.clamp2_log2), mw2 = f32x2(-p.clamp2_log2, -p.clamp2_log2);
-    uint64_t l2 = f32x2(0.f, 0.f);
     bool ok = true;
-    for (int j = grp; j < nblk; j += 2) {
-      bool got = wait_bounded(s_full(grp), (uint32_t)(j >> 1) & 1u, abort_flag, p.timeout_ns);
-      // P_grp was last read by the MMA of block j - 2
-      if (got && j >= 2) got = wait_bounded(p_free(grp), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        if (lane == 0) raise_abort(abort_flag, p.err);
-        break;
-      }
-      tc_fence_after_sync();
-      const bool diag = (j == qt);  // the only block with keys after some queries
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t s0[32], s1[32];
-        const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)grp * kAttnBN + hh * 64;
-        tmem_ld_32x32b_x32(ts, s0);
-        tmem_ld_32x32b_x32(ts + 32, s1);
-        tmem_ld_wait();
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
-          const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-          const uint64_t t2 = fma_f32x2(f32x2(fma_sat(__uint_as_float(u0), ss, 0.5f), fma_sat(__uint_as_float(u1), ss, 0.5f)),
-                                        w2, mw2);
-          float t0, t1;
-          f32x2_split(t2, t0, t1);
-          float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-          if (diag) {
-            const int key = hh * 64 + 2 * c;
-            if (key > r) p0 = 0.f;
-            if (key + 1 > r) p1 = 0.f;
-          }
-          l2 = add_f32x2(l2, f32x2(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
+    int gb0 = 0;  // first global block of the current item
+    for (int k = 0;; ++k) {
+      const int i = attn_item_of((int)blockIdx.x, k, G);
+      if (i >= n_items) break;
+      const int qt = item_qt(i), h = item_h(i), nblk = qt + 1;
+      uint64_t l2 = f32x2(0.f, 0.f);
+      for (int j = (grp - gb0) & 1; j < nblk && ok; j += 2) {
+        const int b = gb0 + j;
+        bool got = wait_sleep(s_full(grp), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns);
+        // P_grp was last read by the MMA of global block b - 2
+        if (got && b >= 2) got = wait_sleep(p_free(grp), (uint32_t)((b >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          if (lane == 0) raise_abort(abort_flag, p.err);
+          break;
         }
-        tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)grp * (kAttnBN / 2) + hh * 32, pk);
+        tc_fence_after_sync();
+        const bool diag = (j == qt);  // the only block with keys after some queries
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t s0[32], s1[32];
+          const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)grp * kAttnBN + hh * 64;
+          tmem_ld_32x32b_x32(ts, s0);
+          tmem_ld_32x32b_x32(ts + 32, s1);
+          tmem_ld_wait();
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
+            const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+            const uint64_t t2 = fma_f32x2(
+                f32x2(fma_sat(__uint_as_float(u0), ss, 0.5f), fma_sat(__uint_as_float(u1), ss, 0.5f)), w2, mw2);
+            float t0, t1;
+            f32x2_split(t2, t0, t1);
+            float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            if (diag) {
+              const int key = hh * 64 + 2 * c;
+              if (key > r) p0 = 0.f;
+              if (key + 1 > r) p1 = 0.f;
+            }
+            l2 = add_f32x2(l2, f32x2(p0, p1));
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)grp * (kAttnBN / 2) + hh * 32, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(p_full(grp));
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(p_full(grp));
-    }
-    float la, lb;
-    f32x2_split(l2, la, lb);
-    const float l = la + lb;
-    bool got = ok && __all_sync(0xffffffffu, wait_bounded(o_full, 0, abort_flag, p.timeout_ns));
-    l_part[half * kAttnBM + r] = l;
-    // every softmax thread reaches this barrier exactly once; it also makes the
-    // two halves' row sums visible to each other
-    ok = named_bar_and(1, kAttnSoftmaxThreads, got);
-    if (ok) {
+      bool got = ok && __all_sync(0xffffffffu, wait_sleep(o_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns));
+      float la, lb;
+      f32x2_split(l2, la, lb);
+      l_part[half * kAttnBM + r] = la + lb;
+      // every softmax thread reaches this barrier once per item; it also makes
+      // the two groups' row sums visible to each other
+      ok = named_bar_and(1, kAttnSoftmaxThreads, got);
+      if (!ok) break;
       tc_fence_after_sync();
       const float inv = 1.f / (l_part[r] + l_part[kAttnBM + r]);
+      const int qrow = qt * kAttnBM + r;
       __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh + half * 64;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_off + half * 64 + c * 32, o);
-        tmem_ld_wait();
-        if (qrow < p.T) {
-          uint32_t pk[16];
+      uint32_t o0[32], o1[32];
+      tmem_ld_32x32b_x32(tmem_base + lane_off + half * 64, o0);
+      tmem_ld_32x32b_x32(tmem_base + lane_off + half * 64 + 32, o1);
+      tmem_ld_wait();
+      // O and this thread's l_part reads are done: the next item may overwrite them
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+      if (qrow < p.T) {
+        uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int c = 0; c < 16; ++c) {
+          pk[c] = pack_bf16x2(__uint_as_float(o0[2 * c]) * inv, __uint_as_float(o0[2 * c + 1]) * inv);
+          pk[16 + c] = pack_bf16x2(__uint_as_float(o1[2 * c]) * inv, __uint_as_float(o1[2 * c + 1]) * inv);
         }
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
-    } else if (lane == 0) {
-      raise_abort(abort_flag, p.err);
+      gb0 += nblk;
     }
+    if (!ok && lane == 0) raise_abort(abort_flag, p.err);
   }
 
   tc_fence_before_sync();
