@@ -40,15 +40,14 @@ namespace moe {
 constexpr int kAttnDh = 128;                         // head dimension
 constexpr int kAttnBM = 128;                         // queries of one CTA (TMEM lanes)
 constexpr int kAttnBN = 128;                         // keys of one block
-constexpr int kAttnStages = 3;                       // stages of the K ring and of the V^T ring
+constexpr int kAttnStages = 3;                       // K/V blocks in flight
 constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 bf16, two 64-column boxes
 constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kAttnSoftmaxWarps = 8;                 // two groups of four: even and odd key blocks
 constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
 constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
-// q_full, q_empty, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full[2], p_free[2],
-// o_full, o_empty, drain
-constexpr int kAttnNumBars = 2 + 4 * kAttnStages + 6 + 3;
+// q_full, q_empty, kv_full[3], kv_empty[3], s_full[2], p_full[2], p_free[2], o_full, o_empty, drain
+constexpr int kAttnNumBars = 2 + 2 * kAttnStages + 6 + 3;
 constexpr size_t kAttnBarBytes = 256;                // barriers, TMEM address, abort flag
 constexpr size_t kAttnSmemBytes =
     1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + kAttnBarBytes + 2 * kAttnBM * sizeof(float);
@@ -142,10 +141,8 @@ __device__ __forceinline__ int attn_item_of(int c, int k, int G) {
 }
 
 // Per CTA, one item after another: warp 0 streams Q (one buffer, reloaded as
-// soon as the item's last Q K^T product is done) and K and V^T blocks through
-// two 3-stage rings (TMA): a K stage is released as soon as its Q K^T product
-// is done, which is a block and a half before the P V product that releases
-// the V^T stage, so the next keys are fetched that much earlier; warp 1 issues S = Q K^T into a double-buffered TMEM S and
+// soon as the item's last Q K^T product is done) and K / V^T blocks through a
+// 3-stage ring (TMA); warp 1 issues S = Q K^T into a double-buffered TMEM S and
 // O += P V with P read from TMEM; warps 2-9 turn S into P (warps 2-5 the even
 // blocks, 6-9 the odd ones, counted across items; one query row per thread: the
 // two groups work on two blocks at once and the two warps that share a
@@ -163,22 +160,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                // [128 x 128] fp16
-  uint8_t* sK = smem + kAttnTile;                    // K ring (fp16), 3 tiles
-  uint8_t* sV = sK + (size_t)kAttnStages * kAttnTile;  // V^T ring (bf16), 3 tiles
+  uint8_t* sKV = smem + kAttnTile;   // stage s: K (fp16) at 2s tiles, V^T (bf16) at 2s + 1 tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (1 + 2 * kAttnStages));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   float* l_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kAttnBarBytes);  // [2][128]
   const uint32_t b0 = smem_addr(bars);
   const uint32_t q_full = b0, q_empty = b0 + 8u;
-  auto k_full = [&](int s) { return b0 + 8u * (2 + s); };
-  auto k_empty = [&](int s) { return b0 + 8u * (2 + kAttnStages + s); };
-  auto v_full = [&](int s) { return b0 + 8u * (2 + 2 * kAttnStages + s); };
-  auto v_empty = [&](int s) { return b0 + 8u * (2 + 3 * kAttnStages + s); };
-  auto s_full = [&](int b) { return b0 + 8u * (2 + 4 * kAttnStages + b); };
-  auto p_full = [&](int b) { return b0 + 8u * (4 + 4 * kAttnStages + b); };
-  auto p_free = [&](int b) { return b0 + 8u * (6 + 4 * kAttnStages + b); };
-  const uint32_t o_full = b0 + 8u * (8 + 4 * kAttnStages);
+  auto kv_full = [&](int s) { return b0 + 8u * (2 + s); };
+  auto kv_empty = [&](int s) { return b0 + 8u * (2 + kAttnStages + s); };
+  auto s_full = [&](int b) { return b0 + 8u * (2 + 2 * kAttnStages + b); };
+  auto p_full = [&](int b) { return b0 + 8u * (4 + 2 * kAttnStages + b); };
+  auto p_free = [&](int b) { return b0 + 8u * (6 + 2 * kAttnStages + b); };
+  const uint32_t o_full = b0 + 8u * (8 + 2 * kAttnStages);
   const uint32_t o_empty = o_full + 8u;
   const uint32_t drain = o_full + 16u;
 
@@ -191,10 +185,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -225,7 +217,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       bool ok = true;
-      int n_k = 0, n_v = 0, n_q = 0;  // K and V^T blocks issued (across items), Q tiles issued
+      int gb = 0, n_q = 0;  // blocks issued (across items), Q tiles issued
       for (int k = 0; ok; ++k) {
         const int i = attn_item_of((int)blockIdx.x, k, G);
         if (i >= n_items) break;
@@ -240,45 +232,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
         tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
         n_q = k + 1;
-        for (int j = 0; j <= qt; ++j) {
-          const int s = n_k % kAttnStages;
-          if (n_k >= kAttnStages &&
-              !wait_sleep(k_empty(s), (uint32_t)((n_k / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
+        for (int j = 0; j <= qt; ++j, ++gb) {
+          const int s = gb % kAttnStages;
+          if (gb >= kAttnStages &&
+              !wait_sleep(kv_empty(s), (uint32_t)((gb / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(k_full(s), kAttnTile);
+          const uint32_t fb = kv_full(s);
+          mbar_arrive_expect_tx(fb, 2 * kAttnTile);
+          uint8_t* sk = sKV + (size_t)(2 * s) * kAttnTile;
+          uint8_t* sv = sk + kAttnTile;
           const int krow = g * p.t_stride + j * kAttnBN;
-          tma_load_2d(smem_addr(sK + (size_t)s * kAttnTile), &tm_k, k_full(s), 0, krow);
-          tma_load_2d(smem_addr(sK + (size_t)s * kAttnTile + kAttnHalf), &tm_k, k_full(s), 64, krow);
-          ++n_k;
-          if (n_v >= kAttnStages &&
-              !wait_sleep(v_empty(s), (uint32_t)((n_v / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(v_full(s), kAttnTile);
-          tma_load_2d(smem_addr(sV + (size_t)s * kAttnTile), &tm_vt, v_full(s), j * kAttnBN, g * kAttnDh);
-          tma_load_2d(smem_addr(sV + (size_t)s * kAttnTile + kAttnHalf), &tm_vt, v_full(s), j * kAttnBN + 64,
-                      g * kAttnDh);
-          ++n_v;
+          tma_load_2d(smem_addr(sk), &tm_k, fb, 0, krow);
+          tma_load_2d(smem_addr(sk + kAttnHalf), &tm_k, fb, 64, krow);
+          tma_load_2d(smem_addr(sv), &tm_vt, fb, j * kAttnBN, g * kAttnDh);
+          tma_load_2d(smem_addr(sv + kAttnHalf), &tm_vt, fb, j * kAttnBN + 64, g * kAttnDh);
         }
       }
       // every release of a stage by the MMA issuer has landed before exit
-      for (int b = (n_k > kAttnStages ? n_k - kAttnStages : 0); b < n_k && ok; ++b)
-        if (!wait_sleep(k_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
-          ok = false;
-      for (int b = (n_v > kAttnStages ? n_v - kAttnStages : 0); b < n_v && ok; ++b)
-        if (!wait_sleep(v_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
+      for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb && ok; ++b)
+        if (!wait_sleep(kv_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
           ok = false;
       if (!ok) {
         raise_abort(abort_flag, p.err);
         // this role's copies still in flight land before the CTA exits
         if (n_q > 0) wait_sleep(q_full, (uint32_t)(n_q - 1) & 1u, nullptr, p.timeout_ns);
-        for (int b = (n_k > kAttnStages ? n_k - kAttnStages : 0); b < n_k; ++b)
-          wait_sleep(k_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
-        for (int b = (n_v > kAttnStages ? n_v - kAttnStages : 0); b < n_v; ++b)
-          wait_sleep(v_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
+        for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb; ++b)
+          wait_sleep(kv_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -290,15 +271,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int gb = 0;  // first block of the current item (across items)
       auto issue_s = [&](int b) -> bool {
         const int s = b % kAttnStages;
-        if (!wait_sleep(k_full(s), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
+        if (!wait_sleep(kv_full(s), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
         tc_fence_after_sync();
-        const uint32_t kb = smem_addr(sK + (size_t)s * kAttnTile);
+        const uint32_t kb = smem_addr(sKV + (size_t)(2 * s) * kAttnTile);
 #pragma unroll
         for (int kk = 0; kk < kAttnDh / 16; ++kk)  // K = 16 along the head dimension
           umma_bf16(tS + (uint32_t)(b & 1) * kAttnBN, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
                     smem_desc_k_sw128(kb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdescF16, kk != 0);
         umma_commit(s_full(b & 1));
-        umma_commit(k_empty(s));  // the K stage is free once this product is done
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -322,19 +302,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (j + 2 == nblk) umma_commit(q_empty);  // the item's last Q K^T product is issued
           }
           if (!wait_sleep(p_full(b & 1), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns) ||
-              !wait_sleep(v_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns) ||
               (j == 0 && k > 0 && !wait_sleep(o_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t vb = smem_addr(sV + (size_t)(b % kAttnStages) * kAttnTile);
+          const uint32_t vb = smem_addr(sKV + (size_t)(2 * (b % kAttnStages) + 1) * kAttnTile);
 #pragma unroll
           for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
             umma_bf16_tmem_a(tO, tP + (uint32_t)(b & 1) * (kAttnBN / 2) + 8 * kk,
                              smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc,
                              (j | kk) != 0);
-          umma_commit(v_empty(b % kAttnStages));
+          umma_commit(kv_empty(b % kAttnStages));
           umma_commit(p_free(b & 1));
         }
         if (!ok) break;
