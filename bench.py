@@ -288,6 +288,31 @@ def attn_work(inp):
     }
 
 
+ATTN_KERNEL_FILES = ["k_attn.cuh", "ptx.cuh", "ptx_pair.cuh", "ptx_tmem.cuh", "common.cuh"]
+
+
+def attn_compulsory_bytes(inp):
+    """Bytes the attention kernel must move at least once: Q, K and V^T in (each
+    key/value head read once from DRAM; the re-reads by the query tiles are L2
+    hits), the context rows out."""
+    return inp.Hq * inp.T * inp.Dh * 2 + 2 * inp.Hkv * inp.T * inp.Dh * 2 + inp.T * inp.Hq * inp.Dh * 2
+
+
+def attn_recorded_traffic(inp):
+    """DRAM bytes per launch of attn_kernel from the committed ncu record, if it
+    was captured on the current source, scaled by compulsory bytes (the key and
+    value heads stay in L2 at every length up to 65536 tokens: 8 heads x 2 x
+    65536 x 256 B = 268 MB would not, so only up to 16384).  Else None."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f).get("attn_kernel")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != source_hash(ATTN_KERNEL_FILES) or inp.T > 16384:
+        return None
+    return int(rec["dram_bytes_per_launch"] * attn_compulsory_bytes(inp) / rec["compulsory_bytes"])
+
+
 def attn_cpu_baseline(inp, budget_s=20.0, seed=7):
     """The attention oracle on this host: keys and values of the whole sequence
     once, then a seeded sample of query tokens; tokens/s = T / (key/value time +
@@ -409,7 +434,9 @@ def run_attn(args, rank, world, local_rank):
     roof["algorithmic_per_launch"] = amount
     roof["kernel_function"] = {"attn": "attn_kernel", "qkv": "grouped_gemm_kernel<1, 0>",
                                "oproj": "grouped_gemm_kernel<1, 0>"}.get(dom, dom)
-    roof["traffic"] = None
+    roof["traffic"] = attn_recorded_traffic(inp) if dom == "attn" else None
+    roof["traffic_note"] = ("ncu DRAM bytes of the T=2048 capture scaled by compulsory bytes; the context rows "
+                            "written stay in L2 when the kernel ends, so the figure sits below the compulsory bytes")
     tc_flops = sum(a for b, a in work.values() if b == "tensor")
     result = {
         "metric": ATTN_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
