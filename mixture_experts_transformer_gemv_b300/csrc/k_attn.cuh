@@ -40,21 +40,20 @@ namespace moe {
 constexpr int kAttnDh = 128;                         // head dimension
 constexpr int kAttnBM = 128;                         // queries of one CTA (TMEM lanes)
 constexpr int kAttnBN = 128;                         // keys of one block
-constexpr int kAttnStages = 3;                       // stages of the K ring and of the V^T ring
+constexpr int kAttnStages = 3;                       // K/V blocks in flight
 constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 bf16, two 64-column boxes
 constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kAttnSoftmaxWarps = 8;                 // two groups of four: even and odd key blocks
 constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
 constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
-constexpr int kAttnSBufs = 3;                        // TMEM S buffers (P is written over its own S)
-// q_full, q_empty, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[3], p_full[3], o_full, o_empty, drain
-constexpr int kAttnNumBars = 2 + 4 * kAttnStages + 2 * kAttnSBufs + 3;
+// q_full, q_empty, kv_full[3], kv_empty[3], s_full[2], p_full[2], p_free[2], o_full, o_empty, drain
+constexpr int kAttnNumBars = 2 + 2 * kAttnStages + 6 + 3;
 constexpr size_t kAttnBarBytes = 256;                // barriers, TMEM address, abort flag
 constexpr size_t kAttnSmemBytes =
     1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + kAttnBarBytes + 2 * kAttnBM * sizeof(float);
 static_assert(8 * kAttnNumBars + 8 <= kAttnBarBytes, "barrier block");
-constexpr uint32_t kAttnTmemCols = 512;              // O | S0 | S1 | S2 (P_b in the first 64 columns of S_b)
-constexpr uint32_t kAttnColS = 128;
+constexpr uint32_t kAttnTmemCols = 512;              // O | S0 | S1 | P0 | P1
+constexpr uint32_t kAttnColS = 128, kAttnColP = 384;
 constexpr uint32_t kAttnIdesc = idesc_bf16_f32(kAttnBM, kAttnBN);  // P V: bf16 x bf16
 // Q K^T: fp16 x fp16 (format 0 in bits 7-9 and 10-12), fp32 accumulator
 constexpr uint32_t kAttnIdescF16 = (1u << 4) | (static_cast<uint32_t>(kAttnBN >> 3) << 17) |
@@ -142,21 +141,14 @@ __device__ __forceinline__ int attn_item_of(int c, int k, int G) {
 }
 
 // Per CTA, one item after another: warp 0 streams Q (one buffer, reloaded as
-// soon as the item's last Q K^T product is done) and K and V^T blocks through
-// two 3-stage rings (TMA; a K stage is released when its Q K^T product is done,
-// a V^T stage when its P V product is).  Warp 1 keeps three S = Q K^T products
-// ahead of the softmax in three TMEM buffers: it issues S_{j+3} right after
-// P V_j, so between S_j completing and P V_j starting the tensor cores have
-// four products of work (about 2000 cycles) while the softmax of block j and
-// its two barrier hand-offs run.  P_j (bf16) is written over the first 64
-// columns of S_j's buffer and read from TMEM as the A operand of P V_j; the
-// tensor core runs one CTA's MMAs in issue order, so S_{j+3}, issued after
-// P V_j, overwrites P_j only after P V_j has read it.  Warps 2-9 turn S into P
-// (warps 2-5 the even blocks, 6-9 the odd ones, counted across items; one query
-// row per thread: the two groups work on two blocks at once and the two warps
-// that share a scheduler are out of phase) and at the end of an item write
-// ctx = O / l.  Block counters run across items, so ring stages, buffers and
-// barrier phases continue from one item to the next.
+// soon as the item's last Q K^T product is done) and K / V^T blocks through a
+// 3-stage ring (TMA); warp 1 issues S = Q K^T into a double-buffered TMEM S and
+// O += P V with P read from TMEM; warps 2-9 turn S into P (warps 2-5 the even
+// blocks, 6-9 the odd ones, counted across items; one query row per thread: the
+// two groups work on two blocks at once and the two warps that share a
+// scheduler are out of phase) and at the end of an item write ctx = O / l.
+// Block counters run across items, so ring stages, buffers and barrier phases
+// continue from one item to the next.
 //
 // Softmax weight of a logit s (c' = c log2(e)):
 //   2^(clamp(s log2(e) / sqrt(128), -c', c') - c') = 2^(2c' (u - 1)),
@@ -168,21 +160,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                // [128 x 128] fp16
-  uint8_t* sK = smem + kAttnTile;                    // K ring (fp16), 3 tiles
-  uint8_t* sV = sK + (size_t)kAttnStages * kAttnTile;  // V^T ring (bf16), 3 tiles
+  uint8_t* sKV = smem + kAttnTile;   // stage s: K (fp16) at 2s tiles, V^T (bf16) at 2s + 1 tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (1 + 2 * kAttnStages));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   float* l_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kAttnBarBytes);  // [2][128]
   const uint32_t b0 = smem_addr(bars);
   const uint32_t q_full = b0, q_empty = b0 + 8u;
-  auto k_full = [&](int s) { return b0 + 8u * (2 + s); };
-  auto k_empty = [&](int s) { return b0 + 8u * (2 + kAttnStages + s); };
-  auto v_full = [&](int s) { return b0 + 8u * (2 + 2 * kAttnStages + s); };
-  auto v_empty = [&](int s) { return b0 + 8u * (2 + 3 * kAttnStages + s); };
-  auto s_full = [&](int b) { return b0 + 8u * (2 + 4 * kAttnStages + b); };
-  auto p_full = [&](int b) { return b0 + 8u * (2 + 4 * kAttnStages + kAttnSBufs + b); };
-  const uint32_t o_full = b0 + 8u * (2 + 4 * kAttnStages + 2 * kAttnSBufs);
+  auto kv_full = [&](int s) { return b0 + 8u * (2 + s); };
+  auto kv_empty = [&](int s) { return b0 + 8u * (2 + kAttnStages + s); };
+  auto s_full = [&](int b) { return b0 + 8u * (2 + 2 * kAttnStages + b); };
+  auto p_full = [&](int b) { return b0 + 8u * (4 + 2 * kAttnStages + b); };
+  auto p_free = [&](int b) { return b0 + 8u * (6 + 2 * kAttnStages + b); };
+  const uint32_t o_full = b0 + 8u * (8 + 2 * kAttnStages);
   const uint32_t o_empty = o_full + 8u;
   const uint32_t drain = o_full + 16u;
 
@@ -195,14 +185,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
     }
-    for (int b = 0; b < kAttnSBufs; ++b) {
+    for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), kAttnSoftmaxThreads / 2);  // every thread of the group that owns the block
+      mbar_init(p_full(b), kAttnSoftmaxThreads / 2);  // every thread of the group that owns buffer b
+      mbar_init(p_free(b), 1);
     }
     mbar_init(o_full, 1);
     mbar_init(o_empty, kAttnSoftmaxWarps);  // one arrival per softmax warp
@@ -228,32 +217,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       bool ok = true;
-      int n_k = 0, n_v = 0, n_q = 0;  // K and V^T blocks issued (across items), Q tiles issued
-      // V^T of a block is issued after the K of the next one: a V^T stage frees
-      // later (after P V) than a K stage (after Q K^T), and waiting for it must
-      // not hold back the keys the tensor cores need first
-      int pend_g = -1, pend_j = 0;
-      auto load_v = [&]() -> bool {
-        const int s = n_v % kAttnStages;
-        if (n_v >= kAttnStages &&
-            !wait_sleep(v_empty(s), (uint32_t)((n_v / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns))
-          return false;
-        mbar_arrive_expect_tx(v_full(s), kAttnTile);
-        tma_load_2d(smem_addr(sV + (size_t)s * kAttnTile), &tm_vt, v_full(s), pend_j * kAttnBN, pend_g * kAttnDh);
-        tma_load_2d(smem_addr(sV + (size_t)s * kAttnTile + kAttnHalf), &tm_vt, v_full(s), pend_j * kAttnBN + 64,
-                    pend_g * kAttnDh);
-        ++n_v;
-        pend_g = -1;
-        return true;
-      };
+      int gb = 0, n_q = 0;  // blocks issued (across items), Q tiles issued
       for (int k = 0; ok; ++k) {
         const int i = attn_item_of((int)blockIdx.x, k, G);
         if (i >= n_items) break;
         const int qt = item_qt(i), h = item_h(i), g = h / p.group;
-        if (pend_g >= 0 && !load_v()) {  // the previous item's last V^T
-          ok = false;
-          break;
-        }
         // the previous item's Q K^T products are done with the Q buffer
         if (k > 0 && !wait_sleep(q_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns)) {
           ok = false;
@@ -264,63 +232,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
         tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
         n_q = k + 1;
-        for (int j = 0; j <= qt; ++j) {
-          const int s = n_k % kAttnStages;
-          if (n_k >= kAttnStages &&
-              !wait_sleep(k_empty(s), (uint32_t)((n_k / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
+        for (int j = 0; j <= qt; ++j, ++gb) {
+          const int s = gb % kAttnStages;
+          if (gb >= kAttnStages &&
+              !wait_sleep(kv_empty(s), (uint32_t)((gb / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(k_full(s), kAttnTile);
+          const uint32_t fb = kv_full(s);
+          mbar_arrive_expect_tx(fb, 2 * kAttnTile);
+          uint8_t* sk = sKV + (size_t)(2 * s) * kAttnTile;
+          uint8_t* sv = sk + kAttnTile;
           const int krow = g * p.t_stride + j * kAttnBN;
-          tma_load_2d(smem_addr(sK + (size_t)s * kAttnTile), &tm_k, k_full(s), 0, krow);
-          tma_load_2d(smem_addr(sK + (size_t)s * kAttnTile + kAttnHalf), &tm_k, k_full(s), 64, krow);
-          ++n_k;
-          if (pend_g >= 0 && !load_v()) {
-            ok = false;
-            break;
-          }
-          pend_g = g;
-          pend_j = j;
+          tma_load_2d(smem_addr(sk), &tm_k, fb, 0, krow);
+          tma_load_2d(smem_addr(sk + kAttnHalf), &tm_k, fb, 64, krow);
+          tma_load_2d(smem_addr(sv), &tm_vt, fb, j * kAttnBN, g * kAttnDh);
+          tma_load_2d(smem_addr(sv + kAttnHalf), &tm_vt, fb, j * kAttnBN + 64, g * kAttnDh);
         }
       }
-      if (ok && pend_g >= 0) ok = load_v();
       // every release of a stage by the MMA issuer has landed before exit
-      for (int b = (n_k > kAttnStages ? n_k - kAttnStages : 0); b < n_k && ok; ++b)
-        if (!wait_sleep(k_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
-          ok = false;
-      for (int b = (n_v > kAttnStages ? n_v - kAttnStages : 0); b < n_v && ok; ++b)
-        if (!wait_sleep(v_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
+      for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb && ok; ++b)
+        if (!wait_sleep(kv_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
           ok = false;
       if (!ok) {
         raise_abort(abort_flag, p.err);
         // this role's copies still in flight land before the CTA exits
         if (n_q > 0) wait_sleep(q_full, (uint32_t)(n_q - 1) & 1u, nullptr, p.timeout_ns);
-        for (int b = (n_k > kAttnStages ? n_k - kAttnStages : 0); b < n_k; ++b)
-          wait_sleep(k_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
-        for (int b = (n_v > kAttnStages ? n_v - kAttnStages : 0); b < n_v; ++b)
-          wait_sleep(v_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
+        for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb; ++b)
+          wait_sleep(kv_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t tO = tmem_base, tS = tmem_base + kAttnColS;
+      const uint32_t tO = tmem_base, tS = tmem_base + kAttnColS, tP = tmem_base + kAttnColP;
       const uint32_t qa = smem_addr(sQ);
       bool ok = true;
       int gb = 0;  // first block of the current item (across items)
       auto issue_s = [&](int b) -> bool {
         const int s = b % kAttnStages;
-        if (!wait_sleep(k_full(s), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
+        if (!wait_sleep(kv_full(s), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
         tc_fence_after_sync();
-        const uint32_t kb = smem_addr(sK + (size_t)s * kAttnTile);
-        const uint32_t d = tS + (uint32_t)(b % kAttnSBufs) * kAttnBN;
+        const uint32_t kb = smem_addr(sKV + (size_t)(2 * s) * kAttnTile);
 #pragma unroll
         for (int kk = 0; kk < kAttnDh / 16; ++kk)  // K = 16 along the head dimension
-          umma_bf16(d, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
+          umma_bf16(tS + (uint32_t)(b & 1) * kAttnBN, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
                     smem_desc_k_sw128(kb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdescF16, kk != 0);
-        umma_commit(s_full(b % kAttnSBufs));
-        umma_commit(k_empty(s));  // the K stage is free once this product is done
+        umma_commit(s_full(b & 1));
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -331,35 +289,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ok = false;
           break;
         }
-        // the first three products of the item; their buffers were last read by
-        // P V products of the previous item, all issued before
-        const int ahead = nblk < kAttnSBufs ? nblk : kAttnSBufs;
-        for (int j = 0; j < ahead && ok; ++j) ok = issue_s(gb + j);
-        if (ok && nblk <= kAttnSBufs) umma_commit(q_empty);  // the item's last Q K^T product is issued
+        ok = issue_s(gb);
+        if (ok && nblk == 1) umma_commit(q_empty);
         for (int j = 0; j < nblk && ok; ++j) {
           const int b = gb + j;
-          if (!wait_sleep(p_full(b % kAttnSBufs), (uint32_t)(b / kAttnSBufs) & 1u, abort_flag, p.timeout_ns) ||
-              !wait_sleep(v_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns) ||
+          // S_{j+1} runs on the tensor cores while the softmax warps work on S_j
+          if (j + 1 < nblk) {
+            if (!issue_s(b + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 == nblk) umma_commit(q_empty);  // the item's last Q K^T product is issued
+          }
+          if (!wait_sleep(p_full(b & 1), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns) ||
               (j == 0 && k > 0 && !wait_sleep(o_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t vb = smem_addr(sV + (size_t)(b % kAttnStages) * kAttnTile);
-          const uint32_t pa = tS + (uint32_t)(b % kAttnSBufs) * kAttnBN;  // P_b over the first 64 columns of S_b
+          const uint32_t vb = smem_addr(sKV + (size_t)(2 * (b % kAttnStages) + 1) * kAttnTile);
 #pragma unroll
           for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
-            umma_bf16_tmem_a(tO, pa + 8 * kk, smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
-                             kAttnIdesc, (j | kk) != 0);
-          umma_commit(v_empty(b % kAttnStages));
-          // S_{j+3} into the buffer P V_j just read (in issue order on the tensor core)
-          if (j + kAttnSBufs < nblk) {
-            if (!issue_s(b + kAttnSBufs)) {
-              ok = false;
-              break;
-            }
-            if (j + kAttnSBufs + 1 == nblk) umma_commit(q_empty);  // the item's last Q K^T product is issued
-          }
+            umma_bf16_tmem_a(tO, tP + (uint32_t)(b & 1) * (kAttnBN / 2) + 8 * kk,
+                             smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc,
+                             (j | kk) != 0);
+          umma_commit(kv_empty(b % kAttnStages));
+          umma_commit(p_free(b & 1));
         }
         if (!ok) break;
         umma_commit(o_full);
@@ -373,7 +328,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int q4 = warp & 3;                 // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
-    const int grp = (warp - 2) >> 2;         // global blocks gb with gb % 2 == grp
+    const int grp = (warp - 2) >> 2;         // global blocks gb with gb % 2 == grp; S and P buffers grp
     const int half = grp;                    // epilogue: O columns [64 half, 64 half + 64)
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -388,9 +343,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint64_t l2 = f32x2(0.f, 0.f);
       for (int j = (grp - gb0) & 1; j < nblk && ok; j += 2) {
         const int b = gb0 + j;
-        // S_b is in buffer b % 3; the MMA wrote it after the P V product that
-        // read the buffer's previous P, so the buffer is free to overwrite
-        const bool got = wait_sleep(s_full(b % kAttnSBufs), (uint32_t)(b / kAttnSBufs) & 1u, abort_flag, p.timeout_ns);
+        bool got = wait_sleep(s_full(grp), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns);
+        // P_grp was last read by the MMA of global block b - 2
+        if (got && b >= 2) got = wait_sleep(p_free(grp), (uint32_t)((b >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           if (lane == 0) raise_abort(abort_flag, p.err);
@@ -401,8 +356,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t s0[32], s1[32];
-          const uint32_t sb = tmem_base + lane_off + kAttnColS + (uint32_t)(b % kAttnSBufs) * kAttnBN;
-          const uint32_t ts = sb + hh * 64;
+          const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)grp * kAttnBN + hh * 64;
           tmem_ld_32x32b_x32(ts, s0);
           tmem_ld_32x32b_x32(ts + 32, s1);
           tmem_ld_wait();
@@ -424,12 +378,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l2 = add_f32x2(l2, f32x2(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
           }
-          // P columns [32 hh, 32 hh + 32) of the buffer: S columns already read
-          tmem_st_32x32b_x32(sb + hh * 32, pk);
+          tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)grp * (kAttnBN / 2) + hh * 32, pk);
         }
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(p_full(b % kAttnSBufs));
+        mbar_arrive(p_full(grp));
       }
       bool got = ok && __all_sync(0xffffffffu, wait_sleep(o_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns));
       float la, lb;
