@@ -9,7 +9,8 @@ seed 1002; expert weights 9.66 GB, larger than L2, so no flush is needed).
 A step is one moe_layer_forward over the whole batch: router, grouping, both
 expert GEMMs, combine, post-norm and residual.
 
-One JSON line on rank 0 (the keys are described in the design doc).  With N > 1
+One JSON line on rank 0: the base keys plus roofline (dominant kernel), cpu_baseline,
+e2e (host buffers), clocks and gpu_launches.  With N > 1
 (torchrun) every rank runs its own replica of the workload on its own GPU: the
 layer is token-parallel with no exchange, so scaling is weak and value = N * T
 / max-over-ranks step time.

@@ -36,7 +36,7 @@
  *    broadcasting, scale shapes (1,N), (8,N), (8,1,N), (8,8,N), transposed from
  *    JAX [in, out] to PyTorch [out, in].
  *
- * Readings where the sources are silent (each also listed in the design notes):
+ * Readings where the sources are silent:
  *  - GELU is the tanh approximation 0.5 u (1 + tanh(sqrt(2/pi)(u + 0.044715 u^3))).
  *  - RMSNorm(v) = v / sqrt(mean(v^2) + eps) * scale, scale applied as is.
  *  - The router sees the unrounded pre-norm output; ties in top-2 go to the
