@@ -271,6 +271,19 @@ moe_status_t moe_layer_workspace(const moe_layer_t* layer, moe_workspace_view_t*
 moe_status_t moe_group_slots_noalloc(const int32_t* topk_idx, const float* topk_prob, int32_t T,
                                      int32_t* expert_counts, int32_t* row_of_slot, void* stream);
 
+/* Self-test of the bounded waits every kernel of this library uses (no device
+ * memory of any layer is touched): one thread of one block waits on an
+ * mbarrier phase that nothing completes.  mode 0: the spinning wait (GEMM,
+ * decode and grouping kernels); mode 1: the sleeping wait (attention kernel);
+ * mode 2: the spinning wait with the abort flag already raised, which must
+ * return at once whatever limit_ns is.  limit_ns in [1 ms, 2 s].  Synchronous
+ * (synchronises the current device).  Returns MOE_ERR_TIMEOUT when the wait gave
+ * up and latched the error word, as it should, with the time it waited in
+ * *elapsed_ns (HOST, may be NULL); MOE_ERR_DEVICE_CHECK if the wait returned
+ * true or did not latch the error; MOE_ERR_CUDA on a CUDA error.  The GPU
+ * context stays usable afterwards. */
+moe_status_t moe_selftest_bounded_wait(int32_t mode, uint64_t limit_ns, uint64_t* elapsed_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -105,6 +105,8 @@ def lib():
         L.moe_layer_workspace.argtypes = [vp, ctypes.POINTER(WorkspaceView)]
         L.moe_group_slots_noalloc.restype = i32
         L.moe_group_slots_noalloc.argtypes = [vp, vp, i32, vp, vp, vp]
+        L.moe_selftest_bounded_wait.restype = i32
+        L.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)]
         L.attn_block_create.restype = i32
         L.attn_block_create.argtypes = [ctypes.POINTER(AttnConfig), ctypes.POINTER(AttnWeights), ctypes.POINTER(vp)]
         L.attn_block_forward.restype = i32
@@ -140,6 +142,14 @@ def declared_functions():
     text = open(HEADER_PATH).read() + open(ATTN_HEADER_PATH).read()
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?((?:moe|attn)_[a-z_0-9]+)\s*\(", text,
                                  re.M)))
+
+
+def selftest_bounded_wait(mode: int, limit_s: float) -> tuple:
+    """moe_selftest_bounded_wait: (status, waited seconds).  The expected status is
+    MOE_ERR_TIMEOUT (the wait gave up and latched the error word)."""
+    el = ctypes.c_uint64(0)
+    st = lib().moe_selftest_bounded_wait(int(mode), int(limit_s * 1e9), ctypes.byref(el))
+    return st, el.value / 1e9
 
 
 def _ptr(t) -> Optional[int]:

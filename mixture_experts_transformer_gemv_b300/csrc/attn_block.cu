@@ -28,6 +28,7 @@
 #include "host_util.h"
 #include "k_attn.cuh"
 #include "k_gemm.cuh"
+#include "k_selftest.cuh"
 
 using namespace moe;
 using namespace moe_host;
@@ -327,6 +328,32 @@ moe_status_t attn_block_sync_status(attn_block_t* B, void* stream) {
 }
 
 int32_t attn_block_launch_count(const attn_block_t* B) { return B ? kAttnLaunches : 0; }
+
+moe_status_t moe_selftest_bounded_wait(int32_t mode, uint64_t limit_ns, uint64_t* elapsed_ns) {
+  if (mode < 0 || mode > 2) return fail(MOE_ERR_INVALID_ARG, "mode must be 0, 1 or 2 (got %d)", mode);
+  if (limit_ns < 1000000ull || limit_ns > 2000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns outside [1 ms, 2 s]");
+  void* buf = nullptr;
+  MOE_CUDA_TRY(cudaMalloc(&buf, 64));
+  uint32_t* err = static_cast<uint32_t*>(buf);
+  uint64_t* res = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(buf) + 16);
+  uint64_t h[2] = {0, 0};
+  uint32_t e = 0;
+  cudaError_t ce = cudaMemset(buf, 0, 64);
+  if (ce == cudaSuccess) {
+    selftest_wait_kernel<<<1, 32>>>(mode, limit_ns, err, res);
+    ce = cudaGetLastError();
+  }
+  if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
+  if (ce == cudaSuccess) ce = cudaMemcpy(h, res, sizeof(h), cudaMemcpyDeviceToHost);
+  if (ce == cudaSuccess) ce = cudaMemcpy(&e, err, sizeof(e), cudaMemcpyDeviceToHost);
+  cudaFree(buf);
+  if (ce != cudaSuccess) return fail(MOE_ERR_CUDA, "self-test: %s", cudaGetErrorString(ce));
+  if (elapsed_ns) *elapsed_ns = h[1];
+  if (h[0] != 0) return fail(MOE_ERR_DEVICE_CHECK, "a wait on a phase nobody completes returned true");
+  if (e & kErrTimeout) return fail(MOE_ERR_TIMEOUT, "the wait gave up after %llu ns", (unsigned long long)h[1]);
+  return fail(MOE_ERR_DEVICE_CHECK, "the wait gave up but did not latch the error word");
+}
 
 moe_status_t attn_block_set_profiling(attn_block_t* B, int32_t enable) {
   if (!B) return fail(MOE_ERR_INVALID_ARG, "null block");

@@ -164,3 +164,10 @@ def test_attn_null_arguments(lib):
     assert lib.attn_block_sync_status(None, None) == 1
     assert lib.attn_block_destroy(None) == 0
     assert lib.attn_block_launch_count(None) == 0
+
+
+def test_selftest_rejects_bad_arguments(lib):
+    el = ctypes.c_uint64(0)
+    assert lib.moe_selftest_bounded_wait(3, 10_000_000, ctypes.byref(el)) == 1
+    assert lib.moe_selftest_bounded_wait(0, 10, ctypes.byref(el)) == 1            # below 1 ms
+    assert lib.moe_selftest_bounded_wait(1, 3_000_000_000, ctypes.byref(el)) == 1  # above 2 s
