@@ -43,7 +43,7 @@ struct attn_block {
   const float* s_post = nullptr;
   void* wqkv = nullptr;  // owned [(Hq + 2 Hkv) 128, d] fp16
   int64_t rows_cap = 0;  // rows of the GEMM buffers: max_tokens rounded up to 256
-  int64_t t_stride = 0;  // token rows per head of Q / K: max_tokens rounded up to 128
+  int64_t t_stride = 0;  // token rows per head of Q / K: max_tokens rounded up to 256
   int n_qkv = 0;         // (Hq + 2 Hkv) 128
   int n_ctx = 0;         // Hq 128
   void* ws = nullptr;
@@ -101,7 +101,7 @@ moe_status_t enqueue(attn_block* B, const void* x, void* y, int T, cudaStream_t 
   };
   const int d = B->cfg.d_model, Hq = B->cfg.n_q_heads, Hkv = B->cfg.n_kv_heads;
   const int rows_pad = (int)align_up((size_t)T, kRowTile);
-  const int t_pad = (int)align_up((size_t)T, kAttnBM);
+  const int t_pad = (int)align_up((size_t)T, 2 * kAttnBM);  // whole pairs of query tiles
   mark(ATTN_K_PRENORM);
   attn_prenorm_kernel<<<rows_pad, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), B->s_pre, B->cfg.eps, T,
                                                 rows_pad, d, B->xn, B->sched);
@@ -134,7 +134,7 @@ moe_status_t enqueue(attn_block* B, const void* x, void* y, int T, cudaStream_t 
     p.t_stride = (int)B->t_stride;
     p.n_q_heads = Hq;
     p.group = Hq / Hkv;
-    p.n_qtiles = t_pad / kAttnBM;
+    p.n_qpairs = t_pad / (2 * kAttnBM);
     const double log2e = 1.4426950408889634;
     p.sat_scale = (float)(1.0 / (2.0 * (double)B->cfg.logit_clamp * std::sqrt((double)kAttnDh)));
     p.clamp2_log2 = (float)(2.0 * (double)B->cfg.logit_clamp * log2e);
@@ -142,8 +142,8 @@ moe_status_t enqueue(attn_block* B, const void* x, void* y, int T, cudaStream_t 
     p.ctx_ld = B->n_ctx;
     p.err = B->err;
     p.timeout_ns = kWaitLimitNs;
-    // persistent: one CTA per SM, each looping over query tiles
-    const int grid = std::min(B->num_sms, p.n_qtiles * Hq);
+    // persistent: one CTA per SM, each looping over pairs of query tiles
+    const int grid = std::min(B->num_sms, p.n_qpairs * Hq);
     attn_kernel<<<grid, kAttnThreads, kAttnSmemBytes, st>>>(B->tm_q, B->tm_k, B->tm_vt, p);
   }
   mark(ATTN_K_OPROJ);
@@ -223,7 +223,7 @@ moe_status_t attn_block_create(const attn_config_t* cfg, const attn_weights_t* w
   B->n_qkv = (Hq + 2 * Hkv) * kAttnDh;
   B->n_ctx = Hq * kAttnDh;
   B->rows_cap = (int64_t)align_up((size_t)c.max_tokens, kRowTile);
-  B->t_stride = (int64_t)align_up((size_t)c.max_tokens, kAttnBM);
+  B->t_stride = (int64_t)align_up((size_t)c.max_tokens, 2 * kAttnBM);
   const size_t R = (size_t)B->rows_cap, TS = (size_t)B->t_stride;
   const size_t sz_wqkv = (size_t)B->n_qkv * d * 2;
   const size_t sz_xn = align_up(R * d * 2, 256), sz_qkv = align_up(R * B->n_qkv * 4, 256);

@@ -38,22 +38,23 @@
 namespace moe {
 
 constexpr int kAttnDh = 128;                         // head dimension
-constexpr int kAttnBM = 128;                         // queries of one CTA (TMEM lanes)
+constexpr int kAttnBM = 128;                         // queries of one tile (TMEM lanes)
 constexpr int kAttnBN = 128;                         // keys of one block
-constexpr int kAttnStages = 3;                       // K/V blocks in flight
-constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 bf16, two 64-column boxes
-constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 bf16, 128-byte swizzle
-constexpr int kAttnSoftmaxWarps = 8;                 // two groups of four: even and odd key blocks
+constexpr int kAttnKStages = 3;                      // K ring stages
+constexpr int kAttnVStages = 2;                      // V^T ring stages
+constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 16-bit values, two 64-column boxes
+constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 values, 128-byte swizzle
+constexpr int kAttnSoftmaxWarps = 8;                 // four per query tile
 constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
 constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
-// q_full, q_empty, kv_full[3], kv_empty[3], s_full[2], p_full[2], p_free[2], o_full, o_empty, drain
-constexpr int kAttnNumBars = 2 + 2 * kAttnStages + 6 + 3;
+// q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], o_full, o_empty, drain
+constexpr int kAttnNumBars = 2 + 2 * kAttnKStages + 2 * kAttnVStages + 4 + 3;
 constexpr size_t kAttnBarBytes = 256;                // barriers, TMEM address, abort flag
 constexpr size_t kAttnSmemBytes =
-    1024 + (size_t)kAttnTile * (1 + 2 * kAttnStages) + kAttnBarBytes + 2 * kAttnBM * sizeof(float);
+    1024 + (size_t)kAttnTile * (2 + kAttnKStages + kAttnVStages) + kAttnBarBytes;
 static_assert(8 * kAttnNumBars + 8 <= kAttnBarBytes, "barrier block");
-constexpr uint32_t kAttnTmemCols = 512;              // O | S0 | S1 | P0 | P1
-constexpr uint32_t kAttnColS = 128, kAttnColP = 384;
+constexpr uint32_t kAttnTmemCols = 512;              // O_A | O_B | S_A | S_B (P_t over the first 64 columns of S_t)
+constexpr uint32_t kAttnColO = 0, kAttnColS = 256;
 constexpr uint32_t kAttnIdesc = idesc_bf16_f32(kAttnBM, kAttnBN);  // P V: bf16 x bf16
 // Q K^T: fp16 x fp16 (format 0 in bits 7-9 and 10-12), fp32 accumulator
 constexpr uint32_t kAttnIdescF16 = (1u << 4) | (static_cast<uint32_t>(kAttnBN >> 3) << 17) |
@@ -63,10 +64,10 @@ static_assert(kAttnSmemBytes <= 232448, "fits one CTA per SM");
 
 struct AttnParams {
   int T;               // sequence length
-  int t_stride;        // rows per head of Q and K, columns of Vt (multiple of 128)
+  int t_stride;        // rows per head of Q and K, columns of Vt (multiple of 256)
   int n_q_heads;       // query heads
   int group;           // query heads per key/value head
-  int n_qtiles;        // ceil(T / 128)
+  int n_qpairs;        // ceil(T / 256): pairs of query tiles
   float sat_scale;     // log2(e) / (sqrt(128) 2 c log2(e)) = 1 / (2 c sqrt(128))
   float clamp2_log2;   // 2 c log2(e)
   __nv_bfloat16* ctx;  // [rows, n_q_heads * 128]
@@ -132,23 +133,29 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
-// Work item i (heaviest first): query tile qt = n_qtiles - 1 - i / Hq of head
-// h = i % Hq, i.e. 128 queries against the key blocks 0..qt.  The kernel is
-// persistent: CTA c takes items c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (G CTAs,
-// alternating direction so the long and short items even out).
+// Work item i (heaviest first): the query tiles qa = 2 (n_qpairs - 1 - i / Hq)
+// and qb = qa + 1 of head h = i % Hq, i.e. 256 queries against the key blocks
+// 0..qb.  The kernel is persistent: CTA c takes items c, 2G - 1 - c, 2G + c,
+// 4G - 1 - c, ... (G CTAs, alternating direction so long and short items even out).
 __device__ __forceinline__ int attn_item_of(int c, int k, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-// Per CTA, one item after another: warp 0 streams Q (one buffer, reloaded as
-// soon as the item's last Q K^T product is done) and K / V^T blocks through a
-// 3-stage ring (TMA); warp 1 issues S = Q K^T into a double-buffered TMEM S and
-// O += P V with P read from TMEM; warps 2-9 turn S into P (warps 2-5 the even
-// blocks, 6-9 the odd ones, counted across items; one query row per thread: the
-// two groups work on two blocks at once and the two warps that share a
-// scheduler are out of phase) and at the end of an item write ctx = O / l.
-// Block counters run across items, so ring stages, buffers and barrier phases
-// continue from one item to the next.
+// Per CTA, one item after another, two query tiles A and B sharing every K and
+// V^T block (half the key traffic per flop of one tile per CTA):
+//  - warp 0 (TMA): Q_A and Q_B (reloaded as soon as the item's last Q K^T
+//    product is done), K blocks through a 3-stage ring and V^T blocks through a
+//    2-stage ring, each V^T issued after the next block's K so a wait for a V^T
+//    stage never holds back keys;
+//  - warp 1 (MMA): S_A(0), S_B(0), then per block j: P V_A(j), S_A(j+1),
+//    P V_B(j), S_B(j+1).  The tensor cores work on one tile while the softmax
+//    of the other runs.  P_t (bf16) is written over the first 64 columns of S_t
+//    and read from TMEM as the A operand of P V_t; the tensor core runs one
+//    CTA's MMAs in issue order, so S_t(j+1), issued after P V_t(j), overwrites
+//    P_t(j) only after it was read;
+//  - warps 2-5 (tile A) and 6-9 (tile B): one query row per thread turns S_t(j)
+//    into P_t(j) and at the end of the item writes ctx = O_t / l.
+// Ring, buffer and phase counters run across items.
 //
 // Softmax weight of a logit s (c' = c log2(e)):
 //   2^(clamp(s log2(e) / sqrt(128), -c', c') - c') = 2^(2c' (u - 1)),
@@ -159,39 +166,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                // [128 x 128] fp16
-  uint8_t* sKV = smem + kAttnTile;   // stage s: K (fp16) at 2s tiles, V^T (bf16) at 2s + 1 tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (1 + 2 * kAttnStages));
+  uint8_t* sQ = smem;                                   // Q_A, Q_B (fp16)
+  uint8_t* sK = smem + 2 * (size_t)kAttnTile;           // K ring (fp16)
+  uint8_t* sV = sK + (size_t)kAttnKStages * kAttnTile;  // V^T ring (bf16)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (2 + kAttnKStages + kAttnVStages));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  float* l_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kAttnBarBytes);  // [2][128]
   const uint32_t b0 = smem_addr(bars);
   const uint32_t q_full = b0, q_empty = b0 + 8u;
-  auto kv_full = [&](int s) { return b0 + 8u * (2 + s); };
-  auto kv_empty = [&](int s) { return b0 + 8u * (2 + kAttnStages + s); };
-  auto s_full = [&](int b) { return b0 + 8u * (2 + 2 * kAttnStages + b); };
-  auto p_full = [&](int b) { return b0 + 8u * (4 + 2 * kAttnStages + b); };
-  auto p_free = [&](int b) { return b0 + 8u * (6 + 2 * kAttnStages + b); };
-  const uint32_t o_full = b0 + 8u * (8 + 2 * kAttnStages);
+  auto k_full = [&](int s) { return b0 + 8u * (2 + s); };
+  auto k_empty = [&](int s) { return b0 + 8u * (2 + kAttnKStages + s); };
+  auto v_full = [&](int s) { return b0 + 8u * (2 + 2 * kAttnKStages + s); };
+  auto v_empty = [&](int s) { return b0 + 8u * (2 + 2 * kAttnKStages + kAttnVStages + s); };
+  auto s_full = [&](int t) { return b0 + 8u * (2 + 2 * kAttnKStages + 2 * kAttnVStages + t); };
+  auto p_full = [&](int t) { return b0 + 8u * (4 + 2 * kAttnKStages + 2 * kAttnVStages + t); };
+  const uint32_t o_full = b0 + 8u * (6 + 2 * kAttnKStages + 2 * kAttnVStages);
   const uint32_t o_empty = o_full + 8u;
   const uint32_t drain = o_full + 16u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = (int)gridDim.x, n_items = p.n_qtiles * p.n_q_heads;
-  auto item_qt = [&](int i) { return p.n_qtiles - 1 - i / p.n_q_heads; };
+  const int G = (int)gridDim.x, n_items = p.n_qpairs * p.n_q_heads;
+  auto item_qa = [&](int i) { return 2 * (p.n_qpairs - 1 - i / p.n_q_heads); };
   auto item_h = [&](int i) { return i % p.n_q_heads; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < kAttnKStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), kAttnSoftmaxThreads / 2);  // every thread of the group that owns buffer b
-      mbar_init(p_free(b), 1);
+    for (int s = 0; s < kAttnVStages; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), kAttnSoftmaxThreads / 2);  // every thread of the tile's group
     }
     mbar_init(o_full, 1);
     mbar_init(o_empty, kAttnSoftmaxWarps);  // one arrival per softmax warp
@@ -217,108 +228,169 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       bool ok = true;
-      int gb = 0, n_q = 0;  // blocks issued (across items), Q tiles issued
-      for (int k = 0; ok; ++k) {
-        const int i = attn_item_of((int)blockIdx.x, k, G);
-        if (i >= n_items) break;
-        const int qt = item_qt(i), h = item_h(i), g = h / p.group;
-        // the previous item's Q K^T products are done with the Q buffer
-        if (k > 0 && !wait_sleep(q_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(q_full, kAttnTile);
-        const int qrow0 = h * p.t_stride + qt * kAttnBM;
-        tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
-        tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
-        n_q = k + 1;
-        for (int j = 0; j <= qt; ++j, ++gb) {
-          const int s = gb % kAttnStages;
-          if (gb >= kAttnStages &&
-              !wait_sleep(kv_empty(s), (uint32_t)((gb / kAttnStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = kv_full(s);
-          mbar_arrive_expect_tx(fb, 2 * kAttnTile);
-          uint8_t* sk = sKV + (size_t)(2 * s) * kAttnTile;
-          uint8_t* sv = sk + kAttnTile;
-          const int krow = g * p.t_stride + j * kAttnBN;
-          tma_load_2d(smem_addr(sk), &tm_k, fb, 0, krow);
-          tma_load_2d(smem_addr(sk + kAttnHalf), &tm_k, fb, 64, krow);
-          tma_load_2d(smem_addr(sv), &tm_vt, fb, j * kAttnBN, g * kAttnDh);
-          tma_load_2d(smem_addr(sv + kAttnHalf), &tm_vt, fb, j * kAttnBN + 64, g * kAttnDh);
-        }
-      }
-      // every release of a stage by the MMA issuer has landed before exit
-      for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb && ok; ++b)
-        if (!wait_sleep(kv_empty(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns))
-          ok = false;
-      if (!ok) {
-        raise_abort(abort_flag, p.err);
-        // this role's copies still in flight land before the CTA exits
-        if (n_q > 0) wait_sleep(q_full, (uint32_t)(n_q - 1) & 1u, nullptr, p.timeout_ns);
-        for (int b = (gb > kAttnStages ? gb - kAttnStages : 0); b < gb; ++b)
-          wait_sleep(kv_full(b % kAttnStages), (uint32_t)(b / kAttnStages) & 1u, nullptr, p.timeout_ns);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t tO = tmem_base, tS = tmem_base + kAttnColS, tP = tmem_base + kAttnColP;
-      const uint32_t qa = smem_addr(sQ);
-      bool ok = true;
-      int gb = 0;  // first block of the current item (across items)
-      auto issue_s = [&](int b) -> bool {
-        const int s = b % kAttnStages;
-        if (!wait_sleep(kv_full(s), (uint32_t)(b / kAttnStages) & 1u, abort_flag, p.timeout_ns)) return false;
-        tc_fence_after_sync();
-        const uint32_t kb = smem_addr(sKV + (size_t)(2 * s) * kAttnTile);
-#pragma unroll
-        for (int kk = 0; kk < kAttnDh / 16; ++kk)  // K = 16 along the head dimension
-          umma_bf16(tS + (uint32_t)(b & 1) * kAttnBN, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
-                    smem_desc_k_sw128(kb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdescF16, kk != 0);
-        umma_commit(s_full(b & 1));
+      int n_k = 0, n_v = 0, n_q = 0;  // K and V^T blocks issued (across items), Q pairs issued
+      int pend_g = -1, pend_j = 0;    // the V^T block issued after the next K
+      auto load_v = [&]() -> bool {
+        const int s = n_v % kAttnVStages;
+        if (n_v >= kAttnVStages &&
+            !wait_sleep(v_empty(s), (uint32_t)((n_v / kAttnVStages) - 1) & 1u, abort_flag, p.timeout_ns))
+          return false;
+        mbar_arrive_expect_tx(v_full(s), kAttnTile);
+        uint8_t* dst = sV + (size_t)s * kAttnTile;
+        tma_load_2d(smem_addr(dst), &tm_vt, v_full(s), pend_j * kAttnBN, pend_g * kAttnDh);
+        tma_load_2d(smem_addr(dst + kAttnHalf), &tm_vt, v_full(s), pend_j * kAttnBN + 64, pend_g * kAttnDh);
+        ++n_v;
+        pend_g = -1;
         return true;
       };
       for (int k = 0; ok; ++k) {
         const int i = attn_item_of((int)blockIdx.x, k, G);
         if (i >= n_items) break;
-        const int nblk = item_qt(i) + 1;
-        if (!wait_sleep(q_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns)) {
+        const int qa = item_qa(i), h = item_h(i), g = h / p.group;
+        if (pend_g >= 0 && !load_v()) {  // the previous item's last V^T
           ok = false;
           break;
         }
-        ok = issue_s(gb);
-        if (ok && nblk == 1) umma_commit(q_empty);
-        for (int j = 0; j < nblk && ok; ++j) {
+        // the previous item's Q K^T products are done with the Q buffers
+        if (k > 0 && !wait_sleep(q_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(q_full, 2 * kAttnTile);
+        const int qrow0 = h * p.t_stride + qa * kAttnBM;
+        tma_load_2d(smem_addr(sQ), &tm_q, q_full, 0, qrow0);
+        tma_load_2d(smem_addr(sQ + kAttnHalf), &tm_q, q_full, 64, qrow0);
+        tma_load_2d(smem_addr(sQ + kAttnTile), &tm_q, q_full, 0, qrow0 + kAttnBM);
+        tma_load_2d(smem_addr(sQ + kAttnTile + kAttnHalf), &tm_q, q_full, 64, qrow0 + kAttnBM);
+        n_q = k + 1;
+        for (int j = 0; j <= qa + 1; ++j) {
+          const int s = n_k % kAttnKStages;
+          if (n_k >= kAttnKStages &&
+              !wait_sleep(k_empty(s), (uint32_t)((n_k / kAttnKStages) - 1) & 1u, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full(s), kAttnTile);
+          const int krow = g * p.t_stride + j * kAttnBN;
+          tma_load_2d(smem_addr(sK + (size_t)s * kAttnTile), &tm_k, k_full(s), 0, krow);
+          tma_load_2d(smem_addr(sK + (size_t)s * kAttnTile + kAttnHalf), &tm_k, k_full(s), 64, krow);
+          ++n_k;
+          if (pend_g >= 0 && !load_v()) {
+            ok = false;
+            break;
+          }
+          pend_g = g;
+          pend_j = j;
+        }
+      }
+      if (ok && pend_g >= 0) ok = load_v();
+      // every release of a stage by the MMA issuer has landed before exit
+      for (int b = (n_k > kAttnKStages ? n_k - kAttnKStages : 0); b < n_k && ok; ++b)
+        if (!wait_sleep(k_empty(b % kAttnKStages), (uint32_t)(b / kAttnKStages) & 1u, abort_flag, p.timeout_ns))
+          ok = false;
+      for (int b = (n_v > kAttnVStages ? n_v - kAttnVStages : 0); b < n_v && ok; ++b)
+        if (!wait_sleep(v_empty(b % kAttnVStages), (uint32_t)(b / kAttnVStages) & 1u, abort_flag, p.timeout_ns))
+          ok = false;
+      if (!ok) {
+        raise_abort(abort_flag, p.err);
+        // this role's copies still in flight land before the CTA exits
+        if (n_q > 0) wait_sleep(q_full, (uint32_t)(n_q - 1) & 1u, nullptr, p.timeout_ns);
+        for (int b = (n_k > kAttnKStages ? n_k - kAttnKStages : 0); b < n_k; ++b)
+          wait_sleep(k_full(b % kAttnKStages), (uint32_t)(b / kAttnKStages) & 1u, nullptr, p.timeout_ns);
+        for (int b = (n_v > kAttnVStages ? n_v - kAttnVStages : 0); b < n_v; ++b)
+          wait_sleep(v_full(b % kAttnVStages), (uint32_t)(b / kAttnVStages) & 1u, nullptr, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      bool ok = true;
+      int gb = 0;           // first K/V block of the current item (across items)
+      int na_tot = 0;       // tile-A blocks before this item (phases of s_full(0), p_full(0))
+      int nb_tot = 0;       // tile-B blocks before this item (phases of s_full(1), p_full(1))
+      // S_t = Q_t K_b^T into tile t's S buffer
+      auto issue_s = [&](int t, int b) {
+        const uint32_t qa = smem_addr(sQ + (size_t)t * kAttnTile);
+        const uint32_t kb = smem_addr(sK + (size_t)(b % kAttnKStages) * kAttnTile);
+        const uint32_t d = tmem_base + kAttnColS + (uint32_t)t * kAttnBN;
+#pragma unroll
+        for (int kk = 0; kk < kAttnDh / 16; ++kk)  // K = 16 along the head dimension
+          umma_bf16(d, smem_desc_k_sw128(qa + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
+                    smem_desc_k_sw128(kb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdescF16, kk != 0);
+        umma_commit(s_full(t));
+      };
+      // O_t += P_t V_b
+      auto issue_pv = [&](int t, int b, bool acc) {
+        const uint32_t vb = smem_addr(sV + (size_t)(b % kAttnVStages) * kAttnTile);
+        const uint32_t pa = tmem_base + kAttnColS + (uint32_t)t * kAttnBN;  // P_t over the first 64 columns of S_t
+        const uint32_t d = tmem_base + kAttnColO + (uint32_t)t * kAttnBN;
+#pragma unroll
+        for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
+          umma_bf16_tmem_a(d, pa + 8 * kk, smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
+                           kAttnIdesc, (acc || kk != 0) ? 1u : 0u);
+      };
+      auto wait_k = [&](int b) {
+        const bool got = wait_sleep(k_full(b % kAttnKStages), (uint32_t)(b / kAttnKStages) & 1u, abort_flag,
+                                    p.timeout_ns);
+        tc_fence_after_sync();
+        return got;
+      };
+      for (int k = 0; ok; ++k) {
+        const int i = attn_item_of((int)blockIdx.x, k, G);
+        if (i >= n_items) break;
+        const int na = item_qa(i) + 1, nb = na + 1;  // key blocks of tile A (0..qa) and tile B (0..qa+1)
+        if (!wait_sleep(q_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns) || !wait_k(gb)) {
+          ok = false;
+          break;
+        }
+        issue_s(0, gb);
+        issue_s(1, gb);
+        umma_commit(k_empty(gb % kAttnKStages));
+        for (int j = 0; j < nb && ok; ++j) {
           const int b = gb + j;
-          // S_{j+1} runs on the tensor cores while the softmax warps work on S_j
-          if (j + 1 < nblk) {
-            if (!issue_s(b + 1)) {
+          // the V^T block of j (both tiles' P V read it)
+          if (!wait_sleep(v_full(b % kAttnVStages), (uint32_t)(b / kAttnVStages) & 1u, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          if (j < na) {
+            // tile A: P V_A(j), then S_A(j+1) over the buffer P V_A(j) just read
+            if (!wait_sleep(p_full(0), (uint32_t)(na_tot + j) & 1u, abort_flag, p.timeout_ns) ||
+                (j == 0 && k > 0 && !wait_sleep(o_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns))) {
               ok = false;
               break;
             }
-            if (j + 2 == nblk) umma_commit(q_empty);  // the item's last Q K^T product is issued
+            tc_fence_after_sync();
+            issue_pv(0, b, j > 0);
           }
-          if (!wait_sleep(p_full(b & 1), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns) ||
-              (j == 0 && k > 0 && !wait_sleep(o_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.timeout_ns))) {
+          const bool more = j + 1 < nb;
+          if (more) {
+            if (!wait_k(b + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 1 < na) issue_s(0, b + 1);
+          }
+          // tile B: P V_B(j), then S_B(j+1)
+          // (O_B is free too: every softmax warp arrived on o_empty, which P V_A(0) waited for)
+          if (!wait_sleep(p_full(1), (uint32_t)(nb_tot + j) & 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t vb = smem_addr(sKV + (size_t)(2 * (b % kAttnStages) + 1) * kAttnTile);
-#pragma unroll
-          for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
-            umma_bf16_tmem_a(tO, tP + (uint32_t)(b & 1) * (kAttnBN / 2) + 8 * kk,
-                             smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc,
-                             (j | kk) != 0);
-          umma_commit(kv_empty(b % kAttnStages));
-          umma_commit(p_free(b & 1));
+          issue_pv(1, b, j > 0);
+          umma_commit(v_empty(b % kAttnVStages));  // both tiles' products of block j are issued
+          if (more) {
+            issue_s(1, b + 1);
+            umma_commit(k_empty((b + 1) % kAttnKStages));
+            if (j + 2 == nb) umma_commit(q_empty);  // the item's last Q K^T product is issued
+          }
         }
         if (!ok) break;
         umma_commit(o_full);
-        gb += nblk;
+        gb += nb;
+        na_tot += na;
+        nb_tot += nb;
       }
       // all MMAs issued by this thread are complete before TMEM is freed
       umma_commit(drain);
@@ -327,26 +399,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
-    const int q4 = warp & 3;                 // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
-    const int grp = (warp - 2) >> 2;         // global blocks gb with gb % 2 == grp; S and P buffers grp
-    const int half = grp;                    // epilogue: O columns [64 half, 64 half + 64)
+    const int q4 = warp & 3;             // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
+    const int t = (warp - 2) >> 2;       // query tile: 0 = A, 1 = B
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t sb = tmem_base + lane_off + kAttnColS + (uint32_t)t * kAttnBN;  // S_t (and P_t)
+    const uint32_t ob = tmem_base + lane_off + kAttnColO + (uint32_t)t * kAttnBN;  // O_t
     const float ss = p.sat_scale;
     const uint64_t w2 = f32x2(p.clamp2_log2, p.clamp2_log2), mw2 = f32x2(-p.clamp2_log2, -p.clamp2_log2);
     bool ok = true;
-    int gb0 = 0;  // first global block of the current item
+    int n_tot = 0;  // this tile's blocks before the current item
     for (int k = 0;; ++k) {
       const int i = attn_item_of((int)blockIdx.x, k, G);
       if (i >= n_items) break;
-      const int qt = item_qt(i), h = item_h(i), nblk = qt + 1;
+      const int qt = item_qa(i) + t, h = item_h(i), nblk = qt + 1;
       uint64_t l2 = f32x2(0.f, 0.f);
-      for (int j = (grp - gb0) & 1; j < nblk && ok; j += 2) {
-        const int b = gb0 + j;
-        bool got = wait_sleep(s_full(grp), (uint32_t)(b >> 1) & 1u, abort_flag, p.timeout_ns);
-        // P_grp was last read by the MMA of global block b - 2
-        if (got && b >= 2) got = wait_sleep(p_free(grp), (uint32_t)((b >> 1) - 1) & 1u, abort_flag, p.timeout_ns);
-        if (!__all_sync(0xffffffffu, got)) {
+      for (int j = 0; j < nblk && ok; ++j) {
+        if (!__all_sync(0xffffffffu, wait_sleep(s_full(t), (uint32_t)(n_tot + j) & 1u, abort_flag, p.timeout_ns))) {
           ok = false;
           if (lane == 0) raise_abort(abort_flag, p.err);
           break;
@@ -356,9 +425,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t s0[32], s1[32];
-          const uint32_t ts = tmem_base + lane_off + kAttnColS + (uint32_t)grp * kAttnBN + hh * 64;
-          tmem_ld_32x32b_x32(ts, s0);
-          tmem_ld_32x32b_x32(ts + 32, s1);
+          tmem_ld_32x32b_x32(sb + hh * 64, s0);
+          tmem_ld_32x32b_x32(sb + hh * 64 + 32, s1);
           tmem_ld_wait();
           uint32_t pk[32];
 #pragma unroll
@@ -378,44 +446,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l2 = add_f32x2(l2, f32x2(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
           }
-          tmem_st_32x32b_x32(tmem_base + lane_off + kAttnColP + (uint32_t)grp * (kAttnBN / 2) + hh * 32, pk);
+          // P columns [32 hh, 32 hh + 32) of the buffer: S columns already read
+          tmem_st_32x32b_x32(sb + hh * 32, pk);
         }
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(p_full(grp));
+        mbar_arrive(p_full(t));
       }
-      bool got = ok && __all_sync(0xffffffffu, wait_sleep(o_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns));
-      float la, lb;
-      f32x2_split(l2, la, lb);
-      l_part[half * kAttnBM + r] = la + lb;
-      // every softmax thread reaches this barrier once per item; it also makes
-      // the two groups' row sums visible to each other
+      n_tot += nblk;
+      const bool got = ok && __all_sync(0xffffffffu, wait_sleep(o_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns));
+      // every softmax thread reaches this barrier once per item, so a thread that
+      // gave up takes all of them out together
       ok = named_bar_and(1, kAttnSoftmaxThreads, got);
       if (!ok) break;
       tc_fence_after_sync();
-      const float inv = 1.f / (l_part[r] + l_part[kAttnBM + r]);
+      float la, lb;
+      f32x2_split(l2, la, lb);
+      const float inv = 1.f / (la + lb);
       const int qrow = qt * kAttnBM + r;
-      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh + half * 64;
-      uint32_t o0[32], o1[32];
-      tmem_ld_32x32b_x32(tmem_base + lane_off + half * 64, o0);
-      tmem_ld_32x32b_x32(tmem_base + lane_off + half * 64 + 32, o1);
-      tmem_ld_wait();
-      // O and this thread's l_part reads are done: the next item may overwrite them
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_empty);
-      if (qrow < p.T) {
-        uint32_t pk[32];
+      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          pk[c] = pack_bf16x2(__uint_as_float(o0[2 * c]) * inv, __uint_as_float(o0[2 * c + 1]) * inv);
-          pk[16 + c] = pack_bf16x2(__uint_as_float(o1[2 * c]) * inv, __uint_as_float(o1[2 * c + 1]) * inv);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o0[32], o1[32];
+        tmem_ld_32x32b_x32(ob + hh * 64, o0);
+        tmem_ld_32x32b_x32(ob + hh * 64 + 32, o1);
+        tmem_ld_wait();
+        if (hh == 1) {
+          // this warp's reads of O are done: the next item's P V may overwrite it
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_empty);
         }
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        if (qrow < p.T) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int c = 0; c < 16; ++c) {
+            pk[c] = pack_bf16x2(__uint_as_float(o0[2 * c]) * inv, __uint_as_float(o0[2 * c + 1]) * inv);
+            pk[16 + c] = pack_bf16x2(__uint_as_float(o1[2 * c]) * inv, __uint_as_float(o1[2 * c + 1]) * inv);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + hh * 64);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
       }
-      gb0 += nblk;
     }
     if (!ok && lane == 0) raise_abort(abort_flag, p.err);
   }
@@ -508,7 +581,7 @@ __global__ void fill_f32_kernel(float* p, float v, int n) {
 // columns each) write Q [Hq][t_stride][128] and K [Hkv][t_stride][128] rotated
 // (pair (2i, 2i + 1) of each head turned by t * base^(-2i/128)) in fp16
 // (saturating) and Vt [Hkv][128][t_stride] (V transposed: keys along rows) in bf16; token rows
-// T <= t < gridDim.x * 32 are written as zeros.  Grid (ceil(T / 128) * 4,
+// T <= t < gridDim.x * 32 are written as zeros.  Grid (ceil(T / 256) * 8,
 // Hq + 2 Hkv), 256 threads: 32 tokens x one head per block.
 __global__ void __launch_bounds__(256) rope_layout_kernel(const float* __restrict__ qkv, int ld,
                                                           const float2* __restrict__ cs, int T, int t_stride, int Hq,
