@@ -44,16 +44,16 @@ constexpr int kAttnKStages = 3;                      // K ring stages
 constexpr int kAttnVStages = 2;                      // V^T ring stages
 constexpr int kAttnTile = kAttnBM * kAttnDh * 2;     // 32 KB: 128 rows x 128 16-bit values, two 64-column boxes
 constexpr int kAttnHalf = kAttnTile / 2;             // one box of 128 rows x 64 values, 128-byte swizzle
-constexpr int kAttnSoftmaxWarps = 8;                 // four per query tile
+constexpr int kAttnSoftmaxWarps = 16;                // eight per query tile: two per TMEM lane quarter, 64 keys each
 constexpr int kAttnSoftmaxThreads = 32 * kAttnSoftmaxWarps;
 constexpr int kAttnThreads = 64 + kAttnSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
 // q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], o_full, o_empty, drain
 constexpr int kAttnNumBars = 2 + 2 * kAttnKStages + 2 * kAttnVStages + 4 + 3;
 constexpr size_t kAttnBarBytes = 256;                // barriers, TMEM address, abort flag
 constexpr size_t kAttnSmemBytes =
-    1024 + (size_t)kAttnTile * (2 + kAttnKStages + kAttnVStages) + kAttnBarBytes;
+    1024 + (size_t)kAttnTile * (2 + kAttnKStages + kAttnVStages) + kAttnBarBytes + 2 * kAttnBM * sizeof(float);
 static_assert(8 * kAttnNumBars + 8 <= kAttnBarBytes, "barrier block");
-constexpr uint32_t kAttnTmemCols = 512;              // O_A | O_B | S_A | S_B (P_t over the first 64 columns of S_t)
+constexpr uint32_t kAttnTmemCols = 512;              // O_A | O_B | S_A | S_B (P_t over columns [0,32) and [64,96) of S_t)
 constexpr uint32_t kAttnColO = 0, kAttnColS = 256;
 constexpr uint32_t kAttnIdesc = idesc_bf16_f32(kAttnBM, kAttnBN);  // P V: bf16 x bf16
 // Q K^T: fp16 x fp16 (format 0 in bits 7-9 and 10-12), fp32 accumulator
@@ -107,6 +107,11 @@ __device__ __forceinline__ bool wait_sleep(uint32_t bar, uint32_t parity, const 
   }
 }
 
+// Named barrier over `count` threads (whole warps) of this CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // a * b + c clamped to [0, 1]
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float r;
@@ -149,19 +154,22 @@ __device__ __forceinline__ int attn_item_of(int c, int k, int G) {
 //    stage never holds back keys;
 //  - warp 1 (MMA): S_A(0), S_B(0), then per block j: P V_A(j), S_A(j+1),
 //    P V_B(j), S_B(j+1).  The tensor cores work on one tile while the softmax
-//    of the other runs.  P_t (bf16) is written over the first 64 columns of S_t
-//    and read from TMEM as the A operand of P V_t; the tensor core runs one
+//    of the other runs.  P_t (bf16) is written over S_t (see below) and read
+//    from TMEM as the A operand of P V_t; the tensor core runs one
 //    CTA's MMAs in issue order, so S_t(j+1), issued after P V_t(j), overwrites
 //    P_t(j) only after it was read;
-//  - warps 2-5 (tile A) and 6-9 (tile B): one query row per thread turns S_t(j)
-//    into P_t(j) and at the end of the item writes ctx = O_t / l.
+//  - warps 2-9 (tile A) and 10-17 (tile B): two threads per query row (keys
+//    0-63 and 64-127 of a block) turn S_t(j) into P_t(j); each writes its 32
+//    columns of P over S columns it read itself ([0,32) and [64,96)), so no
+//    thread overwrites S another has not read; at the end of the item the two
+//    row sums meet in shared memory and ctx = O_t / l is written.
 // Ring, buffer and phase counters run across items.
 //
 // Softmax weight of a logit s (c' = c log2(e)):
 //   2^(clamp(s log2(e) / sqrt(128), -c', c') - c') = 2^(2c' (u - 1)),
 //   u = saturate(s / (2 c sqrt(128)) + 1/2)
 // one saturating FMA per value, one packed FMA per pair, then ex2.
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __maxnreg__(112)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -172,6 +180,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kAttnTile * (2 + kAttnKStages + kAttnVStages));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* l_row = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kAttnBarBytes);  // [tile][128]
   const uint32_t b0 = smem_addr(bars);
   const uint32_t q_full = b0, q_empty = b0 + 8u;
   auto k_full = [&](int s) { return b0 + 8u * (2 + s); };
@@ -322,12 +331,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // O_t += P_t V_b
       auto issue_pv = [&](int t, int b, bool acc) {
         const uint32_t vb = smem_addr(sV + (size_t)(b % kAttnVStages) * kAttnTile);
-        const uint32_t pa = tmem_base + kAttnColS + (uint32_t)t * kAttnBN;  // P_t over the first 64 columns of S_t
+        // P_t: keys 0-63 in S_t columns [0,32), keys 64-127 in [64,96)
+        const uint32_t pa = tmem_base + kAttnColS + (uint32_t)t * kAttnBN;
         const uint32_t d = tmem_base + kAttnColO + (uint32_t)t * kAttnBN;
 #pragma unroll
         for (int kk = 0; kk < kAttnBN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P
-          umma_bf16_tmem_a(d, pa + 8 * kk, smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3),
-                           kAttnIdesc, (acc || kk != 0) ? 1u : 0u);
+          umma_bf16_tmem_a(d, pa + (kk >> 2) * 64 + 8 * (kk & 3),
+                           smem_desc_k_sw128(vb + (kk >> 2) * kAttnHalf) + 2 * (kk & 3), kAttnIdesc,
+                           (acc || kk != 0) ? 1u : 0u);
       };
       auto wait_k = [&](int b) {
         const bool got = wait_sleep(k_full(b % kAttnKStages), (uint32_t)(b / kAttnKStages) & 1u, abort_flag,
@@ -400,11 +411,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int q4 = warp & 3;             // TMEM lanes [32 q4, 32 q4 + 32) are reachable from this warp
-    const int t = (warp - 2) >> 2;       // query tile: 0 = A, 1 = B
+    const int t = (warp - 2) >> 3;       // query tile: 0 = A, 1 = B
+    const int half = ((warp - 2) >> 2) & 1;  // keys [64 half, 64 half + 64) of each block; O columns likewise
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t sb = tmem_base + lane_off + kAttnColS + (uint32_t)t * kAttnBN;  // S_t (and P_t)
-    const uint32_t ob = tmem_base + lane_off + kAttnColO + (uint32_t)t * kAttnBN;  // O_t
+    const uint32_t sb = tmem_base + lane_off + kAttnColS + (uint32_t)t * kAttnBN + half * 64;  // this half of S_t
+    const uint32_t ob = tmem_base + lane_off + kAttnColO + (uint32_t)t * kAttnBN + half * 64;  // this half of O_t
     const float ss = p.sat_scale;
     const uint64_t w2 = f32x2(p.clamp2_log2, p.clamp2_log2), mw2 = f32x2(-p.clamp2_log2, -p.clamp2_log2);
     bool ok = true;
@@ -423,31 +435,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after_sync();
         const bool diag = (j == qt);  // the only block with keys after some queries
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t s0[32], s1[32];
-          tmem_ld_32x32b_x32(sb + hh * 64, s0);
-          tmem_ld_32x32b_x32(sb + hh * 64 + 32, s1);
+        for (int cc = 0; cc < 2; ++cc) {  // 32 keys at a time
+          uint32_t sv[32];
+          tmem_ld_32x32b_x32(sb + cc * 32, sv);
           tmem_ld_wait();
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
-            const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-            const uint64_t t2 = fma_f32x2(
-                f32x2(fma_sat(__uint_as_float(u0), ss, 0.5f), fma_sat(__uint_as_float(u1), ss, 0.5f)), w2, mw2);
+          for (int c = 0; c < 16; ++c) {
+            const uint64_t t2 = fma_f32x2(f32x2(fma_sat(__uint_as_float(sv[2 * c]), ss, 0.5f),
+                                                fma_sat(__uint_as_float(sv[2 * c + 1]), ss, 0.5f)),
+                                          w2, mw2);
             float t0, t1;
             f32x2_split(t2, t0, t1);
             float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
             if (diag) {
-              const int key = hh * 64 + 2 * c;
+              const int key = half * 64 + cc * 32 + 2 * c;
               if (key > r) p0 = 0.f;
               if (key + 1 > r) p1 = 0.f;
             }
             l2 = add_f32x2(l2, f32x2(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
           }
-          // P columns [32 hh, 32 hh + 32) of the buffer: S columns already read
-          tmem_st_32x32b_x32(sb + hh * 32, pk);
+          // 16 P columns over S columns this thread has already read
+          tmem_st_32x32b_x16(sb + cc * 16, pk);
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -455,38 +465,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       n_tot += nblk;
       const bool got = ok && __all_sync(0xffffffffu, wait_sleep(o_full, (uint32_t)k & 1u, abort_flag, p.timeout_ns));
-      // every softmax thread reaches this barrier once per item, so a thread that
-      // gave up takes all of them out together
-      ok = named_bar_and(1, kAttnSoftmaxThreads, got);
-      if (!ok) break;
-      tc_fence_after_sync();
       float la, lb;
       f32x2_split(l2, la, lb);
-      const float inv = 1.f / (la + lb);
+      const float l_mine = la + lb;
+      if (half == 1) l_row[t * kAttnBM + r] = l_mine;
+      // every softmax thread reaches this barrier once per item (a thread that
+      // gave up takes all of them out together); it also publishes the second
+      // halves' row sums
+      ok = named_bar_and(1, kAttnSoftmaxThreads, got);
+      if (!ok) break;
+      if (half == 0) l_row[t * kAttnBM + r] += l_mine;
+      named_bar_sync(1, kAttnSoftmaxThreads);  // the whole row sums are in place
+      tc_fence_after_sync();
+      const float inv = 1.f / l_row[t * kAttnBM + r];
       const int qrow = qt * kAttnBM + r;
-      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh;
+      __nv_bfloat16* dst = p.ctx + (size_t)qrow * p.ctx_ld + (size_t)h * kAttnDh + half * 64;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t o0[32], o1[32];
-        tmem_ld_32x32b_x32(ob + hh * 64, o0);
-        tmem_ld_32x32b_x32(ob + hh * 64 + 32, o1);
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(ob + cc * 32, o);
         tmem_ld_wait();
-        if (hh == 1) {
-          // this warp's reads of O are done: the next item's P V may overwrite it
+        if (cc == 1) {
+          // this warp's reads of O and of the row sums are done: the next item may overwrite them
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(o_empty);
         }
         if (qrow < p.T) {
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            pk[c] = pack_bf16x2(__uint_as_float(o0[2 * c]) * inv, __uint_as_float(o0[2 * c + 1]) * inv);
-            pk[16 + c] = pack_bf16x2(__uint_as_float(o1[2 * c]) * inv, __uint_as_float(o1[2 * c + 1]) * inv);
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + hh * 64);
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
     }
