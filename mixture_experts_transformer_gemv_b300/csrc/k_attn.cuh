@@ -169,7 +169,7 @@ __device__ __forceinline__ int attn_item_of(int c, int k, int G) {
 //   2^(clamp(s log2(e) / sqrt(128), -c', c') - c') = 2^(2c' (u - 1)),
 //   u = saturate(s / (2 c sqrt(128)) + 1/2)
 // one saturating FMA per value, one packed FMA per pair, then ex2.
-__global__ void __maxnreg__(112)
+__global__ void __maxnreg__(96)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
