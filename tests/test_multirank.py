@@ -82,3 +82,29 @@ def test_reference_arm_runs_on_rank0_only():
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_attention_reference_arm_line():
+    """--impl reference for the attention workload (tiny shape, CPU only): one
+    line with the attention metric, the oracle's rate and zero copy bytes."""
+    out = _run_bench(["--impl", "reference", "--workload", "attn_tiny", "--steps", "1", "--warmup", "3"],
+                     {"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"})
+    assert len(out) == 1
+    line = out[0]
+    assert line["impl"] == "reference" and line["value"] > 0 and "attention" in line["metric"]
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_attention_work_counts():
+    """The bench's algorithmic work for the attention block: causal pairs
+    T(T+1)/2 per head counted by brute force, projection flops from the shapes."""
+    import bench
+    import synth
+    inp = synth.make_attn_inputs(37, 256, 4, 2, 1, Dh=128)
+    w = bench.attn_work(inp)
+    pairs = sum(1 for q in range(inp.T) for k in range(inp.T) if k <= q)
+    assert w["attn"] == ("tensor", 4.0 * 128 * 4 * pairs)
+    assert w["qkv"] == ("tensor", 2.0 * 37 * 256 * (4 + 2 * 2) * 128)
+    assert w["oproj"] == ("tensor", 2.0 * 37 * 4 * 128 * 256)
+    assert bench.attn_compulsory_bytes(inp) == 4 * 37 * 128 * 2 + 2 * 2 * 37 * 128 * 2 + 37 * 4 * 128 * 2
