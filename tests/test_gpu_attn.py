@@ -139,3 +139,16 @@ def test_graph_capture():
     _, y_ref, _ = oracle.attn_tokens(inp)
     assert_values(out.float().cpu().numpy().astype(np.float64), y_ref, "graph replay")
     blk.close()
+
+
+@pytest.mark.parametrize("base,clamp", [(1_000_000.0, 20.0), (500.0, 40.0)])
+def test_other_rope_base_and_clamp(base, clamp):
+    """The rotation table and the clamp follow the configuration: another base and
+    clamp bound (40 is the largest the fixed-offset softmax accepts) against the
+    oracle with the same settings, on the workload whose logits reach the clamp."""
+    inp = synth.make_attn_inputs(260, 768, 6, 1, 2010, name="attn_cfg", qk_gain=5.0, rope_base=base, clamp=clamp)
+    blk = make_block(inp)
+    y = run(blk, inp)
+    _, y_ref, _ = oracle.attn_tokens(inp)
+    assert_values(y, y_ref, f"base={base} clamp={clamp}")
+    blk.close()
