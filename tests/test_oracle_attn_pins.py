@@ -205,3 +205,25 @@ def test_workload_shapes():
     assert a.wq.shape == (6144, 6144) and a.wk.shape == (1024, 6144)
     assert a.wv.shape == (1024, 6144) and a.wo.shape == (6144, 6144)
     assert a.clamp == 30.0 and a.Dh == 128
+
+
+def test_multi_head_special_case():
+    """Hkv = Hq (plain multi-head attention, no grouping) against the torch formulation."""
+    inp = small(T=19, d=64, Hq=4, Hkv=4, Dh=8)
+    y_t, ctx_t, _ = torch_block(inp)
+    _, y, ctx = oracle.attn_tokens(inp, want_ctx=True)
+    np.testing.assert_allclose(ctx, ctx_t, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(y, y_t, rtol=1e-9, atol=1e-11)
+
+
+def test_attention_branch_is_scale_invariant():
+    """The pre-norm makes the attention branch independent of the scale of x:
+    y(a x) - a x equals y(x) - x (a = 4, exact in bf16; eps = 0 so the norm's
+    epsilon does not break the invariance)."""
+    inp = small(T=21)
+    inp.eps = 0.0
+    _, y1, _ = oracle.attn_tokens(inp)
+    x1 = f64(inp.x)
+    inp.x = synth.f32_to_bf16_bits((4.0 * x1).astype(np.float32))
+    _, y4, _ = oracle.attn_tokens(inp)
+    np.testing.assert_allclose(y4 - 4.0 * x1, y1 - x1, rtol=1e-9, atol=1e-9)
