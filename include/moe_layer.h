@@ -51,14 +51,16 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,  /* shape or dtype this build does not implement */
   MOE_ERR_OOM = 3,          /* workspace allocation failed in moe_layer_create */
   MOE_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed */
-  MOE_ERR_DEVICE_CHECK = 5, /* a device-side index check failed (MOE_FLAG_DEVICE_CHECKS) */
+  MOE_ERR_DEVICE_CHECK = 5, /* a device-side check failed (MOE_FLAG_DEVICE_CHECKS): an index out of
+                               range, or an int8 layer's fp16 activation past +-65504 (saturated) */
   MOE_ERR_TIMEOUT = 6       /* a bounded device wait ran out; the kernel returned early */
 } moe_status_t;
 
 typedef enum { MOE_WEIGHT_BF16 = 0, MOE_WEIGHT_INT8 = 1 } moe_weight_dtype_t;
 
 /* Bits of moe_config_t.flags */
-#define MOE_FLAG_DEVICE_CHECKS 0x1u /* kernels validate routing indices and row maps */
+#define MOE_FLAG_DEVICE_CHECKS 0x1u /* kernels validate routing indices and row maps; int8 layers
+                                      also report fp16 saturation of their activations */
 #define MOE_FLAG_FORCE_TC 0x2u      /* always use the tensor-core grouped GEMM path */
 #define MOE_FLAG_FORCE_GEMV 0x4u    /* always use the weight-streaming decode path */
 
@@ -254,7 +256,8 @@ moe_status_t moe_layer_workspace(const moe_layer_t* layer, moe_workspace_view_t*
  * host that gives an op only its input and output buffers (there cudaMalloc
  * fails or stalls the device mid-step).
  *   topk_idx      DEVICE [T, 2] int32, experts in [0, 8) (e.g. moe_layer_forward's
- *                 topk_idx); an out-of-range index is counted as expert 0
+ *                 topk_idx); an out-of-range index is counted as expert 0 and
+ *                 NOT reported: this entry point has no error word to latch it in
  *   topk_prob     DEVICE [T, 2] fp32, their probabilities
  *   T             0 <= T <= 16384 (larger T: MOE_ERR_INVALID_ARG); T == 0 is a no-op
  *   expert_counts DEVICE [8] int32, written: slots per expert
@@ -262,7 +265,7 @@ moe_status_t moe_layer_workspace(const moe_layer_t* layer, moe_workspace_view_t*
  *                 expert's slots are laid out contiguously in token order and
  *                 each expert's block is padded to a multiple of 128 rows
  *   stream        cudaStream_t (as void*), asynchronous
- * Scratch lives in one static device array of about 264 KB that every GPU
+ * Scratch lives in one static device array of 270,592 bytes (about 264 KB) that every GPU
  * loading this library holds until the process exits.  All calls share it, so
  * calls that overlap on the GPU (other streams, other threads) race: order them.
  * The first call on a device looks up the array's device address (a one-time

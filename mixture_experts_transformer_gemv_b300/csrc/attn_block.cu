@@ -100,7 +100,7 @@ moe_status_t enqueue(attn_block* B, const void* x, void* y, int T, cudaStream_t 
     if (ev) cudaEventRecord(ev[k], st);
   };
   const int d = B->cfg.d_model, Hq = B->cfg.n_q_heads, Hkv = B->cfg.n_kv_heads;
-  const int rows_pad = (int)align_up((size_t)T, kRowTile);
+  const int rows_pad = (int)align_up((size_t)T, kGemmBM);
   const int t_pad = (int)align_up((size_t)T, 2 * kAttnBM);  // whole pairs of query tiles
   mark(ATTN_K_PRENORM);
   attn_prenorm_kernel<<<rows_pad, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), B->s_pre, B->cfg.eps, T,
@@ -222,7 +222,7 @@ moe_status_t attn_block_create(const attn_config_t* cfg, const attn_weights_t* w
   const int d = c.d_model, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   B->n_qkv = (Hq + 2 * Hkv) * kAttnDh;
   B->n_ctx = Hq * kAttnDh;
-  B->rows_cap = (int64_t)align_up((size_t)c.max_tokens, kRowTile);
+  B->rows_cap = (int64_t)align_up((size_t)c.max_tokens, kGemmBM);
   B->t_stride = (int64_t)align_up((size_t)c.max_tokens, 2 * kAttnBM);
   const size_t R = (size_t)B->rows_cap, TS = (size_t)B->t_stride;
   const size_t sz_wqkv = (size_t)B->n_qkv * d * 2;
@@ -269,10 +269,10 @@ moe_status_t attn_block_create(const attn_config_t* cfg, const attn_weights_t* w
   if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return bail(fail(MOE_ERR_CUDA, "workspace initialisation kernels failed"));
 
-  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_xn, B->xn, d, R, kGemmHalfM);
-  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_wqkv, B->wqkv, d, (uint64_t)B->n_qkv, kGemmHalfN);
-  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_ctx, B->ctx, (uint64_t)B->n_ctx, R, kGemmHalfM);
-  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_wo, B->wo, (uint64_t)B->n_ctx, d, kGemmHalfN);
+  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_xn, B->xn, d, R, kGemmBoxRows);
+  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_wqkv, B->wqkv, d, (uint64_t)B->n_qkv, kGemmBoxRows);
+  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_ctx, B->ctx, (uint64_t)B->n_ctx, R, kGemmBoxRows);
+  if (s == MOE_OK) s = make_tmap_bf16(&B->tm_wo, B->wo, (uint64_t)B->n_ctx, d, kGemmBoxRows);
   if (s == MOE_OK) s = make_tmap_bf16(&B->tm_q, B->q, kAttnDh, (uint64_t)Hq * TS, kAttnBM);
   if (s == MOE_OK) s = make_tmap_bf16(&B->tm_k, B->k, kAttnDh, (uint64_t)Hkv * TS, kAttnBN);
   if (s == MOE_OK) s = make_tmap_bf16(&B->tm_vt, B->vt, TS, (uint64_t)Hkv * kAttnDh, kAttnDh);

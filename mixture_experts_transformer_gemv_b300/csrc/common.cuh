@@ -8,15 +8,20 @@ namespace moe {
 
 constexpr int kNumExperts = 8;   // Grok-1: 8 experts ("Jah-yee/grok" README, architecture diagram)
 constexpr int kTopK = 2;         // top-2 routing
-constexpr int kRowTile = 256;    // rows of one expert GEMM tile (a CTA pair); expert row blocks are padded to it
+constexpr int kRowPad = 128;     // expert row blocks are padded to a multiple of this (half a CTA-pair tile)
 
 // Device error word bits (latched in the handle, read by moe_layer_sync_status).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrCheck = 2u;
+// An int8 layer carries its normed rows and GeGLU activations in fp16; with
+// device checks on, a value beyond the fp16 range (|v| > 65504, stored
+// saturated or, for a normed row, as infinity) sets this bit.
+constexpr uint32_t kErrSaturate = 4u;
+constexpr float kF16Max = 65504.f;
 
 // Layout of the small scheduling block K2 writes and the GEMMs read:
 //   [0, E)        counts[e]       slots routed to expert e
-//   [E, 2E + 1)   row_offset[e]   first permuted row of expert e (multiple of kRowTile);
+//   [E, 2E + 1)   row_offset[e]   first permuted row of expert e (multiple of kRowPad);
 //                                 row_offset[E] = total padded rows
 constexpr int kSchedInts = 2 * kNumExperts + 1;
 

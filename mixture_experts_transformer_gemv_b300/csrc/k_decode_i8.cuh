@@ -95,6 +95,7 @@ struct DecI8Params {
   int scale_experts;          // E_s: 8 (per expert) or 1 (shared)
   int scale_groups;           // G groups along the reduction; 1 = per output channel only
   int group_kb;               // G > 1: k-blocks of 128 per group
+  int checks;                 // K3q: report activations past the fp16 range
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -299,11 +300,15 @@ __global__ void __launch_bounds__(DecI8Cfg<EPI>::kThreads, 1)
         const float sw = chan ? __uint_as_float((uint32_t)p.scale0[si] << 16) : 1.0f;
         const float sv = chan ? __uint_as_float((uint32_t)p.scale1[si] << 16) : 1.0f;
         uint16_t* out = static_cast<uint16_t*>(p.out);
+        bool sat = false;
 #pragma unroll
         for (int s = 0; s < kDecNS; ++s)
-          if (s < d.cnt)
-            out[(size_t)(d.row0 + s) * p.n_out + n] =
-                f16_sat(gelu_tanh(sw * __uint_as_float(h[s])) * (sv * __uint_as_float(v[s])));
+          if (s < d.cnt) {
+            const float a = gelu_tanh(sw * __uint_as_float(h[s])) * (sv * __uint_as_float(v[s]));
+            sat |= fabsf(a) > kF16Max;
+            out[(size_t)(d.row0 + s) * p.n_out + n] = f16_sat(a);
+          }
+        if (p.checks && __any_sync(0xffffffffu, sat) && lane == 0) atomicOr(p.err, kErrSaturate);
       } else {
         uint32_t y[16];
         tmem_ld_32x32b_x16(tb, y);

@@ -7,7 +7,7 @@
 // diagram: GELU(x W) (*) (x Wv), then the output projection; weights in PyTorch
 // [out, in] order per "TevunahAi/Grok-1-BF16", "Weight Verification").
 //
-// A tile is M = 256 permuted rows x N = 256 accumulator columns.  One thread of
+// A full tile is M = 256 permuted rows x N = 256 accumulator columns.  One thread of
 // the even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16): A rows
 // [0,128) and B rows [0,128) come from the even CTA's shared memory, A rows
 // [128,256) and B rows [128,256) from the odd CTA's, and each CTA's Tensor Memory
@@ -29,14 +29,25 @@
 //               of its own TMA stages to the even CTA's barrier.
 //   warps 2-5   epilogue of the CTA's 128 rows: tcgen05.ld, GeGLU or scaling,
 //               stores; then tell the even CTA's MMA warp the accumulator is free
-//   warps 6-13  int8 weights only: int8 -> fp16 conversion of the CTA's B half
+//   warps 6-13  int8 weights only: int8 -> fp16 conversion of the CTA's B half,
+//               two groups of four warps on alternate k-blocks
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap the
 // mainloop of tile i+1.
 //
 // Tiles never mix experts: expert e owns permuted rows [row_offset[e],
-// row_offset[e+1]), a multiple of 256.  Tile t maps to (expert, n-block,
-// m-block) with the m-block fastest, so pairs working at the same time share
-// the same weight tile through L2.
+// row_offset[e+1]), a multiple of 128.  Its rows are cut into full tiles of 256
+// and, when 128 rows are left, one half tile: there the pair issues M = 128
+// MMAs (half the tensor-core work of a full tile), each CTA staging 64 A rows.
+// With M = 128 the pair's Tensor Memory layout differs: each CTA's TMEM lanes
+// 0-63 hold its 64 rows against accumulator columns [0, 128) and lanes 64-127
+// the same rows against columns [128, 256), in TMEM columns [0, 128).  So in
+// the up projection's half tile each CTA stages 64 rows of W and the same 64
+// rows of Wv (the even CTA channels [0, 64) of the n-block, the odd CTA [64,
+// 128)): every TMEM lane then holds h and v of the same 64 channels of one row.
+// Tile t maps to (expert, n-block, m-block) with the m-block fastest, so pairs
+// working at the same time share the same weight tile through L2.
+//
+// Every TMA box is 64 rows (8 KB of bf16): a CTA's 128 rows take two boxes.
 //
 // int8 weights ("TevunahAi/Grok-1-BF16", "Conversion Details": int8 values
 // with bf16 scales, one per expert and output channel for the (8, 1, N) scale
@@ -67,8 +78,9 @@
 
 namespace moe {
 
-constexpr int kGemmBM = 256;     // rows per tile (pair)
-constexpr int kGemmHalfM = 128;  // rows per CTA
+constexpr int kGemmBM = 256;     // rows per full tile (pair)
+constexpr int kGemmHalfM = 128;  // rows per CTA of a full tile; rows of a half tile
+constexpr int kGemmBoxRows = 64; // rows of every TMA box of the GEMMs (A and B)
 constexpr int kGemmBN = 256;     // MMA N (accumulator columns)
 constexpr int kGemmHalfN = 128;  // B rows per CTA
 constexpr int kGemmBK = 64;      // K per stage (64 bf16 = one 128-byte swizzle row)
@@ -77,16 +89,22 @@ constexpr int kConvWarp0 = 6;    // first converter warp (warps 6-13, int8 weigh
 constexpr int kEpiWarps = 4;
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kConvGroups = 2;                              // converter groups, alternate k-blocks
+constexpr int kConvGroupThreads = kConvThreads / kConvGroups;
 constexpr int kATileBytes = kGemmHalfM * kGemmBK * 2;   // 16 KB
 constexpr int kBTileBytes = kGemmHalfN * kGemmBK * 2;   // 16 KB (bf16, swizzled)
 constexpr int kB8TileBytes = kGemmHalfN * kGemmBK;      // 8 KB (int8 staging, dense rows of 64 B)
 constexpr uint32_t kTmemCols = 2 * kGemmBN;              // two fp32 accumulators of 128 x 256 per CTA
 constexpr uint32_t kGemmIdesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+constexpr uint32_t kGemmIdescHalf = idesc_bf16_f32(kGemmHalfM, kGemmBN);
 // fp16 A and B (format 0 in bits 7-9 and 10-12): int8 weights converted to fp16,
 // or fp16 operands on the bf16 path (f16_operands)
-constexpr uint32_t kGemmIdescF16 = (1u << 4) | (static_cast<uint32_t>(kGemmBN >> 3) << 17) |
-                                   (static_cast<uint32_t>(kGemmBM >> 4) << 24);
-static_assert(kGemmBM == kRowTile, "expert row blocks are whole tiles");
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+constexpr uint32_t kGemmIdescF16 = idesc_f16_f32(kGemmBM, kGemmBN);
+constexpr uint32_t kGemmIdescF16Half = idesc_f16_f32(kGemmHalfM, kGemmBN);
+static_assert(kGemmBM == 2 * kRowPad, "an expert's row block is full tiles and at most one half tile");
 
 // Per weight type:
 //   bf16: a TMA ring of 6 stages, A 16 KB + B 16 KB each; 6 warps.
@@ -99,6 +117,7 @@ struct GemmCfg {
   static constexpr int kStages = 6;             // TMA ring
   static constexpr int kBStages = WQ ? 3 : 0;   // converted-B ring
   static constexpr int kStageBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
+  static constexpr int kStageBytesHalf = kATileBytes / 2 + (WQ ? kB8TileBytes : kBTileBytes);  // half tile
   static constexpr int kThreads = 32 * (kConvWarp0 + (WQ ? kConvWarps : 0));
   // full, empty (TMA ring), bfull, bempty (converted ring), tmem_full x2, tmem_empty x2, drain
   static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 5;
@@ -122,27 +141,39 @@ struct GemmParams {
   int scale_groups;              // int8: G groups along the reduction; 1 = per output channel only
   int group_kb;                  // int8, G > 1: k-blocks of 64 per group
   int f16_operands;              // bf16 path: A and B hold fp16 instead of bf16 (both the same type)
+  int checks;                    // int8 up projection: report activations past the fp16 range
   uint32_t* err;                 // device error word
   uint64_t timeout_ns;           // limit of every wait
 };
 
 struct TileCoord {
   int e, row0, n_blk;
+  bool half;  // 128 rows (M = 128 MMAs) instead of 256
 };
 
-// Tile t -> (expert, first row, n-block); tiles of expert e are
-// [ (off[e]/256) * n_tiles, (off[e+1]/256) * n_tiles ), m-block fastest.
-__device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExperts + 1], int n_tiles) {
+// m-blocks (full or half tiles) of the experts before e: mb[e] =
+// sum_{q < e} ceil((off[q + 1] - off[q]) / 256).
+__device__ __forceinline__ void mblock_prefix(const int (&off)[kNumExperts + 1], int (&mb)[kNumExperts + 1]) {
+  mb[0] = 0;
+#pragma unroll
+  for (int q = 0; q < kNumExperts; ++q) mb[q + 1] = mb[q] + (off[q + 1] - off[q] + kGemmBM - 1) / kGemmBM;
+}
+
+// Tile t -> (expert, first row, n-block, half); tiles of expert e are
+// [mb[e] * n_tiles, mb[e + 1] * n_tiles), m-block fastest.
+__device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExperts + 1],
+                                                 const int (&mb)[kNumExperts + 1], int n_tiles) {
   int e = 0;
 #pragma unroll
   for (int q = 1; q < kNumExperts; ++q)
-    if (t >= (off[q] / kGemmBM) * n_tiles) e = q;
-  const int mt = off[e + 1] / kGemmBM - off[e] / kGemmBM;
-  const int local = t - (off[e] / kGemmBM) * n_tiles;
+    if (t >= mb[q] * n_tiles) e = q;
+  const int mt = mb[e + 1] - mb[e];
+  const int local = t - mb[e] * n_tiles;
   TileCoord c;
   c.e = e;
   c.n_blk = local / mt;
   c.row0 = off[e] + (local % mt) * kGemmBM;
+  c.half = off[e + 1] - c.row0 < kGemmBM;
   return c;
 }
 
@@ -205,10 +236,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
   const bool leader = rank == 0;
   const int pair = (int)cluster_id_x(), num_pairs = (int)num_clusters_x();
 
-  int off[kNumExperts + 1];
+  int off[kNumExperts + 1], mb[kNumExperts + 1];
 #pragma unroll
   for (int q = 0; q <= kNumExperts; ++q) off[q] = p.sched[kNumExperts + q];
-  const int num_tiles = (off[kNumExperts] / kGemmBM) * p.n_tiles;
+  mblock_prefix(off, mb);
+  const int num_tiles = mb[kNumExperts] * p.n_tiles;
   const int kb_count = p.K / kGemmBK;
 
   if (threadIdx.x == 0) {
@@ -253,23 +285,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const TileCoord tc = decode_tile(t, off, p.n_tiles);
-        const int arow = tc.row0 + (int)rank * kGemmHalfM;
-        // this CTA's 128 rows of B: W (even) or Wv (odd) for the up projection,
-        // the first or second 128 output rows of W1 for the down projection
-        const int brow = (EPI == kEpiGeglu) ? tc.e * p.b_rows_per_expert + tc.n_blk * kGemmHalfN
-                                            : tc.e * p.b_rows_per_expert + tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
-        const CUtensorMap* bmap = (EPI == kEpiGeglu && !leader) ? &tm_b1 : &tm_b0;
+        const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
+        // this CTA's A rows: 128 of a full tile, 64 of a half tile
+        const int arow = tc.row0 + (int)rank * (tc.half ? kGemmBoxRows : kGemmHalfM);
+        // this CTA's 128 rows of B, as two boxes of 64 rows.  Up projection, full
+        // tile: 128 rows of W (even) or Wv (odd); half tile: the CTA's 64 rows of
+        // the n-block from W, then the same 64 rows from Wv.  Down projection:
+        // the first or second 128 output rows of W1.
+        const int nrow = tc.e * p.b_rows_per_expert;
+        int brow0, brow1;
+        const CUtensorMap *bmap0 = &tm_b0, *bmap1 = &tm_b0;
+        if (EPI == kEpiGeglu && tc.half) {
+          brow0 = brow1 = nrow + tc.n_blk * kGemmHalfN + (int)rank * kGemmBoxRows;
+          bmap1 = &tm_b1;
+        } else if (EPI == kEpiGeglu) {
+          brow0 = nrow + tc.n_blk * kGemmHalfN;
+          brow1 = brow0 + kGemmBoxRows;
+          if (!leader) bmap0 = bmap1 = &tm_b1;
+        } else {
+          brow0 = nrow + tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
+          brow1 = brow0 + kGemmBoxRows;
+        }
+        constexpr int kBBox = (WQ ? kB8TileBytes : kBTileBytes) / 2;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
-          tma_load_2d(smem_addr(sA + stage * kATileBytes), &tm_a, fb, kb * kGemmBK, arow);
-          tma_load_2d(smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes), bmap, fb, kb * kGemmBK,
-                      brow);
+          mbar_arrive_expect_tx(fb, tc.half ? C::kStageBytesHalf : C::kStageBytes);
+          const uint32_t sa = smem_addr(sA + stage * kATileBytes);
+          tma_load_2d(sa, &tm_a, fb, kb * kGemmBK, arow);
+          if (!tc.half) tma_load_2d(sa + kATileBytes / 2, &tm_a, fb, kb * kGemmBK, arow + kGemmBoxRows);
+          const uint32_t sb = smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes);
+          tma_load_2d(sb, bmap0, fb, kb * kGemmBK, brow0);
+          tma_load_2d(sb + kBBox, bmap1, fb, kb * kGemmBK, brow1);
           for (int s = 0; s < C::kStages; ++s)
             if (s == (int)stage) issued[s] = (int)phase;
           if (++stage == (uint32_t)C::kStages) {
@@ -302,13 +352,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        const bool half = decode_tile(t, off, mb, p.n_tiles).half;
         if (!wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kGemmBN;
-        const uint32_t idesc = (WQ || p.f16_operands) ? kGemmIdescF16 : kGemmIdesc;
+        const uint32_t idesc = (WQ || p.f16_operands) ? (half ? kGemmIdescF16Half : kGemmIdescF16)
+                                                      : (half ? kGemmIdescHalf : kGemmIdesc);
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded_cluster(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
               (WQ && !wait_bounded_cluster(bfull_bar(bstage), bphase, abort_flag, p.timeout_ns))) {
@@ -372,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
     const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are reachable from this warp
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < num_tiles; t += num_pairs) {
-      const TileCoord tc = decode_tile(t, off, p.n_tiles);
+      const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
       bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -380,16 +432,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         break;
       }
       tc_fence_after_sync();
-      const int row = tc.row0 + (int)rank * kGemmHalfM + q * 32 + lane;
+      // Full tile: lane = row of the CTA's 128, all 256 accumulator columns.
+      // Half tile: lane % 64 = row of the CTA's 64, lanes >= 64 hold accumulator
+      // columns [128, 256) in TMEM columns [0, 128).
+      const int hsel = tc.half ? (q >> 1) : 0;
+      const int row = tc.half ? tc.row0 + (int)rank * kGemmBoxRows + (q & 1) * 32 + lane
+                              : tc.row0 + (int)rank * kGemmHalfM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kGemmBN;
       if (EPI == kEpiGeglu) {
-        const int n0 = tc.n_blk * kGemmHalfN;
+        // full tile: channels n0 + [0, 128), h in TMEM columns [0, 128), v in [128, 256);
+        // half tile: channels n0 + 64 hsel + [0, 64), h in [0, 64), v in [64, 128)
+        const int nch = tc.half ? kGemmHalfN / 2 : kGemmHalfN;
+        const int n0 = tc.n_blk * kGemmHalfN + hsel * (kGemmHalfN / 2);
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.n_out + n0;
+        bool sat = false;  // int8 layers, device checks: an activation past the fp16 range
 #pragma unroll 1
-        for (int c = 0; c < kGemmHalfN / 32; ++c) {
+        for (int c = 0; c < nch / 32; ++c) {
           uint32_t h[32], v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, h);
-          tmem_ld_32x32b_x32(tbase + kGemmHalfN + c * 32, v);
+          tmem_ld_32x32b_x32(tbase + nch + c * 32, v);
           tmem_ld_wait();
           if (WQ && p.scale_groups == 1) {  // per-output-channel scales of W and Wv (same for every row)
             const size_t so = (size_t)(p.scale_experts > 1 ? tc.e : 0) * p.n_out + n0 + c * 32;
@@ -411,17 +472,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
             const float a0 = gelu_tanh(__uint_as_float(h[2 * j])) * __uint_as_float(v[2 * j]);
             const float a1 = gelu_tanh(__uint_as_float(h[2 * j + 1])) * __uint_as_float(v[2 * j + 1]);
             pk[j] = WQ ? pack_f16x2_sat(a0, a1) : pack_bf16x2(a0, a1);  // int8 layers carry fp16 rows
+            if (WQ) sat |= fmaxf(fabsf(a0), fabsf(a1)) > kF16Max;
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
+        if (WQ && p.checks && __any_sync(0xffffffffu, sat) && lane == 0) atomicOr(p.err, kErrSaturate);
       } else {
+        // full tile: output columns n_blk 256 + [0, 256); half tile: n_blk 256 + 128 hsel + [0, 128)
         float* orow = static_cast<float*>(p.out) + (size_t)row * p.n_out;
         const float ps = p.row_scale[row];
+        const int ncol = tc.half ? kGemmBN / 2 : kGemmBN;
 #pragma unroll 1
-        for (int c = 0; c < kGemmBN / 32; ++c) {
-          const int col0 = tc.n_blk * kGemmBN + c * 32;
+        for (int c = 0; c < ncol / 32; ++c) {
+          const int col0 = tc.n_blk * kGemmBN + hsel * (kGemmBN / 2) + c * 32;
           if (col0 >= p.n_out) break;  // ragged last block along d (warp-uniform)
           uint32_t y[32];
           tmem_ld_32x32b_x32(tbase + c * 32, y);
@@ -459,21 +524,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-  } else if (WQ) {
+  } else if constexpr (WQ) {
     // -------------------------------------------------- int8 -> fp16 converter
     // Staging tile: 128 rows x 64 int8, row r at byte 64 r.  MMA tile: 128 rows x
     // 64 fp16 in 128-byte swizzle atoms of 8 rows: element (r, k) at
     // (r / 8) * 1024 + (r % 8) * 128 + ((k / 8) ^ (r % 8)) * 16 + (k % 8) * 2.
-    const int ct = threadIdx.x - kConvWarp0 * 32;
-    uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
+    // Two groups of four warps take alternate k-blocks (group g the k-blocks
+    // with an even or odd running count), so two conversions are in flight at
+    // once.  A group can be at most one k-block ahead of the other (k-block
+    // j + 2 needs converted buffer (j + 2) % 3 back from the MMA, which needs
+    // k-block j - 1 converted), so a wait on a ring barrier never sees a phase
+    // two ahead of the one it expects.
+    const int grp = (warp - kConvWarp0) / (kConvWarps / kConvGroups);
+    const int ct = threadIdx.x - (kConvWarp0 + grp * (kConvWarps / kConvGroups)) * 32;
+    int gk = 0;  // running k-block count over this CTA's tiles
     bool ok = true;
     for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-      // grouped scales (G > 1): this CTA's B rows are weight rows nb + r
-      const TileCoord tc = decode_tile(t, off, p.n_tiles);
-      const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN : tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
-      const uint16_t* gsc = (EPI == kEpiGeglu && !leader) ? p.scale1 : p.scale0;
+      // grouped scales (G > 1): staged B row r is weight row nb + r of the matrix
+      // whose scales are gsc; in an up-projection half tile rows [64, 128) are
+      // the same channels of Wv as rows [0, 64) of W
+      const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
+      const bool split_wv = EPI == kEpiGeglu && tc.half;
+      const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN + (tc.half ? (int)rank * kGemmBoxRows : 0)
+                                        : tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
+      const uint16_t* gsc = (EPI == kEpiGeglu && !leader && !tc.half) ? p.scale1 : p.scale0;
       const size_t gsc_e = (size_t)(p.scale_experts > 1 ? tc.e : 0) * p.scale_groups;
       for (int kb = 0; kb < kb_count; ++kb) {
+        const int my = gk++;
+        if ((my & 1) != grp) continue;
+        const uint32_t stage = (uint32_t)(my % C::kStages), phase = (uint32_t)(my / C::kStages) & 1u;
+        const uint32_t bstage = (uint32_t)(my % C::kBStages), bphase = (uint32_t)(my / C::kBStages) & 1u;
         const bool got = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
                                                      wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag,
                                                                   p.timeout_ns));
@@ -484,8 +564,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           // this row's group scale (bf16 bits in both halves of s2)
           auto convert = [&](auto with_scale) {
 #pragma unroll
-            for (int i = 0; i < kB8TileBytes / 16 / kConvThreads; ++i) {
-              const int u = ct + i * kConvThreads;
+            for (int i = 0; i < kB8TileBytes / 16 / kConvGroupThreads; ++i) {
+              const int u = ct + i * kConvGroupThreads;
               const int r = u >> 2, c = u & 3;
               const uint4 qv = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
               uint4 o0, o1;
@@ -494,8 +574,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
               i8x4_to_f16x4(qv.z, o1.x, o1.y);
               i8x4_to_f16x4(qv.w, o1.z, o1.w);
               if constexpr (decltype(with_scale)::value) {
-                const int n = nb + r;
-                const uint32_t sb = n < p.n_out ? gsc[(gsc_e + kb / p.group_kb) * p.n_out + n] : 0u;
+                const bool wv_row = split_wv && r >= kGemmBoxRows;
+                const int n = nb + (wv_row ? r - kGemmBoxRows : r);
+                const uint16_t* sarr = wv_row ? p.scale1 : gsc;
+                const uint32_t sb = n < p.n_out ? sarr[(gsc_e + kb / p.group_kb) * p.n_out + n] : 0u;
                 __half2 sh = __float2half2_rn(__uint_as_float(sb << 16));
                 const uint32_t s2 = *reinterpret_cast<uint32_t*>(&sh);
                 o0 = make_uint4(f16x2_mul(o0.x, s2), f16x2_mul(o0.y, s2), f16x2_mul(o0.z, s2), f16x2_mul(o0.w, s2));
@@ -512,38 +594,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
             convert(std::false_type{});
           fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
         }
-        // Every converter warp of this CTA reaches this barrier each k-block and
-        // they leave the loop together (a warp that gave up waiting makes all
-        // give up).  After it every converted row of the buffer is written and
-        // fenced for the async proxy; one thread tells the even CTA's MMA warp.
-        // The odd CTA's arrival is relaxed: a cluster-scope release costs about
-        // a microsecond per k-block, and the barrier already ordered the writes.
-        ok = named_bar_and(1, kConvThreads, got);
+        // Every warp of the group reaches this barrier each of its k-blocks and
+        // they leave the loop together (a warp that gave up waiting makes the
+        // group give up; the abort flag then stops the other group).  After it
+        // every converted row of the buffer is written and fenced for the async
+        // proxy; one thread tells the even CTA's MMA warp.  The odd CTA's
+        // arrival is relaxed: a cluster-scope release costs about a microsecond
+        // per k-block, and the barrier already ordered the writes.
+        // (barrier ids 1 and 2 as constants: a computed id reserves all 16)
+        ok = grp == 0 ? named_bar_and(1, kConvGroupThreads, got) : named_bar_and(2, kConvGroupThreads, got);
         if (!ok) break;
-        if (threadIdx.x == kConvWarp0 * 32) {
+        if (ct == 0) {
           if (leader)
             mbar_arrive(bfull_bar(bstage));
           else
             mbar_arrive_cluster_relaxed(map_to_cta(bfull_bar(bstage), 0));
         }
-        if (++stage == (uint32_t)C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++bstage == (uint32_t)C::kBStages) {
-          bstage = 0;
-          bphase ^= 1u;
-        }
       }
     }
-    // every release of a converted buffer by the MMA issuer has landed before exit
-    for (int i = 0; i < C::kBStages && ok; ++i) {
-      ok = __all_sync(0xffffffffu, wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag, p.timeout_ns));
-      if (++bstage == (uint32_t)C::kBStages) {
-        bstage = 0;
-        bphase ^= 1u;
-      }
-    }
+    // every release of a converted buffer by the MMA issuer has landed before
+    // exit: group 0 waits for the releases of the last uses of every buffer
+    if (grp == 0)
+      for (int j = max(0, gk - C::kBStages); j < gk && ok; ++j)
+        ok = __all_sync(0xffffffffu, wait_bounded(bempty_bar((uint32_t)(j % C::kBStages)),
+                                                  (uint32_t)(j / C::kBStages) & 1u, abort_flag, p.timeout_ns));
     if (!ok && lane == 0) raise_abort(abort_flag, p.err);
   }
 

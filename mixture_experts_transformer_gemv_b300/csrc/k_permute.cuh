@@ -9,6 +9,9 @@
 //   row_offset[e]  = sum_{e' < e} ceil(counts[e'] / 128) * 128   (tiles never mix experts)
 //   rows of expert e, in slot order s = 2t + r (stable: token, then rank);
 //   padding rows (up to the next multiple of 128) get token -1 and weight 0.
+// With checks != 0 an expert index outside [0, 8) is counted as expert 0 and a
+// row past rows_cap is not written; each case also sets kErrCheck in *err
+// unless err is null.
 // A single CTA does the scan (it is a few microseconds even at T = 65536);
 // the gather of the normed rows into expert order runs on all SMs.
 #pragma once
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
   for (int s = s0; s < s1; ++s) {
     int e = idx[s];
     if (checks && (e < 0 || e >= kNumExperts)) {
-      atomicOr(err, kErrCheck);
+      if (err) atomicOr(err, kErrCheck);
       e = 0;
     }
 #pragma unroll
@@ -70,10 +73,10 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
     int off = 0;
     for (int e = 0; e < kNumExperts; ++e) {
       s_off[e] = off;
-      off += (s_counts[e] + kRowTile - 1) / kRowTile * kRowTile;
+      off += (s_counts[e] + kRowPad - 1) / kRowPad * kRowPad;
     }
     s_off[kNumExperts] = off;
-    if (checks && off > rows_cap) atomicOr(err, kErrCheck);
+    if (checks && off > rows_cap) if (err) atomicOr(err, kErrCheck);
   }
   __syncthreads();
   int pos[kNumExperts];
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
     for (int q = 0; q < kNumExperts; ++q)
       if (q == e) row = pos[q]++;
     if (checks && row >= rows_cap) {
-      atomicOr(err, kErrCheck);
+      if (err) atomicOr(err, kErrCheck);
       row_of_slot[s] = 0;
       continue;
     }
@@ -112,13 +115,16 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
 
 // xn_perm[row] = xn[token_of_row[row]] (zeros for padding rows); rows beyond
 // row_offset[E] are left alone.  Grid-stride over rows, 16-byte accesses.
-// to_f16 != 0 (int8 weight-streaming path) stores the rows as fp16 instead of
-// bf16: every bf16 value of a normed row converts exactly unless it is below
-// the fp16 normal range (|v| < 2^-14), where the error is under 2^-24.
+// to_f16 != 0 (int8 weights) stores the rows as fp16 instead of bf16: every
+// bf16 value of a normed row converts exactly unless it is below the fp16
+// normal range (|v| < 2^-14), where the error is under 2^-24, or beyond its
+// largest value (|v| > 65504, stored as infinity; with checks != 0 this sets
+// kErrSaturate in *err).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ xn,
                                                           const int32_t* __restrict__ token_of_row,
                                                           const int32_t* __restrict__ sched, int d, int to_f16,
-                                                          __nv_bfloat16* __restrict__ xn_perm) {
+                                                          __nv_bfloat16* __restrict__ xn_perm, int checks,
+                                                          uint32_t* __restrict__ err) {
   const int rows = sched[2 * kNumExperts];
   const int nchunk = d >> 3;
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -129,6 +135,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
       for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
         uint4 v = src[c];
         if (to_f16) {
+          if (checks) {
+            const float m = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                                        fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))),
+                                  fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
+                                        fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+            if (m > kF16Max) atomicOr(err, kErrSaturate);
+          }
           v.x = f16x2_from_bf16x2(v.x);
           v.y = f16x2_from_bf16x2(v.y);
           v.z = f16x2_from_bf16x2(v.z);

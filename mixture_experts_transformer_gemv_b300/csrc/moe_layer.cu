@@ -94,7 +94,8 @@ struct moe_layer {
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
-  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1_128{};  // boxes of 128 rows x 64
+  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w64{}, tm_wv64{}, tm_w1_64{};  // grouped GEMMs: boxes of 64 rows x 64
+  CUtensorMap tm_w{}, tm_wv{}, tm_w1_128{};                           // decode path: boxes of 128 rows x 64
   CUtensorMap tm_xn_perm16{}, tm_act16{};                             // decode path: 16-row boxes
   CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes)
   CUtensorMap tm_w8d{}, tm_wv8d{}, tm_w18d{};           // int8 weights, 64-byte swizzle (decode)
@@ -176,7 +177,8 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     const int grid = (int)std::min<int64_t>(L->rows_cap, (int64_t)L->num_sms * 8);
     // int8 layers multiply in fp16 (int8 -> fp16 is one shuffle and one
     // subtraction), so their activation rows are fp16
-    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, int8 ? 1 : 0, L->xn_perm);
+    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, int8 ? 1 : 0, L->xn_perm,
+                                             checks, L->err);
   }
   mark(3);
   if (decode && int8) {
@@ -193,6 +195,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.scale_experts = L->cfg.scale_experts;
     p.scale_groups = L->cfg.scale_groups;
     p.group_kb = d / L->cfg.scale_groups / kDq8BK;
+    p.checks = checks;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     decode_gemm_i8_kernel<kEpiGeglu><<<L->num_sms, DecI8Cfg<kEpiGeglu>::kThreads, DecI8Cfg<kEpiGeglu>::kSmemBytes,
@@ -224,6 +227,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.scale_experts = L->cfg.scale_experts;
     p.scale_groups = L->cfg.scale_groups;
     p.group_kb = d / L->cfg.scale_groups / kGemmBK;
+    p.checks = checks;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     if (int8)
@@ -232,7 +236,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
           L->tm_xn_perm, L->tm_w8, L->tm_wv8, p);
     else
       grouped_gemm_kernel<kEpiGeglu, false><<<L->gemm_grid[kEpiGeglu][0], kGemmThreads, kGemmSmemBytes, st>>>(
-          L->tm_xn_perm, L->tm_w, L->tm_wv, p);
+          L->tm_xn_perm, L->tm_w64, L->tm_wv64, p);
   }
   mark(4);
   if (decode && int8) {
@@ -287,7 +291,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
                                             GemmCfg<true>::kSmemBytes, st>>>(L->tm_act, L->tm_w18, L->tm_w18, p);
     else
       grouped_gemm_kernel<kEpiDown, false><<<L->gemm_grid[kEpiDown][0], kGemmThreads, kGemmSmemBytes, st>>>(
-          L->tm_act, L->tm_w1_128, L->tm_w1_128, p);
+          L->tm_act, L->tm_w1_64, L->tm_w1_64, p);
   }
   mark(5);
   {
@@ -399,7 +403,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   L->device = dev;
   L->num_sms = prop.multiProcessorCount;
   const int64_t T = c.max_tokens, d = c.d_model, F = c.d_ffn;
-  L->rows_cap = (int64_t)align_up((size_t)(2 * T), kRowTile) + (int64_t)kNumExperts * kRowTile;
+  L->rows_cap = (int64_t)align_up((size_t)(2 * T), kRowPad) + (int64_t)kNumExperts * kRowPad;
   const int64_t R = L->rows_cap;
 
   // one workspace block, every buffer 1 KB aligned
@@ -440,17 +444,20 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   while (L->ksplit_i8 > 1 && (F / kDq8BK) % L->ksplit_i8) L->ksplit_i8 /= 2;
   moe_status_t s = MOE_OK;
   if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmHalfM);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmHalfM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmBoxRows);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmBoxRows);
   if (c.weight_dtype == MOE_WEIGHT_BF16) {
     static_assert(kGemmHalfN == kDecBM, "the GEMM and decode paths share the 128-row weight boxes");
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmHalfN);
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv, w->wv, d, kNumExperts * F, kGemmHalfN);
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kGemmHalfN);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w64, w->w, d, kNumExperts * F, kGemmBoxRows);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv64, w->wv, d, kNumExperts * F, kGemmBoxRows);
+    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_64, w->w1, F, kNumExperts * d, kGemmBoxRows);
   } else {
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmHalfN, kGemmBK);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmHalfN, kGemmBK);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmBoxRows, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmBoxRows, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmBoxRows, kGemmBK);
     if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8d, w->w, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == MOE_OK)
       s = make_tmap_i8(&L->tm_wv8d, w->wv, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -568,7 +575,9 @@ moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
     MOE_CUDA_TRY(cudaMemsetAsync(L->err, 0, sizeof(uint32_t), st));
     MOE_CUDA_TRY(cudaStreamSynchronize(st));
     if (h & kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device wait ran out of time (error word 0x%x)", h);
-    return fail(MOE_ERR_DEVICE_CHECK, "a device index check failed (error word 0x%x)", h);
+    if (h & kErrCheck) return fail(MOE_ERR_DEVICE_CHECK, "a device index check failed (error word 0x%x)", h);
+    return fail(MOE_ERR_DEVICE_CHECK,
+                "an fp16 activation of an int8 layer passed +-65504 and was saturated (error word 0x%x)", h);
   }
   return ok();
 }
@@ -759,9 +768,11 @@ moe_status_t moe_layer_workspace(const moe_layer_t* L, moe_workspace_view_t* v) 
 // the address (cudaGetSymbolAddress, with that device current) and caches it.
 namespace {
 constexpr int kNoAllocMaxTokens = 16384;
-constexpr int kNoAllocRows = 2 * kNoAllocMaxTokens + kNumExperts * kRowTile;
+constexpr int kNoAllocRows = 2 * kNoAllocMaxTokens + kNumExperts * kRowPad;
 constexpr size_t kNoAllocSchedBytes = 256;  // kSchedInts int32, padded
-constexpr size_t kNoAllocScratchBytes = kNoAllocSchedBytes + 2 * (size_t)kNoAllocRows * 4 + 256;
+// schedule block, then token_of_row and prob_of_row of every permuted row
+constexpr size_t kNoAllocScratchBytes = kNoAllocSchedBytes + 2 * (size_t)kNoAllocRows * 4;
+static_assert(kNoAllocScratchBytes == 270592, "the size stated in moe_layer.h");
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices] = {};
@@ -798,12 +809,13 @@ extern "C" moe_status_t moe_group_slots_noalloc(const int32_t* topk_idx, const f
   int32_t* sched = reinterpret_cast<int32_t*>(b);
   int32_t* token_of_row = reinterpret_cast<int32_t*>(b + kNoAllocSchedBytes);
   float* prob_of_row = reinterpret_cast<float*>(b + kNoAllocSchedBytes + (size_t)kNoAllocRows * 4);
-  uint32_t* err = reinterpret_cast<uint32_t*>(b + kNoAllocSchedBytes + 2 * (size_t)kNoAllocRows * 4);
   // Index checks on: the indices come from the caller, and an out-of-range one
-  // is counted as expert 0 instead of indexing past the arrays.  The kernel
-  // writes every scratch word it later reads, so nothing needs clearing.
+  // is counted as expert 0 instead of indexing past the arrays.  No error word
+  // is passed, so such an index is not reported (the header says so).  The
+  // kernel writes every scratch word it later reads, so nothing needs clearing.
   permute_kernel<<<1, kPermuteThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      topk_idx, topk_prob, T, sched, row_of_slot, token_of_row, prob_of_row, expert_counts, kNoAllocRows, 1, err);
+      topk_idx, topk_prob, T, sched, row_of_slot, token_of_row, prob_of_row, expert_counts, kNoAllocRows, 1,
+      nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
   return ok();

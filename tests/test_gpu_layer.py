@@ -175,7 +175,9 @@ def test_intermediates_match_oracle():
     r = oracle.route(inp, keep_xn=True)
     np.testing.assert_allclose(xn, r.xn, rtol=2 ** -8, atol=1e-6)
     np.testing.assert_array_equal(counts, np.bincount(r.idx.ravel(), minlength=8))
-    assert np.all(off % 256 == 0) and np.all(np.diff(off) >= counts)
+    # each expert's block is its slots padded to the next multiple of 128 rows
+    assert off[0] == 0 and np.all(off % 128 == 0)
+    np.testing.assert_array_equal(np.diff(off), (counts + 127) // 128 * 128)
     for t in (0, 17, T - 1):
         for rank in range(2):
             e = int(r.idx[t, rank])
@@ -285,6 +287,32 @@ def test_int8_decode_one_expert_heavy_batch():
 def test_int8_skewed_and_checks():
     inp = synth.make_inputs(256, 256, 512, 74, name="int8_skew", weight_dtype="int8", bias=synth.SKEW_BIAS)
     _full_check(inp, flags=moe.MOE_FLAG_DEVICE_CHECKS)
+
+
+@pytest.mark.parametrize("T", [64, 8])  # grouped tensor-core GEMM path; T <= 16 decode path
+def test_int8_fp16_saturation_is_reported(T):
+    """int8 layers carry their GeGLU activations in fp16, which saturates at
+    +-65504.  With scales ~1000x the synthetic workload's, the activations pass
+    that bound (checked on the oracle first).  Device checks off: the forward
+    reports nothing.  Device checks on: moe_layer_sync_status reports
+    MOE_ERR_DEVICE_CHECK naming the saturation, and the read clears it."""
+    inp = synth.make_inputs(T, 256, 512, 90 + T, name="int8_sat", weight_dtype="int8", int8_scale_range=(0.2, 0.4))
+    r = oracle.route(inp, keep_xn=True)
+    _, _, a, _ = oracle.expert_ffn(inp, r.xn[0], int(r.idx[0, 0]))
+    assert np.max(np.abs(a)) > 65504.0
+    x = bf16_tensor(inp.x)
+    layer = make_layer(inp)
+    layer.forward(x)
+    torch.cuda.synchronize()
+    layer.sync_status()
+    layer.close()
+    layer = make_layer(inp, flags=moe.MOE_FLAG_DEVICE_CHECKS)
+    layer.forward(x)
+    with pytest.raises(moe.MoeError) as ei:
+        layer.sync_status()
+    assert ei.value.status == moe.MOE_ERR_DEVICE_CHECK and "65504" in str(ei.value)
+    layer.sync_status()  # cleared by the read
+    layer.close()
 
 
 def test_int8_intermediates_match_oracle():
