@@ -167,14 +167,26 @@ def group_slots_noalloc(topk_idx, topk_prob, expert_counts, row_of_slot, stream=
     """moe_group_slots_noalloc: per-expert counts and the slot -> row map of the
     layer's grouping step, with no memory allocated (scratch is a static device
     array; T <= 16384; calls must not overlap on the GPU).  All tensors CUDA,
-    int32 / fp32, contiguous: topk_idx, topk_prob [T, 2] in; expert_counts [8],
-    row_of_slot [T, 2] out."""
+    int32 / fp32, contiguous, on one device: topk_idx, topk_prob [T, 2] in;
+    expert_counts [8], row_of_slot [T, 2] out.  Mis-shaped tensors raise
+    ValueError before anything is enqueued."""
     import torch
+    # shapes first: the kernel indexes [T, 2] and [8] arrays, so a short buffer
+    # would be read or written past its end
+    if topk_idx.dim() != 2 or topk_idx.shape[1] != 2:
+        raise ValueError(f"group_slots_noalloc: topk_idx must be [T, 2] (got {tuple(topk_idx.shape)})")
     T = topk_idx.shape[0]
+    for name, t in (("topk_prob", topk_prob), ("row_of_slot", row_of_slot)):
+        if tuple(t.shape) != (T, 2):
+            raise ValueError(f"group_slots_noalloc: {name} must be [{T}, 2] (got {tuple(t.shape)})")
+    if expert_counts.dim() != 1 or expert_counts.numel() < 8:
+        raise ValueError(f"group_slots_noalloc: expert_counts must be [8] (got {tuple(expert_counts.shape)})")
     for t, dt in ((topk_idx, torch.int32), (topk_prob, torch.float32), (expert_counts, torch.int32),
                   (row_of_slot, torch.int32)):
         if not (t.is_cuda and t.dtype == dt and t.is_contiguous()):
             raise ValueError("group_slots_noalloc: tensors must be contiguous CUDA int32 / fp32")
+    if len({t.device for t in (topk_idx, topk_prob, expert_counts, row_of_slot)}) != 1:
+        raise ValueError("group_slots_noalloc: all tensors must be on the same device")
     _check(lib().moe_group_slots_noalloc(topk_idx.data_ptr(), topk_prob.data_ptr(), T, expert_counts.data_ptr(),
                                          row_of_slot.data_ptr(), _stream_handle(stream)), "moe_group_slots_noalloc")
 

@@ -171,3 +171,28 @@ def test_selftest_rejects_bad_arguments(lib):
     assert lib.moe_selftest_bounded_wait(3, 10_000_000, ctypes.byref(el)) == 1
     assert lib.moe_selftest_bounded_wait(0, 10, ctypes.byref(el)) == 1            # below 1 ms
     assert lib.moe_selftest_bounded_wait(1, 3_000_000_000, ctypes.byref(el)) == 1  # above 2 s
+
+
+@pytest.mark.parametrize("what", ["idx_1d", "idx_3col", "prob_short", "ros_short", "counts_short"])
+def test_noalloc_binding_rejects_misshaped_tensors(what):
+    """group_slots_noalloc checks every shape before anything reaches the GPU:
+    a [T, 2] array shorter than topk_idx, or fewer than 8 counts, would make the
+    grouping kernel read or write past the caller's buffers.  CPU tensors are
+    enough: the shape check comes before the device check."""
+    import torch
+    import mixture_experts_transformer_gemv_b300 as moe
+    T = 10
+    a = {"idx": torch.zeros((T, 2), dtype=torch.int32), "prob": torch.zeros((T, 2), dtype=torch.float32),
+         "counts": torch.zeros((8,), dtype=torch.int32), "ros": torch.zeros((T, 2), dtype=torch.int32)}
+    if what == "idx_1d":
+        a["idx"] = torch.zeros((2 * T,), dtype=torch.int32)
+    elif what == "idx_3col":
+        a["idx"] = torch.zeros((T, 3), dtype=torch.int32)
+    elif what == "prob_short":
+        a["prob"] = torch.zeros((T - 1, 2), dtype=torch.float32)
+    elif what == "ros_short":
+        a["ros"] = torch.zeros((T, 1), dtype=torch.int32)
+    else:
+        a["counts"] = torch.zeros((7,), dtype=torch.int32)
+    with pytest.raises(ValueError, match="must be"):
+        moe.group_slots_noalloc(a["idx"], a["prob"], a["counts"], a["ros"])

@@ -6,7 +6,9 @@ op only its input and output buffers).  Its scratch is a static device array
 shared by every call, so this checks two calls in a row, with different inputs,
 each against the grouping the layer's own forward computed (moe_layer_forward,
 read back through the workspace view).  Integer outputs must match exactly.
-Collected last so a stop-at-first-failure run has already run everything else.
+The groupings are also checked against the rule written out in numpy (stable
+slot order, blocks padded to 128 rows).  Collected last so a
+stop-at-first-failure run has already run everything else.
 """
 import numpy as np
 import pytest
@@ -29,6 +31,37 @@ def _forward_grouping(layer, inp):
     return idx, prob, counts.cpu().numpy(), ros
 
 
+def _numpy_grouping(idx):
+    """The grouping rule written out: slots s = 2t + r in order, each expert's
+    block padded to a multiple of 128 rows, experts in index order."""
+    idx = idx.reshape(-1)
+    counts = np.bincount(idx, minlength=8)
+    off = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)])
+    ros = np.empty_like(idx)
+    nxt = off[:8].copy()
+    for s, e in enumerate(idx):
+        ros[s] = nxt[e]
+        nxt[e] += 1
+    return counts, ros.reshape(-1, 2), off
+
+
+def _check_noalloc(layer, inp):
+    idx, prob, counts_ref, ros_ref = _forward_grouping(layer, inp)
+    counts = torch.full((8,), -1, dtype=torch.int32, device="cuda")
+    ros = torch.full((inp.T, 2), -1, dtype=torch.int32, device="cuda")
+    moe.group_slots_noalloc(idx, prob, counts, ros)
+    torch.cuda.synchronize()
+    counts_np, ros_np = counts.cpu().numpy(), ros.cpu().numpy()
+    np.testing.assert_array_equal(counts_np, counts_ref)
+    np.testing.assert_array_equal(ros_np, ros_ref)
+    c2, r2, off = _numpy_grouping(idx.cpu().numpy())
+    np.testing.assert_array_equal(counts_np, c2)
+    np.testing.assert_array_equal(ros_np, r2)
+    # every expert's block starts at a multiple of 128 rows
+    assert np.all(off % 128 == 0)
+    return counts_np
+
+
 def test_noalloc_grouping_matches_layer_forward_twice():
     from mixture_experts_transformer_gemv_b300 import build
     build.build()
@@ -37,15 +70,20 @@ def test_noalloc_grouping_matches_layer_forward_twice():
     layer_a = make_layer(a)
     layer_b = make_layer(b)
     for inp, layer in ((a, layer_a), (b, layer_b)):
-        idx, prob, counts_ref, ros_ref = _forward_grouping(layer, inp)
-        counts = torch.full((8,), -1, dtype=torch.int32, device="cuda")
-        ros = torch.full((inp.T, 2), -1, dtype=torch.int32, device="cuda")
-        moe.group_slots_noalloc(idx, prob, counts, ros)
-        torch.cuda.synchronize()
-        np.testing.assert_array_equal(counts.cpu().numpy(), counts_ref)
-        np.testing.assert_array_equal(ros.cpu().numpy(), ros_ref)
+        _check_noalloc(layer, inp)
     layer_a.close()
     layer_b.close()
+
+
+def test_noalloc_at_its_token_limit_with_skewed_routing():
+    """T = 16384, the largest the static array takes, with the skewed router
+    (most slots on expert 0): the padded row count comes closest to the
+    array's capacity here."""
+    inp = synth.make_inputs(16384, 256, 512, 53, bias=synth.SKEW_BIAS, name="noalloc_limit")
+    layer = make_layer(inp)
+    counts = _check_noalloc(layer, inp)
+    assert counts.sum() == 2 * 16384 and counts[0] > counts[1:].max()
+    layer.close()
 
 
 def test_noalloc_rejects_sizes_beyond_its_limit():
