@@ -9,8 +9,16 @@ seed 1002; expert weights 9.66 GB, larger than L2, so no flush is needed).
 A step is one moe_layer_forward over the whole batch: router, grouping, both
 expert GEMMs, combine, post-norm and residual.
 
-One JSON line on rank 0: the base keys plus roofline (dominant kernel), cpu_baseline,
-e2e (host buffers), clocks and gpu_launches.  With N > 1
+One JSON line on rank 0: the base keys plus roofline (dominant kernel), cpu_baseline
+(with the run's parity summary against the oracle), e2e (host buffers), clocks
+(SM clock, power and throttle reasons sampled every 10 ms over the timed region)
+and gpu_launches.  A tensor-bound roofline divides by the measured burst bf16
+rate when the timed region is shorter than 2 s (else the sustained rate) and
+keeps both fractions.  The default single-GPU run adds two keys: "band" (the
+same weights at T = 16 ... 1024 tokens, across the switch from the
+weight-streaming decode kernels to the grouped tensor-core GEMMs) and "configs"
+(one line each for the decode T=8, int8 T=2048, int8 decode T=8 and skewed
+T=4096 workloads, each with its own step time, roofline and clocks).  With N > 1
 (torchrun) every rank runs its own replica of the workload on its own GPU: the
 layer is token-parallel with no exchange, so scaling is weak and value = N * T
 / max-over-ranks step time.
@@ -117,6 +125,7 @@ def config_block(inp):
 
 
 DECODE_MAX_T = 16  # the library's weight-streaming path takes T <= 16
+ROW_PAD = 128  # each expert's permuted rows are padded to a multiple of this
 
 
 def algorithmic_work(inp, counts):
@@ -160,7 +169,7 @@ def compulsory_bytes(role, inp, counts):
     if inp.T <= DECODE_MAX_T:
         rows = 2 * inp.T
     else:
-        rows = int(sum((c + 255) // 256 * 256 for c in counts))
+        rows = int(sum((c + ROW_PAD - 1) // ROW_PAD * ROW_PAD for c in counts))
     if role == "up_geglu":
         return n_act * 2 * F * d * wb + rows * d * 2 + rows * F * 2
     return n_act * d * F * wb + rows * F * 2 + rows * d * 4
@@ -183,59 +192,168 @@ def recorded_traffic(role, inp, counts):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """SM clock, power and throttle reasons sampled every 10 ms while the timed
+    region runs (NVML from a background thread; nvidia-smi every 100 ms if NVML
+    is unavailable).  Only reads: no clock or power setting is changed."""
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4), ("hw_power_brake_slowdown", 0x80))
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+    def __init__(self, cuda_index, period_s=0.01):
+        self.cuda_index = cuda_index
+        self.period = period_s
+        self.rows = []  # (sm_mhz, sm_max_mhz, power_w, reason bits)
+        self._stop = None
+        self._thread = None
+        self._proc = None
+        self._path = None
+        self.source = None
+        self.nvml_error = None
+
+    @staticmethod
+    def _nvml():
+        """The NVML functions the sampler reads, from libnvidia-ml through ctypes
+        (the driver's library; no Python package needed)."""
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        return nv
+
+    def _handle(self, nv):
+        import ctypes
+        h = ctypes.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle for the device")
+        return h
 
     def start(self):
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        import ctypes
+        import threading
+        try:
+            nv = self._nvml()
+            h = self._handle(nv)
+            clk, smax, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(smax)) != 0:  # 1 = NVML_CLOCK_SM
+                raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+            self._stop = threading.Event()
+
+            def loop():
+                while not self._stop.is_set():
+                    if (nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
+                            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 and
+                            reasons(h, ctypes.byref(rs)) == 0):
+                        self.rows.append((float(clk.value), float(smax.value), mw.value / 1000.0, int(rs.value)))
+                    self._stop.wait(self.period)
+            self._thread = threading.Thread(target=loop, daemon=True)
+            self._thread.start()
+            self.source = f"NVML every {self.period * 1e3:.0f} ms"
+        except Exception as e:  # no NVML: fall back to nvidia-smi and say why
+            self.nvml_error = f"{type(e).__name__}: {e}"[:200]
+            self._start_smi()
+        time.sleep(0.05)
+
+    def _start_smi(self):
+        fd, self._path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self._proc = subprocess.Popen(["nvidia-smi", "-i", str(self.cuda_index), f"--query-gpu={self.FIELDS}",
+                                           "--format=csv,noheader,nounits", "-lms", "100"],
+                                          stdout=open(self._path, "w"), stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi every 100 ms"
         except OSError:
-            self.proc = None
-        time.sleep(0.3)
+            self._proc = None
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _stop_smi(self):
         time.sleep(0.15)
-        self.proc.terminate()
+        self._proc.terminate()
         try:
-            self.proc.wait(timeout=5)
+            self._proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            self._proc.kill()
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
-        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 300] or sm
-        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+        with open(self._path) as f:
+            for line in f:
+                p = [q.strip() for q in line.split(",")]
+                if len(p) < 9 or num(p[1]) is None:
+                    continue
+                bits = 0
+                for (name, bit), col in zip(self.REASONS[:4], p[5:9]):
+                    if col.lower().startswith("active"):
+                        bits |= bit
+                self.rows.append((num(p[1]), num(p[2]) or 0.0, num(p[3]) or 0.0, bits))
+        os.unlink(self._path)
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
+        elif self._proc is not None:
+            self._stop_smi()
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"]}
+        rows = self.rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.source}
+        sm = np.array([r[0] for r in rows])
+        pw = np.array([r[2] for r in rows])
+        loaded = sm[pw > 300] if np.any(pw > 300) else sm
+        reasons = sorted({name for r in rows for name, bit in self.REASONS if r[3] & bit})
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_loaded": int(loaded.size), "source": self.source,
+                "sm_mhz_min": float(loaded.min()), "sm_mhz_p90": float(np.percentile(loaded, 90)),
+                "power_w_max": float(pw.max()),
+                "power_cap_share": round(float(np.mean([bool(r[3] & 0x4) for r in rows])), 3),
+                **({"nvml_error": self.nvml_error} if self.nvml_error else {})}
+
+
+def tensor_roofline(achieved_tflops, pk, peak_kind, timed_s, clk):
+    """Roofline of a tensor-core kernel.  A timed region shorter than 2 s is the
+    burst condition (the GPU has not settled at its power cap), so the peak is
+    the measured burst rate; longer regions use the sustained rate.  Both
+    fractions are kept, and the SM clock sampled over the region gives the
+    fraction of the burst rate scaled to that clock (the burst GEMM is taken to
+    run at the maximum SM clock)."""
+    burst, sust = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
+    use_burst = timed_s < 2.0
+    peak = burst if use_burst else sust
+    roof = {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved_tflops / peak, 4),
+            "peak_kind": f"{'bf16_tflops (burst)' if use_burst else 'bf16_tflops_sustained'} ({peak_kind}); "
+                         "fp16 operands run at the bf16 rate",
+            "frac_of_burst": round(achieved_tflops / burst, 4), "frac_of_sustained": round(achieved_tflops / sust, 4)}
+    if clk.get("sm_mhz") and clk.get("sm_max_mhz"):
+        roof["frac_of_burst_at_sampled_clock"] = round(achieved_tflops / (burst * clk["sm_mhz"] / clk["sm_max_mhz"]),
+                                                       4)
+    return roof
+
+
+def roof_peak_tc(pk, timed_s):
+    """The tensor-core peak tensor_roofline takes for a timed region of timed_s seconds."""
+    return pk["bf16_tflops"] if timed_s < 2.0 else pk["bf16_tflops_sustained"]
+
+
+def hbm_roofline(achieved_gbs, pk, peak_kind):
+    return {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved_gbs / pk["hbm_gbs"], 4), "peak_kind": f"hbm_gbs ({peak_kind})",
+            "frac_of_nominal_8tbs": round(achieved_gbs / 8000.0, 4)}
 
 
 # ------------------------------------------------------------------ our arm
@@ -420,17 +538,11 @@ def run_attn(args, rank, world, local_rank):
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
     bound, amount = work[dom]
     dur_s = kernels[dom]["ms_per_launch"] / 1e3
+    timed_s = ms_total / 1e3
     if bound == "tensor":
-        achieved = amount / dur_s / 1e12
-        peak = pk["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
-                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4)}
+        roof = tensor_roofline(amount / dur_s / 1e12, pk, peak_kind, timed_s, clk)
     else:
-        achieved = amount / dur_s / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})"}
+        roof = hbm_roofline(amount / dur_s / 1e9, pk, peak_kind)
     roof["kernel"] = dom
     roof["algorithmic_per_launch"] = amount
     roof["kernel_function"] = {"attn": "attn_kernel", "qkv": "grouped_gemm_kernel<1, 0>",
@@ -450,7 +562,7 @@ def run_attn(args, rank, world, local_rank):
                    "l2": "no flush: the step reads 0.2 GB of weights and writes/reads 1.3 GB of activations "
                          "(larger than L2) between the same kernels every step"},
         "roofline": roof,
-        "block_tc_frac": round(tc_flops / (ms_step / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 4),
+        "block_tc_frac": round(tc_flops / (ms_step / 1e3) / 1e12 / roof_peak_tc(pk, timed_s), 4),
         "kernels": kernels,
         "e2e": {"value": round(whole_job_tokens_per_s(world, inp.T, e2e_s), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(inp.T * inp.d * 2), "d2h_bytes_per_step": int(inp.T * inp.d * 2),
@@ -470,9 +582,166 @@ def run_attn(args, rank, world, local_rank):
     return result
 
 
+def workload_dtype(inp):
+    """Arithmetic type of the path: bf16 weights multiply in bf16; int8 weights
+    are converted exactly to fp16 on chip and multiply in fp16 (fp32 accumulate,
+    scales applied in fp32)."""
+    return "bf16" if inp.weight_dtype == "bf16" else "w8a16"
+
+
+def device_weights(inp):
+    import torch
+    weights = {
+        "gate": torch.from_numpy(inp.gate).cuda(),
+        "gate_bias": None if inp.bias is None else torch.from_numpy(inp.bias).cuda(),
+        "pre_norm_scale": torch.from_numpy(inp.s_pre).cuda(), "post_norm_scale": torch.from_numpy(inp.s_post).cuda(),
+    }
+    for k in ("w", "wv", "w1"):
+        a = getattr(inp, k)
+        weights[k] = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if inp.weight_dtype == "bf16"
+                      else torch.from_numpy(a)).cuda()
+    if inp.weight_dtype == "int8":
+        for k in ("w_scale", "wv_scale", "w1_scale"):
+            weights[k] = torch.from_numpy(getattr(inp, k).view(np.int16)).view(torch.bfloat16).cuda()
+    return weights
+
+
+def measure_layer(layer, inp, x, out, steps, warmup, local_rank, dist):
+    """Time `steps` forwards of `layer` on device tensor x (after `warmup`
+    untimed ones), with the per-kernel CUDA events of the library on the same
+    stream and the clocks sampled over the timed region.  Returns the step time
+    (max over ranks), per-kernel rates, the dominant kernel's roofline, the
+    routing of x and the clock record."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    layer.sync_status()
+    _, idx, prob, counts = layer.forward(x, out, routing=True)
+    rstats = layer.router_stats().cpu().numpy()
+    counts = counts.cpu().numpy()
+    torch.cuda.synchronize()
+
+    layer.set_profiling(True)
+    layer.profile_read(reset=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    launches0 = layer.launch_count()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        layer.forward(x, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = layer.launch_count() - launches0
+    ms_total = ev0.elapsed_time(ev1)
+    layer.sync_status()
+    prof = layer.profile_read(reset=True)
+    layer.set_profiling(False)
+    ms_step = max_over_ranks(ms_total / steps, dist, "cuda")
+
+    pk, peak_kind = peaks()
+    work = algorithmic_work(inp, counts)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        kernels[name] = {"ms_per_launch": ms / max(n, 1), "launches": n}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
+    bound, amount = work[dom]
+    dur_s = kernels[dom]["ms_per_launch"] / 1e3
+    timed_s = ms_total / 1e3
+    if bound == "tensor":
+        roof = tensor_roofline(amount / dur_s / 1e12, pk, peak_kind, timed_s, clk)
+    else:
+        roof = hbm_roofline(amount / dur_s / 1e9, pk, peak_kind)
+    roof["kernel"] = dom
+    roof["algorithmic_per_launch"] = amount
+    roof["kernel_function"] = kernel_function(dom, inp)[0]
+    roof["traffic"] = recorded_traffic(dom, inp, counts)
+    for name in kernels:
+        b, a = work[name]
+        d_s = kernels[name]["ms_per_launch"] / 1e3
+        kernels[name]["achieved"] = round(a / d_s / (1e12 if b == "tensor" else 1e9), 1) if d_s > 0 else None
+        kernels[name]["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
+        kernels[name]["ms_per_launch"] = round(kernels[name]["ms_per_launch"], 4)
+    layer_flops = 6.0 * inp.d * inp.F * 2 * inp.T
+    step_bytes = sum(a for b, a in work.values() if b == "hbm")
+    res = {
+        "ms_per_step": round(ms_step, 4), "timed_region_s": round(timed_s, 4), "roofline": roof,
+        "layer_tc_frac": round(layer_flops / (ms_step / 1e3) / 1e12 / roof_peak_tc(pk, timed_s), 4),
+        "layer_hbm_frac": round(step_bytes / (ms_step / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+        "kernels": kernels,
+        "expert_counts": [int(c) for c in counts],
+        "router_stats": {"mean_prob": [round(float(v), 5) for v in rstats[:8]],
+                         "entropy_nats": round(float(rstats[8]), 5), "collapse_index": round(float(rstats[9]), 5)},
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+    if inp.T <= DECODE_MAX_T:
+        # the memory-bound case: chosen experts' weights over the whole step
+        wb = 1 if inp.weight_dtype == "int8" else 2
+        n_act = int(sum(1 for c in counts if c > 0))
+        wbytes = n_act * 3 * inp.d * inp.F * wb
+        res["step_weight_gbs"] = round(wbytes / (ms_step / 1e3) / 1e9, 1)
+        res["step_weight_frac"] = round(wbytes / (ms_step / 1e3) / 1e9 / pk["hbm_gbs"], 4)
+        res["step_weight_frac_of_nominal_8tbs"] = round(wbytes / (ms_step / 1e3) / 1e9 / 8000.0, 4)
+    return res, (out, idx, prob)
+
+
+def sub_line(inp, layer, x, steps, warmup, local_rank):
+    """One workload's line inside the headline run: its own step time,
+    throughput, dominant-kernel roofline and clock record."""
+    import torch
+    out = torch.empty_like(x)
+    m, _ = measure_layer(layer, inp, x, out, steps, warmup, local_rank, None)
+    return {"workload": config_block(inp)["workload"], "dtype": workload_dtype(inp), "steps": steps,
+            "warmup": warmup, "value": round(inp.T / (m["ms_per_step"] / 1e3), 1), "unit": UNIT, **m}
+
+
+# Token counts of the sweep across the switch from the weight-streaming decode
+# kernels (T <= 16) to the grouped tensor-core GEMMs, up to the compute-bound knee.
+BAND_TOKENS = (16, 17, 32, 64, 128, 256, 512, 1024)
+
+
+def band_sweep(inp, layer, x_all, steps, warmup, local_rank):
+    """The prefill weights at small token counts: step time, expert-weight bytes
+    per second (HBM-bound side) and flops per second (tensor-bound side)."""
+    pk, _ = peaks()
+    rows = []
+    for T in BAND_TOKENS:
+        sub = synth_subset(inp, T)
+        x = x_all[:T].contiguous()
+        r = sub_line(sub, layer, x, steps, warmup, local_rank)
+        ms = r["ms_per_step"]
+        n_act = int(sum(1 for c in r["expert_counts"] if c > 0))
+        wbytes = n_act * 3 * inp.d * inp.F * (1 if inp.weight_dtype == "int8" else 2)
+        rows.append({"T": T, "ms_per_step": ms, "value": r["value"],
+                     "path": "decode (weight-streaming)" if T <= DECODE_MAX_T else "grouped tensor-core GEMM",
+                     "weight_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+                     "weight_frac_of_hbm": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                     "tflops": round(6.0 * inp.d * inp.F * 2 * T / (ms / 1e3) / 1e12, 1),
+                     "up_ms": r["kernels"]["up_geglu"]["ms_per_launch"],
+                     "down_ms": r["kernels"]["down"]["ms_per_launch"],
+                     "expert_counts": r["expert_counts"], "sm_mhz": r["clocks"].get("sm_mhz")})
+    return rows
+
+
+def synth_subset(inp, T):
+    """The same inputs restricted to the first T tokens (the weights are shared)."""
+    import synth
+    return synth.MoeInputs(**{**inp.__dict__, "T": T, "x": np.ascontiguousarray(inp.x[:T])})
+
+
+SUB_WORKLOADS = ("decode", "int8", "int8_decode", "skew")
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
-    import synth
     import mixture_experts_transformer_gemv_b300 as moe
     from mixture_experts_transformer_gemv_b300 import build as moe_build
 
@@ -487,60 +756,16 @@ def run_ours(args, rank, world, local_rank):
     inp = make_workload(args.workload)
     log(f"[rank {rank}] inputs generated in {time.time() - t0:.1f} s")
     x_host = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16)
-    weights = {
-        "gate": torch.from_numpy(inp.gate).cuda(),
-        "gate_bias": None if inp.bias is None else torch.from_numpy(inp.bias).cuda(),
-        "pre_norm_scale": torch.from_numpy(inp.s_pre).cuda(), "post_norm_scale": torch.from_numpy(inp.s_post).cuda(),
-    }
-    for k in ("w", "wv", "w1"):
-        a = getattr(inp, k)
-        weights[k] = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if inp.weight_dtype == "bf16"
-                      else torch.from_numpy(a)).cuda()
-    if inp.weight_dtype == "int8":
-        for k in ("w_scale", "wv_scale", "w1_scale"):
-            weights[k] = torch.from_numpy(getattr(inp, k).view(np.int16)).view(torch.bfloat16).cuda()
+    weights = device_weights(inp)
     x = x_host.cuda()
     out = torch.empty_like(x)
     layer = moe.MoeLayer(inp.d, inp.F, inp.T, weights, eps=inp.eps, weight_dtype=inp.weight_dtype,
                          scale_shape=(inp.scale_experts, inp.scale_groups))
-    stream = torch.cuda.current_stream()
-
-    # warm-up
-    for _ in range(args.warmup):
-        layer.forward(x, out)
-    torch.cuda.synchronize()
-    layer.sync_status()
-    _, _, _, counts = layer.forward(x, out, routing=True)
-    rstats = layer.router_stats().cpu().numpy()
-    counts = counts.cpu().numpy()
-    torch.cuda.synchronize()
-
-    # timed region: K forwards, per-kernel events recorded on the same stream
-    layer.set_profiling(True)
-    layer.profile_read(reset=True)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    launches0 = layer.launch_count()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        layer.forward(x, out)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clk = clocks.stop()
-    launches = layer.launch_count() - launches0
-    ms_total = ev0.elapsed_time(ev1)
-    layer.sync_status()
-    prof = layer.profile_read(reset=True)
-    layer.set_profiling(False)
-
-    ms_step = max_over_ranks(ms_total / args.steps, dist, "cuda")
+    m, (out, idx, prob) = measure_layer(layer, inp, x, out, args.steps, args.warmup, local_rank, dist)
+    ms_step = m["ms_per_step"]
     value = whole_job_tokens_per_s(world, inp.T, ms_step / 1e3)
+    y_gpu = out.float().cpu().numpy().astype(np.float64)
+    idx_gpu, prob_gpu = idx.cpu().numpy(), prob.cpu().numpy()
 
     # end to end through the host-buffer entry points (pinned memory, copies inside
     # the timed region every step).  Pipelined: moe_layer_forward_host_async keeps
@@ -569,69 +794,58 @@ def run_ours(args, rank, world, local_rank):
         layer.forward_host(xh[0], oh[0])
     e2e_sync_s = max_over_ranks((time.perf_counter() - t1) / e2e_steps, dist, "cuda")
 
-    # kernels: average device time per launch, dominant kernel's roofline
-    pk, peak_kind = peaks()
-    work = algorithmic_work(inp, counts)
-    kernels = {}
-    for name, (ms, n) in prof.items():
-        kernels[name] = {"ms_per_launch": ms / max(n, 1), "launches": n}
-    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
-    bound, amount = work[dom]
-    dur_s = kernels[dom]["ms_per_launch"] / 1e3
-    if bound == "tensor":
-        achieved = amount / dur_s / 1e12
-        peak = pk["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
-                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4)}
-    else:
-        achieved = amount / dur_s / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
-                "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)}
-    roof["kernel"] = dom
-    roof["algorithmic_per_launch"] = amount
-    roof["kernel_function"] = kernel_function(dom, inp)[0]
-    roof["traffic"] = recorded_traffic(dom, inp, counts)
-    for name in kernels:
-        b, a = work[name]
-        d_s = kernels[name]["ms_per_launch"] / 1e3
-        kernels[name]["achieved"] = round(a / d_s / (1e12 if b == "tensor" else 1e9), 1) if d_s > 0 else None
-        kernels[name]["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
-        kernels[name]["ms_per_launch"] = round(kernels[name]["ms_per_launch"], 4)
-    layer_flops = 6.0 * inp.d * inp.F * 2 * inp.T
-    layer_tc_frac = layer_flops / (ms_step / 1e3) / 1e12 / pk["bf16_tflops_sustained"]
-    step_bytes = sum(a for b, a in work.values() if b == "hbm")
-    layer_hbm_frac = step_bytes / (ms_step / 1e3) / 1e9 / pk["hbm_gbs"]
-
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)",
+        "vs_baseline": None, "dtype": workload_dtype(inp),
+        "data": "synthetic (seeded; random-init weights of the Grok-1 shapes)",
         "config": config_block(inp),
-        "roofline": roof,
-        "layer_tc_frac": round(layer_tc_frac, 4),
-        "layer_hbm_frac": round(layer_hbm_frac, 4),
-        "kernels": kernels,
-        "expert_counts": [int(c) for c in counts],
-        "router_stats": {"mean_prob": [round(float(v), 5) for v in rstats[:8]],
-                         "entropy_nats": round(float(rstats[8]), 5), "collapse_index": round(float(rstats[9]), 5)},
+        **{k: v for k, v in m.items() if k != "ms_per_step"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(inp.T * inp.d * 2),
                 "d2h_bytes_per_step": int(inp.T * inp.d * 2), "ms_per_step": round(e2e_s * 1e3, 3),
                 "entry_point": "moe_layer_forward_host_async, two calls in flight (pinned host buffers)",
                 "sync_value": round(whole_job_tokens_per_s(world, inp.T, e2e_sync_s), 1),
                 "sync_ms_per_step": round(e2e_sync_s * 1e3, 3),
                 "sync_entry_point": "moe_layer_forward_host (synchronous)"},
-        "gpu_launches": int(launches),
         "gemm_grid": layer.gemm_grid(),
-        "clocks": clk,
     }
-    layer.close()
-    del weights
-    torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_seconds, gpu=(y_gpu, idx_gpu, prob_gpu))
+    subs = args.workload == WORKLOAD and world == 1 and not args.no_subconfigs
+    if subs:
+        # the band between the decode kernels and the compute-bound knee, on the same weights
+        result["band"] = band_sweep(inp, layer, x, max(5, args.steps // 2), args.warmup, local_rank)
+    layer.close()
+    del weights, x, out
+    torch.cuda.empty_cache()
+    if subs:
+        # the other Grok-1-shape workloads, one line each (single GPU only: each
+        # loads its own 4.8-9.7 GB of expert weights)
+        lines = {}
+        int8_dev = None
+        for name in SUB_WORKLOADS:
+            t0 = time.time()
+            if name == "int8_decode" and int8_dev is not None:
+                sub_inp = synth_subset(int8_dev[0], 8)
+                sub_inp.name = name
+                w_dev = int8_dev[1]
+            else:
+                sub_inp = make_workload(name)
+                w_dev = device_weights(sub_inp)
+            log(f"[rank {rank}] {name}: inputs ready in {time.time() - t0:.1f} s")
+            xs = torch.from_numpy(sub_inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+            lay = moe.MoeLayer(sub_inp.d, sub_inp.F, sub_inp.T, w_dev, eps=sub_inp.eps,
+                               weight_dtype=sub_inp.weight_dtype,
+                               scale_shape=(sub_inp.scale_experts, sub_inp.scale_groups))
+            lines[name] = sub_line(sub_inp, lay, xs, args.steps, args.warmup, local_rank)
+            lay.close()
+            if name == "int8":
+                int8_dev = (sub_inp, w_dev)
+            elif name == "int8_decode":
+                int8_dev = None
+            del w_dev, xs
+            torch.cuda.empty_cache()
+        result["configs"] = lines
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -644,13 +858,19 @@ def oracle_token_sample(inp, n, seed=7):
     return np.sort(rng.choice(inp.T, size=n, replace=False))
 
 
-def cpu_baseline(inp, budget_s=20.0):
+def cpu_baseline(inp, budget_s=20.0, gpu=None):
     """The oracle as it stands on this host: routing of all T tokens plus the
     full layer on a seeded token sample sized to ~budget_s; tokens/s =
-    1 / (layer seconds per sampled token + routing seconds per token)."""
+    1 / (layer seconds per sampled token + routing seconds per token).
+
+    With gpu = (y, topk_idx, topk_prob) of the timed run's output, the same
+    oracle results also give the run's parity summary: routing compared on all
+    T tokens (near-ties of the 2nd and 3rd probability within 1e-6 excluded and
+    counted), values on the sampled tokens against the per-element bound
+    0.02 |y_ref| + 0.02 rms(y_ref row)."""
     import oracle
     t0 = time.perf_counter()
-    oracle.route(inp)
+    ref_route = oracle.route(inp)
     t_route = (time.perf_counter() - t0) / inp.T
     t0 = time.perf_counter()
     oracle.moe_tokens(inp, oracle_token_sample(inp, 1, seed=1))
@@ -658,13 +878,29 @@ def cpu_baseline(inp, budget_s=20.0):
     n = int(max(1, min(64, budget_s / max(t_one, 1e-3))))
     toks = oracle_token_sample(inp, n)
     t0 = time.perf_counter()
-    oracle.moe_tokens(inp, toks)
+    ref = oracle.moe_tokens(inp, toks)
     t_tok = (time.perf_counter() - t0) / n
     per_token = t_tok + t_route
-    return {"value": round(1.0 / per_token, 4), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"routing of all {inp.T} tokens ({t_route * inp.T:.2f} s) + full layer on {n} seeded tokens "
-                      f"({t_tok * n:.1f} s); fp64 C oracle, OpenMP over rows",
-            "seconds_per_token": round(per_token, 4)}
+    res = {"value": round(1.0 / per_token, 4), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": f"routing of all {inp.T} tokens ({t_route * inp.T:.2f} s) + full layer on {n} seeded tokens "
+                     f"({t_tok * n:.1f} s); fp64 C oracle, OpenMP over rows",
+           "seconds_per_token": round(per_token, 4)}
+    if gpu is not None:
+        y, idx, prob = gpu
+        excl = oracle.near_tie_tokens(ref_route.p, 1e-6)
+        order_tie = oracle.near_order_tie_tokens(ref_route.p, 1e-6)
+        same_set = np.all(np.sort(idx, axis=1) == np.sort(ref_route.idx, axis=1), axis=1)
+        yr = ref.y
+        rms = np.sqrt(np.mean(yr * yr, axis=1, keepdims=True))
+        ratio = np.abs(y[toks] - yr) / (0.02 * np.abs(yr) + 0.02 * rms)
+        res["parity"] = {
+            "routing_tokens": int(inp.T), "near_tie_excluded": int(excl.sum()),
+            "routing_set_mismatch": int(np.sum(~same_set & ~excl)),
+            "routing_order_mismatch": int(np.sum(~np.all(idx == ref_route.idx, axis=1) & ~excl & ~order_tie)),
+            "value_tokens": int(len(toks)), "value_max_tolerance_ratio": round(float(ratio.max()), 4),
+            "value_violations": int(np.sum(ratio > 1.0)),
+            "tolerance": "|y - y_ref| <= 0.02 |y_ref| + 0.02 rms(y_ref row), per element"}
+    return res
 
 
 def run_reference(args):
@@ -735,6 +971,8 @@ def main():
                     help="prefill (T=8192) is the headline workload")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-subconfigs", action="store_true",
+                    help="headline workload only: skip the band sweep and the decode/int8/skew sub-lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
