@@ -108,14 +108,17 @@ static_assert(kGemmBM == 2 * kRowPad, "an expert's row block is full tiles and a
 
 // Per weight type:
 //   bf16: a TMA ring of 6 stages, A 16 KB + B 16 KB each; 6 warps.
-//   int8: a TMA ring of 6 stages, A 16 KB + int8 B 8 KB each, and a ring of 3
-//         converted bf16 B halves (16 KB each) between the converter warps and
-//         the MMA warp; 14 warps.  (Measured: deeper rings, 8 + 2 or 6 + 5, do
-//         not change the rate.)
+//   int8: a TMA ring of 5 stages, A 16 KB + int8 B 8 KB each, and a ring of 6
+//         converted fp16 B halves (16 KB each) between the converter warps and
+//         the MMA warp; 14 warps.  (Measured at the int8 workload, TMA + converted
+//         stages: 6 + 3 1030-1040 TFLOP/s, 5 + 6 1059-1072, 5 + 5 1064, 4 + 6
+//         1009, 3 + 6 883.  Loading the int8 weights into the converters'
+//         registers straight from global memory, two k-blocks ahead, instead of
+//         staging them by TMA: 660.)
 template <bool WQ>
 struct GemmCfg {
-  static constexpr int kStages = 6;             // TMA ring
-  static constexpr int kBStages = WQ ? 3 : 0;   // converted-B ring
+  static constexpr int kStages = WQ ? 5 : 6;    // TMA ring
+  static constexpr int kBStages = WQ ? 6 : 0;   // converted-B ring
   static constexpr int kStageBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
   static constexpr int kStageBytesHalf = kATileBytes / 2 + (WQ ? kB8TileBytes : kBTileBytes);  // half tile
   static constexpr int kThreads = 32 * (kConvWarp0 + (WQ ? kConvWarps : 0));
@@ -531,10 +534,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
     // (r / 8) * 1024 + (r % 8) * 128 + ((k / 8) ^ (r % 8)) * 16 + (k % 8) * 2.
     // Two groups of four warps take alternate k-blocks (group g the k-blocks
     // with an even or odd running count), so two conversions are in flight at
-    // once.  A group can be at most one k-block ahead of the other (k-block
-    // j + 2 needs converted buffer (j + 2) % 3 back from the MMA, which needs
-    // k-block j - 1 converted), so a wait on a ring barrier never sees a phase
-    // two ahead of the one it expects.
+    // once.  A wait on a ring barrier never sees a phase two ahead of the one
+    // it expects: the next phase of any slot a group waits on (a TMA stage or
+    // a converted buffer) needs that group's own conversion first.
     const int grp = (warp - kConvWarp0) / (kConvWarps / kConvGroups);
     const int ct = threadIdx.x - (kConvWarp0 + grp * (kConvWarps / kConvGroups)) * 32;
     int gk = 0;  // running k-block count over this CTA's tiles

@@ -10,18 +10,30 @@
 //   p      = softmax(l)                      (max-subtracted, fp32)
 //   i0, i1 = two largest p, ties to the lower index; weights p_i0, p_i1
 //
-// One CTA of 256 threads handles kRouterTok tokens (4 for large T, 1 for small
-// T, where more CTAs hide latency better): every gate value it loads feeds all
-// of them (the gate is [8, d] fp32 and is read from L2 once per CTA, not once
-// per token).  x rows are read with 16-byte loads, twice (the second
-// pass hits L1/L2).
+// One CTA of 256 threads handles kRouterTok tokens (8 for large T at d <= 7168,
+// fewer for wider rows, 1 for small T, where more CTAs hide latency better).
+// Its x rows are copied once into shared memory (cp.async, 16 bytes per copy)
+// and both passes read them there, so every x byte crosses HBM once.  Every
+// gate value the CTA loads feeds all of its tokens (the gate is [8, d] fp32
+// and is read from L2 once per CTA, not once per token); the experts are taken
+// four (at 8 tokens, two) at a time so the gate values, the normed chunk and the
+// 8 x kRouterTok partial logits fit in registers at two CTAs per SM.
 #pragma once
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
 constexpr int kRouterThreads = 256;
-constexpr int kRouterTokMax = 4;  // tokens per CTA for large T; 1 for small T (more CTAs)
+constexpr int kRouterTokMax = 8;             // tokens per CTA for large T
+constexpr int kRouterSmemMax = 112 * 1024;   // staged x rows per CTA (two CTAs per SM)
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 
 template <int kRouterTok>
 __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
@@ -29,6 +41,7 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
     const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
     __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
     int32_t* __restrict__ user_idx, float* __restrict__ user_prob, float* __restrict__ p_part) {
+  extern __shared__ __align__(16) uint8_t router_smem[];  // x rows [kRouterTok][d] bf16
   __shared__ float red[kRouterThreads / 32][kRouterTok * kNumExperts];
   __shared__ float rnorm[kRouterTok];
   __shared__ float s_p[kRouterTok][kNumExperts];
@@ -36,6 +49,17 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
   const int ntok = min(kRouterTok, T - t0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = d >> 3;  // 8 bf16 per 16-byte chunk
+  const uint32_t xs = smem_addr(router_smem);
+  auto xchunk = [&](int i, int c) {
+    return *reinterpret_cast<const uint4*>(router_smem + ((size_t)i * d + (size_t)c * 8) * 2);
+  };
+
+  // ---- the CTA's x rows into shared memory, one read of HBM
+  for (int i = 0; i < ntok; ++i)
+    for (int c = threadIdx.x; c < nchunk; c += kRouterThreads)
+      cp_async16(xs + (uint32_t)(((size_t)i * d + (size_t)c * 8) * 2), x + (size_t)(t0 + i) * d + c * 8);
+  cp_async_wait_all();
+  __syncthreads();
 
   // ---- pass 1: sum of squares per token
   float ss[kRouterTok];
@@ -45,11 +69,11 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
 #pragma unroll
     for (int i = 0; i < kRouterTok; ++i) {
       if (i < ntok) {
-        uint4 v = ld_nc_v4(x + (size_t)(t0 + i) * d + c * 8);
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint4 v = xchunk(i, c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
+          const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
           ss[i] = fmaf(a, a, ss[i]);
           ss[i] = fmaf(b, b, ss[i]);
         }
@@ -73,7 +97,10 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
 #pragma unroll
   for (int i = 0; i < kRouterTok; ++i) r[i] = rnorm[i];
 
-  // ---- pass 2: xn (bf16 copy out) and the 8 logits of every token
+  // ---- pass 2: xn (bf16 copy out) and the 8 logits of every token, experts
+  // in groups of four (two at 8 tokens per CTA); the normed chunk is recomputed
+  // from shared memory for every group: the same fp32 products
+  constexpr int kEPer = kRouterTok >= 8 ? 2 : 4;
   float lg[kRouterTok][kNumExperts];
 #pragma unroll
   for (int i = 0; i < kRouterTok; ++i)
@@ -84,40 +111,41 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
     const float4 sa = *reinterpret_cast<const float4*>(s_pre + c * 8);
     const float4 sb = *reinterpret_cast<const float4*>(s_pre + c * 8 + 4);
     const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-    // the normed values of this chunk for every token (and their bf16 copy out)
-    float xn[kRouterTok][8];
 #pragma unroll
-    for (int i = 0; i < kRouterTok; ++i) {
-      if (i < ntok) {
-        uint4 v = ld_nc_v4(x + (size_t)(t0 + i) * d + c * 8);
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int h = 0; h < kNumExperts / kEPer; ++h) {
+      float g[kEPer][8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          xn[i][2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
-          xn[i][2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
-        }
-        uint4 o;
-        o.x = pack_bf16x2(xn[i][0], xn[i][1]);
-        o.y = pack_bf16x2(xn[i][2], xn[i][3]);
-        o.z = pack_bf16x2(xn[i][4], xn[i][5]);
-        o.w = pack_bf16x2(xn[i][6], xn[i][7]);
-        *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xn[i][j] = 0.f;
+      for (int e = 0; e < kEPer; ++e) {
+        const float4 ga = *reinterpret_cast<const float4*>(gate + (size_t)(kEPer * h + e) * d + c * 8);
+        const float4 gb = *reinterpret_cast<const float4*>(gate + (size_t)(kEPer * h + e) * d + c * 8 + 4);
+        g[e][0] = ga.x; g[e][1] = ga.y; g[e][2] = ga.z; g[e][3] = ga.w;
+        g[e][4] = gb.x; g[e][5] = gb.y; g[e][6] = gb.z; g[e][7] = gb.w;
       }
-    }
-    // one expert's 8 gate values at a time, used by every token (registers stay
-    // low enough for two CTAs per SM)
 #pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) {
-      const float4 ga = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8);
-      const float4 gb = *reinterpret_cast<const float4*>(gate + (size_t)e * d + c * 8 + 4);
-      const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+      for (int i = 0; i < kRouterTok; ++i) {
+        if (i < ntok) {
+          const uint4 v = xchunk(i, c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          float xn[8];
 #pragma unroll
-      for (int i = 0; i < kRouterTok; ++i)
+          for (int q = 0; q < 4; ++q) {
+            xn[2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
+            xn[2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
+          }
+          if (h == 0) {
+            uint4 o;
+            o.x = pack_bf16x2(xn[0], xn[1]);
+            o.y = pack_bf16x2(xn[2], xn[3]);
+            o.z = pack_bf16x2(xn[4], xn[5]);
+            o.w = pack_bf16x2(xn[6], xn[7]);
+            *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
+          }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xn[i][j], g[j], lg[i][e]);
+          for (int e = 0; e < kEPer; ++e)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lg[i][kEPer * h + e] = fmaf(xn[j], g[e][j], lg[i][kEPer * h + e]);
+        }
+      }
     }
   }
   // block reduction of the kRouterTok x 8 partial logits

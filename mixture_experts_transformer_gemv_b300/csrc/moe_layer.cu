@@ -158,17 +158,32 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
   const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) || (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
   mark(0);
-  // 4 tokens per router CTA once there are enough CTAs to fill the GPU twice over
-  const int rtok = (T >= 2 * kRouterTokMax * L->num_sms) ? kRouterTokMax : 1;
+  // tokens per router CTA: the most (8, 4 or 2) whose x rows fit the CTA's
+  // shared memory while there are enough CTAs to fill the GPU twice over, else 1
+  int rtok = 1;
+  for (int k = kRouterTokMax; k > 1; k /= 2)
+    if (T >= 2 * k * L->num_sms && (size_t)k * d * 2 <= (size_t)kRouterSmemMax) {
+      rtok = k;
+      break;
+    }
   L->last_router_ctas = (T + rtok - 1) / rtok;
-  if (rtok == kRouterTokMax)
-    router_kernel<kRouterTokMax><<<L->last_router_ctas, kRouterThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
-        L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
-  else
-    router_kernel<1><<<L->last_router_ctas, kRouterThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(hidden), T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale,
-        L->cfg.eps, L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
+  {
+    const size_t rsm = (size_t)rtok * d * 2;
+    const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
+    auto launch = [&](auto kern) {
+      kern<<<L->last_router_ctas, kRouterThreads, rsm, st>>>(xh, T, d, L->w.gate, L->w.gate_bias,
+                                                             L->w.pre_norm_scale, L->cfg.eps, L->xn, L->idx,
+                                                             L->prob, topk_idx, topk_prob, L->p_part);
+    };
+    if (rtok == 8)
+      launch(router_kernel<8>);
+    else if (rtok == 4)
+      launch(router_kernel<4>);
+    else if (rtok == 2)
+      launch(router_kernel<2>);
+    else
+      launch(router_kernel<1>);
+  }
   mark(1);
   permute_kernel<<<1, kPermuteThreads, 0, st>>>(L->idx, L->prob, T, L->sched, L->row_of_slot, L->token_of_row,
                                                L->prob_of_row, counts, (int)L->rows_cap, checks, L->err);
@@ -466,6 +481,15 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
+  {
+    const void* rk[4] = {(const void*)router_kernel<1>, (const void*)router_kernel<2>, (const void*)router_kernel<4>,
+                         (const void*)router_kernel<8>};
+    for (int i = 0; i < 4 && s == MOE_OK; ++i) {
+      const size_t need = std::min<size_t>((size_t)(1 << i) * d * 2, (size_t)kRouterSmemMax);
+      if (cudaFuncSetAttribute(rk[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need) != cudaSuccess)
+        s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (router) failed");
+    }
+  }
   if (s == MOE_OK &&
       cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)

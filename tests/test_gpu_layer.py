@@ -41,7 +41,10 @@ def test_tiny_workload_all_tokens():
     (1000, 256, 640, 32),    # two row blocks per expert, F/128 = 5
     (200, 384, 512, 33),     # d = 384: the last down-projection tile is half outside d
     (7, 256, 512, 34),       # fewer slots than a tile in every expert
-    (1500, 256, 512, 36),    # enough tokens for the 4-tokens-per-CTA router
+    (1500, 256, 512, 36),    # 4 tokens per router CTA (below the 8-token threshold of 2 x 8 x SMs)
+    (2400, 256, 512, 37),    # 8 tokens per router CTA, ragged last CTA (2400 = 300 x 8)
+    (1200, 7680, 256, 38),   # wide rows: 8 rows would not fit the router's shared memory, 4 do
+    (600, 14464, 256, 39),   # wider still: 2 tokens per router CTA
 ])
 def test_mid_shapes(T, d, F, seed):
     _full_check(synth.make_inputs(T, d, F, seed, name=f"mid{T}x{d}x{F}"))
