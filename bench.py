@@ -94,11 +94,14 @@ def peaks():
 #   profile_small_int8   T=2048, F=4096, int8 weights (0.6 GB) + bf16 scales
 #   profile_decode_small T=8,    F=8192, bf16 weights (2.4 GB), the decode kernels
 #   profile_decode_small_int8   the same with int8 weights (1.2 GB)
+#   profile_router       T=8192, F=512 (0.15 GB of weights): the router kernel at the
+#                        headline token count (8 tokens per CTA)
 PROFILE_CASES = {
     "profile_small": dict(T=2048, d=6144, F=4096, seed=2000, weight_dtype="bf16"),
     "profile_small_int8": dict(T=2048, d=6144, F=4096, seed=2001, weight_dtype="int8"),
     "profile_decode_small": dict(T=8, d=6144, F=8192, seed=2002, weight_dtype="bf16"),
     "profile_decode_small_int8": dict(T=8, d=6144, F=8192, seed=2003, weight_dtype="int8"),
+    "profile_router": dict(T=8192, d=6144, F=512, seed=2004, weight_dtype="bf16"),
 }
 
 

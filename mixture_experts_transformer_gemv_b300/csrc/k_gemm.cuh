@@ -47,7 +47,9 @@
 // Tile t maps to (expert, n-block, m-block) with the m-block fastest, so pairs
 // working at the same time share the same weight tile through L2.
 //
-// Every TMA box is 64 rows (8 KB of bf16): a CTA's 128 rows take two boxes.
+// A full tile's operands arrive as one 128-row TMA box per CTA and operand; a
+// half tile's A and its up-projection B halves (64 rows of W, 64 of Wv) as
+// 64-row boxes (a second set of tensor maps).
 //
 // int8 weights ("TevunahAi/Grok-1-BF16", "Conversion Details": int8 values
 // with bf16 scales, one per expert and output channel for the (8, 1, N) scale
@@ -80,7 +82,7 @@ namespace moe {
 
 constexpr int kGemmBM = 256;     // rows per full tile (pair)
 constexpr int kGemmHalfM = 128;  // rows per CTA of a full tile; rows of a half tile
-constexpr int kGemmBoxRows = 64; // rows of every TMA box of the GEMMs (A and B)
+constexpr int kGemmBoxRows = 64; // rows of the half tiles' TMA boxes
 constexpr int kGemmBN = 256;     // MMA N (accumulator columns)
 constexpr int kGemmHalfN = 128;  // B rows per CTA
 constexpr int kGemmBK = 64;      // K per stage (64 bf16 = one 128-byte swizzle row)
@@ -108,22 +110,28 @@ static_assert(kGemmBM == 2 * kRowPad, "an expert's row block is full tiles and a
 
 // Per weight type:
 //   bf16: a TMA ring of 6 stages, A 16 KB + B 16 KB each; 6 warps.
-//   int8: a TMA ring of 5 stages, A 16 KB + int8 B 8 KB each, and a ring of 6
+//   int8: a TMA ring of 5 stages, A 16 KB + int8 B 8 KB each, and a ring of 5
 //         converted fp16 B halves (16 KB each) between the converter warps and
-//         the MMA warp; 14 warps.  (Measured at the int8 workload, TMA + converted
-//         stages: 6 + 3 1030-1040 TFLOP/s, 5 + 6 1059-1072, 5 + 5 1064, 4 + 6
-//         1009, 3 + 6 883.  Loading the int8 weights into the converters'
-//         registers straight from global memory, two k-blocks ahead, instead of
-//         staging them by TMA: 660.)
+//         the MMA warp; 14 warps.  Both rings have the same depth, so k-block g
+//         uses TMA stage g % 5 and converted buffer g % 5, and one commit of the
+//         MMA issuer per k-block (to the stage's empty barrier, which the
+//         converters also wait on) frees both; a second commit per k-block cost
+//         8 %.  (Measured at the int8 workload, TMA + converted stages with two
+//         commits: 6 + 3 1030-1040 TFLOP/s, 5 + 6 1059-1072, 5 + 5 1064, 4 + 6
+//         1009, 3 + 6 883; 5 + 5 with one commit 1126-1144.  Loading the int8
+//         weights into the converters' registers straight from global memory,
+//         two k-blocks ahead, instead of staging them by TMA: 660.)
 template <bool WQ>
 struct GemmCfg {
   static constexpr int kStages = WQ ? 5 : 6;    // TMA ring
-  static constexpr int kBStages = WQ ? 6 : 0;   // converted-B ring
+  static constexpr int kBStages = WQ ? 5 : 0;   // converted-B ring (same depth: one release for both)
   static constexpr int kStageBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
   static constexpr int kStageBytesHalf = kATileBytes / 2 + (WQ ? kB8TileBytes : kBTileBytes);  // half tile
   static constexpr int kThreads = 32 * (kConvWarp0 + (WQ ? kConvWarps : 0));
-  // full, empty (TMA ring), bfull, bempty (converted ring), tmem_full x2, tmem_empty x2, drain
-  static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 5;
+  // full, empty (TMA ring; empty also frees the converted buffer of the same index),
+  // bfull (converted ring), tmem_full x2, tmem_empty x2, drain
+  static constexpr int kNumBars = 2 * kStages + kBStages + 5;
+  static_assert(!WQ || kBStages == kStages, "one release frees a TMA stage and its converted buffer");
   static constexpr size_t kSmemBytes =
       1024 + (size_t)kStages * kStageBytes + (size_t)kBStages * kBTileBytes + kNumBars * 8 + 16;
 };
@@ -210,7 +218,9 @@ __device__ __forceinline__ void load_scales8(const uint16_t* p, float (&s)[8]) {
 template <int EPI, bool WQ>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
-                        const __grid_constant__ CUtensorMap tm_b1, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_ah,
+                        const __grid_constant__ CUtensorMap tm_b0h, const __grid_constant__ CUtensorMap tm_b1h,
+                        const GemmParams p) {
   using C = GemmCfg<WQ>;
   extern __shared__ uint8_t smem_raw[];
   // The layout depends only on compile-time sizes, so the offsets are the same
@@ -228,8 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (C::kStages + s); };
   auto bfull_bar = [&](uint32_t j) { return bar0 + 8u * (2 * C::kStages + j); };
-  auto bempty_bar = [&](uint32_t j) { return bar0 + 8u * (2 * C::kStages + C::kBStages + j); };
-  const uint32_t bar_t = bar0 + 8u * (2 * C::kStages + 2 * C::kBStages);
+  const uint32_t bar_t = bar0 + 8u * (2 * C::kStages + C::kBStages);
   auto tfull_bar = [&](uint32_t a) { return bar_t + 8u * a; };
   auto tempty_bar = [&](uint32_t a) { return bar_t + 8u * (2 + a); };
   const uint32_t drain_bar = bar_t + 8u * 4;
@@ -255,7 +264,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
     }
     for (int j = 0; j < C::kBStages; ++j) {
       mbar_init(bfull_bar(j), 2);  // one arrival per CTA (after all its converter warps)
-      mbar_init(bempty_bar(j), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -268,7 +276,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b0);
-    if (EPI == kEpiGeglu) tma_prefetch_desc(&tm_b1);
+    tma_prefetch_desc(&tm_ah);
+    if (EPI == kEpiGeglu) {
+      tma_prefetch_desc(&tm_b1);
+      tma_prefetch_desc(&tm_b0h);
+      tma_prefetch_desc(&tm_b1h);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
@@ -291,24 +304,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
         // this CTA's A rows: 128 of a full tile, 64 of a half tile
         const int arow = tc.row0 + (int)rank * (tc.half ? kGemmBoxRows : kGemmHalfM);
-        // this CTA's 128 rows of B, as two boxes of 64 rows.  Up projection, full
-        // tile: 128 rows of W (even) or Wv (odd); half tile: the CTA's 64 rows of
-        // the n-block from W, then the same 64 rows from Wv.  Down projection:
-        // the first or second 128 output rows of W1.
+        // this CTA's 128 rows of B.  Up projection, full tile: 128 rows of W
+        // (even) or Wv (odd), one box; half tile: the CTA's 64 rows of the
+        // n-block from W, then the same 64 rows from Wv (two 64-row boxes).
+        // Down projection: the first or second 128 output rows of W1, one box.
         const int nrow = tc.e * p.b_rows_per_expert;
-        int brow0, brow1;
-        const CUtensorMap *bmap0 = &tm_b0, *bmap1 = &tm_b0;
-        if (EPI == kEpiGeglu && tc.half) {
-          brow0 = brow1 = nrow + tc.n_blk * kGemmHalfN + (int)rank * kGemmBoxRows;
-          bmap1 = &tm_b1;
-        } else if (EPI == kEpiGeglu) {
-          brow0 = nrow + tc.n_blk * kGemmHalfN;
-          brow1 = brow0 + kGemmBoxRows;
-          if (!leader) bmap0 = bmap1 = &tm_b1;
-        } else {
-          brow0 = nrow + tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
-          brow1 = brow0 + kGemmBoxRows;
-        }
+        const bool split_b = EPI == kEpiGeglu && tc.half;
+        const int brow = (EPI == kEpiGeglu) ? nrow + tc.n_blk * kGemmHalfN + (tc.half ? (int)rank * kGemmBoxRows : 0)
+                                            : nrow + tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
+        const CUtensorMap* bmap = (EPI == kEpiGeglu && !leader) ? &tm_b1 : &tm_b0;
         constexpr int kBBox = (WQ ? kB8TileBytes : kBTileBytes) / 2;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -318,11 +322,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, tc.half ? C::kStageBytesHalf : C::kStageBytes);
           const uint32_t sa = smem_addr(sA + stage * kATileBytes);
-          tma_load_2d(sa, &tm_a, fb, kb * kGemmBK, arow);
-          if (!tc.half) tma_load_2d(sa + kATileBytes / 2, &tm_a, fb, kb * kGemmBK, arow + kGemmBoxRows);
+          tma_load_2d(sa, tc.half ? &tm_ah : &tm_a, fb, kb * kGemmBK, arow);
           const uint32_t sb = smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes);
-          tma_load_2d(sb, bmap0, fb, kb * kGemmBK, brow0);
-          tma_load_2d(sb + kBBox, bmap1, fb, kb * kGemmBK, brow1);
+          if (split_b) {
+            tma_load_2d(sb, &tm_b0h, fb, kb * kGemmBK, brow);
+            tma_load_2d(sb + kBBox, &tm_b1h, fb, kb * kGemmBK, brow);
+          } else {
+            tma_load_2d(sb, bmap, fb, kb * kGemmBK, brow);
+          }
           for (int s = 0; s < C::kStages; ++s)
             if (s == (int)stage) issued[s] = (int)phase;
           if (++stage == (uint32_t)C::kStages) {
@@ -382,7 +389,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
             phase ^= 1u;
           }
           if (WQ) {
-            umma_commit_pair(bempty_bar(bstage), 0x3);
             if (++bstage == (uint32_t)C::kBStages) {
               bstage = 0;
               bphase ^= 1u;
@@ -557,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         const uint32_t stage = (uint32_t)(my % C::kStages), phase = (uint32_t)(my / C::kStages) & 1u;
         const uint32_t bstage = (uint32_t)(my % C::kBStages), bphase = (uint32_t)(my / C::kBStages) & 1u;
         const bool got = __all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns) &&
-                                                     wait_bounded(bempty_bar(bstage), bphase ^ 1u, abort_flag,
+                                                     wait_bounded(empty_bar(bstage), bphase ^ 1u, abort_flag,
                                                                   p.timeout_ns));
         if (got) {
           const uint8_t* src = sB8 + stage * kB8TileBytes;
@@ -618,7 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
     // exit: group 0 waits for the releases of the last uses of every buffer
     if (grp == 0)
       for (int j = max(0, gk - C::kBStages); j < gk && ok; ++j)
-        ok = __all_sync(0xffffffffu, wait_bounded(bempty_bar((uint32_t)(j % C::kBStages)),
+        ok = __all_sync(0xffffffffu, wait_bounded(empty_bar((uint32_t)(j % C::kBStages)),
                                                   (uint32_t)(j / C::kBStages) & 1u, abort_flag, p.timeout_ns));
     if (!ok && lane == 0) raise_abort(abort_flag, p.err);
   }

@@ -94,10 +94,11 @@ struct moe_layer {
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
-  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w64{}, tm_wv64{}, tm_w1_64{};  // grouped GEMMs: boxes of 64 rows x 64
-  CUtensorMap tm_w{}, tm_wv{}, tm_w1_128{};                           // decode path: boxes of 128 rows x 64
+  CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1_128{};  // boxes of 128 rows x 64
+  CUtensorMap tm_xn_perm64{}, tm_act64{}, tm_w64{}, tm_wv64{};       // grouped GEMMs' half tiles: 64 rows x 64
   CUtensorMap tm_xn_perm16{}, tm_act16{};                             // decode path: 16-row boxes
-  CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes)
+  CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes of 128 rows)
+  CUtensorMap tm_w8h{}, tm_wv8h{};                      // int8 weights, half tiles (64 rows)
   CUtensorMap tm_w8d{}, tm_wv8d{}, tm_w18d{};           // int8 weights, 64-byte swizzle (decode)
 
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
@@ -248,10 +249,10 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     if (int8)
       grouped_gemm_kernel<kEpiGeglu, true><<<L->gemm_grid[kEpiGeglu][1], GemmCfg<true>::kThreads,
                                              GemmCfg<true>::kSmemBytes, st>>>(
-          L->tm_xn_perm, L->tm_w8, L->tm_wv8, p);
+          L->tm_xn_perm, L->tm_w8, L->tm_wv8, L->tm_xn_perm64, L->tm_w8h, L->tm_wv8h, p);
     else
       grouped_gemm_kernel<kEpiGeglu, false><<<L->gemm_grid[kEpiGeglu][0], kGemmThreads, kGemmSmemBytes, st>>>(
-          L->tm_xn_perm, L->tm_w64, L->tm_wv64, p);
+          L->tm_xn_perm, L->tm_w, L->tm_wv, L->tm_xn_perm64, L->tm_w64, L->tm_wv64, p);
   }
   mark(4);
   if (decode && int8) {
@@ -303,10 +304,10 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.timeout_ns = kWaitLimitNs;
     if (int8)
       grouped_gemm_kernel<kEpiDown, true><<<L->gemm_grid[kEpiDown][1], GemmCfg<true>::kThreads,
-                                            GemmCfg<true>::kSmemBytes, st>>>(L->tm_act, L->tm_w18, L->tm_w18, p);
+                                            GemmCfg<true>::kSmemBytes, st>>>(L->tm_act, L->tm_w18, L->tm_w18, L->tm_act64, L->tm_w18, L->tm_w18, p);
     else
       grouped_gemm_kernel<kEpiDown, false><<<L->gemm_grid[kEpiDown][0], kGemmThreads, kGemmSmemBytes, st>>>(
-          L->tm_act, L->tm_w1_64, L->tm_w1_64, p);
+          L->tm_act, L->tm_w1_128, L->tm_w1_128, L->tm_act64, L->tm_w1_128, L->tm_w1_128, p);
   }
   mark(5);
   {
@@ -459,8 +460,10 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   while (L->ksplit_i8 > 1 && (F / kDq8BK) % L->ksplit_i8) L->ksplit_i8 /= 2;
   moe_status_t s = MOE_OK;
   if (cudaMemset(L->ws, 0, total) != cudaSuccess) s = fail(MOE_ERR_CUDA, "workspace memset failed");
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmBoxRows);
-  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmBoxRows);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm, L->xn_perm, d, R, kGemmHalfM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act, L->act, F, R, kGemmHalfM);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm64, L->xn_perm, d, R, kGemmBoxRows);
+  if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act64, L->act, F, R, kGemmBoxRows);
   if (c.weight_dtype == MOE_WEIGHT_BF16) {
     static_assert(kGemmHalfN == kDecBM, "the GEMM and decode paths share the 128-row weight boxes");
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w, w->w, d, kNumExperts * F, kGemmHalfN);
@@ -468,11 +471,12 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_128, w->w1, F, kNumExperts * d, kGemmHalfN);
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w64, w->w, d, kNumExperts * F, kGemmBoxRows);
     if (s == MOE_OK) s = make_tmap_bf16(&L->tm_wv64, w->wv, d, kNumExperts * F, kGemmBoxRows);
-    if (s == MOE_OK) s = make_tmap_bf16(&L->tm_w1_64, w->w1, F, kNumExperts * d, kGemmBoxRows);
   } else {
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmBoxRows, kGemmBK);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmBoxRows, kGemmBK);
-    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmBoxRows, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8, w->w, d, kNumExperts * F, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8, w->wv, d, kNumExperts * F, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w18, w->w1, F, kNumExperts * d, kGemmHalfN, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8h, w->w, d, kNumExperts * F, kGemmBoxRows, kGemmBK);
+    if (s == MOE_OK) s = make_tmap_i8(&L->tm_wv8h, w->wv, d, kNumExperts * F, kGemmBoxRows, kGemmBK);
     if (s == MOE_OK) s = make_tmap_i8(&L->tm_w8d, w->w, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == MOE_OK)
       s = make_tmap_i8(&L->tm_wv8d, w->wv, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
