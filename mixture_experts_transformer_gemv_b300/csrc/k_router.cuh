@@ -10,8 +10,11 @@
 //   p      = softmax(l)                      (max-subtracted, fp32)
 //   i0, i1 = two largest p, ties to the lower index; weights p_i0, p_i1
 //
-// One CTA of 256 threads handles kRouterTok tokens (8 for large T at d <= 7168,
-// fewer for wider rows, 1 for small T, where more CTAs hide latency better).
+// Two kernels compute this.  For T >= 8 x SMs with a gate that fits shared
+// memory (d <= 7136), router_persistent_kernel: one CTA per SM holds the gate
+// and walks groups of 4 tokens.  Otherwise router_kernel: one CTA of 256
+// threads handles kRouterTok tokens (8 for large T at d <= 7168, fewer for wider
+// rows, 1 for small T, where more CTAs hide latency better).
 // Its x rows are copied once into shared memory (cp.async, 16 bytes per copy)
 // and both passes read them there, so every x byte crosses HBM once.  Every
 // gate value the CTA loads feeds all of its tokens (the gate is [8, d] fp32
@@ -33,6 +36,53 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// softmax + top-2 of one token's 8 logits (gate bias included in l): writes
+// the routing outputs of token t and leaves the probabilities in p.
+__device__ __forceinline__ void softmax_top2(const float (&l)[kNumExperts], int t, int32_t* __restrict__ idx_out,
+                                             float* __restrict__ prob_out, int32_t* __restrict__ user_idx,
+                                             float* __restrict__ user_prob, float (&p)[kNumExperts]) {
+  float mx = l[0];
+#pragma unroll
+  for (int e = 1; e < kNumExperts; ++e) mx = fmaxf(mx, l[e]);
+  float Z = 0.f;
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) {
+    p[e] = expf(l[e] - mx);
+    Z += p[e];
+  }
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) p[e] = p[e] / Z;
+  // strict '>' keeps the lower index on ties
+  int i0 = 0;
+  float b0 = p[0];
+#pragma unroll
+  for (int e = 1; e < kNumExperts; ++e)
+    if (p[e] > b0) {
+      b0 = p[e];
+      i0 = e;
+    }
+  int i1 = -1;
+  float b1 = -1.f;
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e)
+    if (e != i0 && p[e] > b1) {
+      b1 = p[e];
+      i1 = e;
+    }
+  idx_out[2 * t] = i0;
+  idx_out[2 * t + 1] = i1;
+  prob_out[2 * t] = b0;
+  prob_out[2 * t + 1] = b1;
+  if (user_idx) {
+    user_idx[2 * t] = i0;
+    user_idx[2 * t + 1] = i1;
+  }
+  if (user_prob) {
+    user_prob[2 * t] = b0;
+    user_prob[2 * t + 1] = b1;
+  }
 }
 
 template <int kRouterTok>
@@ -170,53 +220,14 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
   // ---- softmax + top-2, one thread per token
   if (threadIdx.x < ntok) {
     const int i = threadIdx.x, t = t0 + i;
-    float l[kNumExperts];
+    float l[kNumExperts], p[kNumExperts];
 #pragma unroll
     for (int e = 0; e < kNumExperts; ++e) {
       float s = 0.f;
       for (int w = 0; w < kRouterThreads / 32; ++w) s += red[w][i * kNumExperts + e];
       l[e] = s + (gate_bias ? gate_bias[e] : 0.f);
     }
-    float mx = l[0];
-#pragma unroll
-    for (int e = 1; e < kNumExperts; ++e) mx = fmaxf(mx, l[e]);
-    float p[kNumExperts], Z = 0.f;
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) {
-      p[e] = expf(l[e] - mx);
-      Z += p[e];
-    }
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) p[e] = p[e] / Z;
-    // strict '>' keeps the lower index on ties
-    int i0 = 0;
-    float b0 = p[0];
-#pragma unroll
-    for (int e = 1; e < kNumExperts; ++e)
-      if (p[e] > b0) {
-        b0 = p[e];
-        i0 = e;
-      }
-    int i1 = -1;
-    float b1 = -1.f;
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e)
-      if (e != i0 && p[e] > b1) {
-        b1 = p[e];
-        i1 = e;
-      }
-    idx_out[2 * t] = i0;
-    idx_out[2 * t + 1] = i1;
-    prob_out[2 * t] = b0;
-    prob_out[2 * t + 1] = b1;
-    if (user_idx) {
-      user_idx[2 * t] = i0;
-      user_idx[2 * t + 1] = i1;
-    }
-    if (user_prob) {
-      user_prob[2 * t] = b0;
-      user_prob[2 * t + 1] = b1;
-    }
+    softmax_top2(l, t, idx_out, prob_out, user_idx, user_prob, p);
 #pragma unroll
     for (int e = 0; e < kNumExperts; ++e) s_p[i][e] = p[e];
   } else if (threadIdx.x < kRouterTok) {
@@ -231,6 +242,186 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
 #pragma unroll
     for (int i = 0; i < kRouterTok; ++i) s += s_p[i][threadIdx.x];
     p_part[blockIdx.x * kNumExperts + threadIdx.x] = s;
+  }
+}
+
+// Persistent router for large T: one CTA per SM copies the gate [8, d] fp32 into
+// shared memory once and walks groups of kRouterPTok tokens (group g =
+// blockIdx.x, blockIdx.x + gridDim.x, ...), each token's x chunks read once
+// into registers.  A thread owns the same 16-byte chunks of d (c = tid + 256 k)
+// for every token, and every sum runs in the same order as in router_kernel
+// (over the thread's chunks, then the lanes of the warp, then the warps), so
+// xn, the logits and the routing are the same bit for bit; only the gate no
+// longer streams from L2 once per CTA of 8 tokens, and the next group's rows
+// are loaded while the current group is computed.
+constexpr int kRouterPTok = 4;
+
+template <int CH>  // 16-byte chunks of d per thread: d <= 2048 CH
+__global__ void __launch_bounds__(kRouterThreads, 1) router_persistent_kernel(
+    const __nv_bfloat16* __restrict__ x, int T, int d, const float* __restrict__ gate,
+    const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
+    __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
+    int32_t* __restrict__ user_idx, float* __restrict__ user_prob, float* __restrict__ p_part) {
+  extern __shared__ __align__(16) uint8_t router_smem[];  // gate [8][d] fp32
+  __shared__ float red[kRouterThreads / 32][kRouterPTok * kNumExperts];
+  __shared__ float rnorm[kRouterPTok];
+  __shared__ float s_p[kRouterPTok][kNumExperts];
+  const float* gsm = reinterpret_cast<const float*>(router_smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = d >> 3;
+  for (int i = threadIdx.x; i < 2 * d; i += kRouterThreads)  // 8 d floats = 2 d chunks of 16 bytes
+    cp_async16(smem_addr(router_smem) + (uint32_t)i * 16u, gate + (size_t)i * 4);
+  cp_async_wait_all();
+  __syncthreads();
+
+  const int ngroups = (T + kRouterPTok - 1) / kRouterPTok;
+  // this thread's x chunks of group g (zeros past T or d)
+  auto load_group = [&](int g, uint4 (&v)[kRouterPTok][CH]) {
+    const int nt = min(kRouterPTok, T - g * kRouterPTok);
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i)
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        const int c = threadIdx.x + k * kRouterThreads;
+        v[i][k] = (i < nt && c < nchunk) ? ld_nc_v4(x + (size_t)(g * kRouterPTok + i) * d + c * 8)
+                                         : make_uint4(0, 0, 0, 0);
+      }
+  };
+  // the next group's rows are loaded while this group is computed
+  uint4 xnext[kRouterPTok][CH];
+  if (blockIdx.x < ngroups) load_group(blockIdx.x, xnext);
+  for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
+    const int t0 = grp * kRouterPTok;
+    const int ntok = min(kRouterPTok, T - t0);
+    uint4 xv[kRouterPTok][CH];
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i)
+#pragma unroll
+      for (int k = 0; k < CH; ++k) xv[i][k] = xnext[i][k];
+    if (grp + (int)gridDim.x < ngroups) load_group(grp + gridDim.x, xnext);
+    // ---- sum of squares per token
+    float ss[kRouterPTok];
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i) ss[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      if (threadIdx.x + k * kRouterThreads < nchunk) {
+#pragma unroll
+        for (int i = 0; i < kRouterPTok; ++i) {
+          if (i < ntok) {
+            const uint32_t w[4] = {xv[i][k].x, xv[i][k].y, xv[i][k].z, xv[i][k].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
+              ss[i] = fmaf(a, a, ss[i]);
+              ss[i] = fmaf(b, b, ss[i]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+      if (lane == 0) red[warp][i] = ss[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < kRouterPTok) {
+      float sum = 0.f;
+      for (int w = 0; w < kRouterThreads / 32; ++w) sum += red[w][threadIdx.x];
+      rnorm[threadIdx.x] = 1.0f / sqrtf(sum / (float)d + eps);
+    }
+    __syncthreads();
+    float r[kRouterPTok];
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i) r[i] = rnorm[i];
+
+    // ---- xn (bf16 copy out) and the 8 logits of every token
+    float lg[kRouterPTok][kNumExperts];
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i)
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) lg[i][e] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const int c = threadIdx.x + k * kRouterThreads;
+      if (c < nchunk) {
+        const float4 sa = *reinterpret_cast<const float4*>(s_pre + c * 8);
+        const float4 sb = *reinterpret_cast<const float4*>(s_pre + c * 8 + 4);
+        const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+        float xn[kRouterPTok][8];
+#pragma unroll
+        for (int i = 0; i < kRouterPTok; ++i) {
+          const uint32_t w[4] = {xv[i][k].x, xv[i][k].y, xv[i][k].z, xv[i][k].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            xn[i][2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
+            xn[i][2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
+          }
+          if (i < ntok) {
+            uint4 o;
+            o.x = pack_bf16x2(xn[i][0], xn[i][1]);
+            o.y = pack_bf16x2(xn[i][2], xn[i][3]);
+            o.z = pack_bf16x2(xn[i][4], xn[i][5]);
+            o.w = pack_bf16x2(xn[i][6], xn[i][7]);
+            *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < kNumExperts; ++e) {
+          const float4 ga = *reinterpret_cast<const float4*>(gsm + (size_t)e * d + c * 8);
+          const float4 gb = *reinterpret_cast<const float4*>(gsm + (size_t)e * d + c * 8 + 4);
+          const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+          for (int i = 0; i < kRouterPTok; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xn[i][j], g[j], lg[i][e]);
+        }
+      }
+    }
+    // ---- block reduction of the partial logits, then softmax + top-2 per token
+#pragma unroll
+    for (int i = 0; i < kRouterPTok; ++i)
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) {
+        float v = lg[i][e];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        lg[i][e] = v;
+      }
+    __syncthreads();  // red[] is reused
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kRouterPTok; ++i)
+#pragma unroll
+        for (int e = 0; e < kNumExperts; ++e) red[warp][i * kNumExperts + e] = lg[i][e];
+    }
+    __syncthreads();
+    if (threadIdx.x < ntok) {
+      const int i = threadIdx.x;
+      float l[kNumExperts], pr[kNumExperts];
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) {
+        float sum = 0.f;
+        for (int w = 0; w < kRouterThreads / 32; ++w) sum += red[w][i * kNumExperts + e];
+        l[e] = sum + (gate_bias ? gate_bias[e] : 0.f);
+      }
+      softmax_top2(l, t0 + i, idx_out, prob_out, user_idx, user_prob, pr);
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) s_p[i][e] = pr[e];
+    } else if (threadIdx.x < kRouterPTok) {
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) s_p[threadIdx.x][e] = 0.f;
+    }
+    // this group's sum of the router probabilities, per expert, in token order
+    __syncthreads();
+    if (threadIdx.x < kNumExperts) {
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRouterPTok; ++i) sum += s_p[i][threadIdx.x];
+      p_part[grp * kNumExperts + threadIdx.x] = sum;
+    }
   }
 }
 

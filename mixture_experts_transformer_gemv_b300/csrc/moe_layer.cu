@@ -92,6 +92,7 @@ struct moe_layer {
   int last_router_ctas = 0; // router CTAs of that forward
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
+  int router_persistent_ch = 0;  // chunks per thread of the persistent router (0: not usable at this d)
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
   CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1_128{};  // boxes of 128 rows x 64
@@ -159,31 +160,51 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
   const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) || (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
   mark(0);
-  // tokens per router CTA: the most (8, 4 or 2) whose x rows fit the CTA's
-  // shared memory while there are enough CTAs to fill the GPU twice over, else 1
-  int rtok = 1;
-  for (int k = kRouterTokMax; k > 1; k /= 2)
-    if (T >= 2 * k * L->num_sms && (size_t)k * d * 2 <= (size_t)kRouterSmemMax) {
-      rtok = k;
-      break;
-    }
-  L->last_router_ctas = (T + rtok - 1) / rtok;
-  {
-    const size_t rsm = (size_t)rtok * d * 2;
+  // Large T with a gate that fits shared memory: the persistent router (one CTA
+  // per SM, the gate staged once, groups of 4 tokens).  Otherwise tokens per
+  // router CTA: the most (8, 4 or 2) whose x rows fit the CTA's shared memory
+  // while there are enough CTAs to fill the GPU twice over, else 1.
+  if (L->router_persistent_ch > 0 && T >= 8 * L->num_sms) {
+    const int groups = (T + kRouterPTok - 1) / kRouterPTok;
+    const int grid = std::min(groups, L->num_sms);
+    const size_t gsm = (size_t)kNumExperts * d * 4;
     const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
     auto launch = [&](auto kern) {
-      kern<<<L->last_router_ctas, kRouterThreads, rsm, st>>>(xh, T, d, L->w.gate, L->w.gate_bias,
-                                                             L->w.pre_norm_scale, L->cfg.eps, L->xn, L->idx,
-                                                             L->prob, topk_idx, topk_prob, L->p_part);
+      kern<<<grid, kRouterThreads, gsm, st>>>(xh, T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale, L->cfg.eps,
+                                              L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
     };
-    if (rtok == 8)
-      launch(router_kernel<8>);
-    else if (rtok == 4)
-      launch(router_kernel<4>);
-    else if (rtok == 2)
-      launch(router_kernel<2>);
-    else
-      launch(router_kernel<1>);
+    switch (L->router_persistent_ch) {
+      case 1: launch(router_persistent_kernel<1>); break;
+      case 2: launch(router_persistent_kernel<2>); break;
+      case 3: launch(router_persistent_kernel<3>); break;
+      default: launch(router_persistent_kernel<4>); break;
+    }
+    L->last_router_ctas = groups;  // one routing-statistics partial sum per group
+  } else {
+    int rtok = 1;
+    for (int k = kRouterTokMax; k > 1; k /= 2)
+      if (T >= 2 * k * L->num_sms && (size_t)k * d * 2 <= (size_t)kRouterSmemMax) {
+        rtok = k;
+        break;
+      }
+    L->last_router_ctas = (T + rtok - 1) / rtok;
+    {
+      const size_t rsm = (size_t)rtok * d * 2;
+      const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
+      auto launch = [&](auto kern) {
+        kern<<<L->last_router_ctas, kRouterThreads, rsm, st>>>(xh, T, d, L->w.gate, L->w.gate_bias,
+                                                               L->w.pre_norm_scale, L->cfg.eps, L->xn, L->idx,
+                                                               L->prob, topk_idx, topk_prob, L->p_part);
+      };
+      if (rtok == 8)
+        launch(router_kernel<8>);
+      else if (rtok == 4)
+        launch(router_kernel<4>);
+      else if (rtok == 2)
+        launch(router_kernel<2>);
+      else
+        launch(router_kernel<1>);
+    }
   }
   mark(1);
   permute_kernel<<<1, kPermuteThreads, 0, st>>>(L->idx, L->prob, T, L->sched, L->row_of_slot, L->token_of_row,
@@ -485,6 +506,19 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
+  {
+    // the persistent router holds the gate (32 d bytes) in shared memory: d <= 8192 and the gate must fit
+    const int ch = (int)((d / 8 + kRouterThreads - 1) / kRouterThreads);
+    const size_t gsm = (size_t)kNumExperts * d * 4;
+    if (ch <= 4 && gsm + 4096 <= (size_t)prop.sharedMemPerBlockOptin) {
+      const void* pk[4] = {(const void*)router_persistent_kernel<1>, (const void*)router_persistent_kernel<2>,
+                           (const void*)router_persistent_kernel<3>, (const void*)router_persistent_kernel<4>};
+      if (cudaFuncSetAttribute(pk[ch - 1], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm) == cudaSuccess)
+        L->router_persistent_ch = ch;
+      else
+        cudaGetLastError();
+    }
+  }
   {
     const void* rk[4] = {(const void*)router_kernel<1>, (const void*)router_kernel<2>, (const void*)router_kernel<4>,
                          (const void*)router_kernel<8>};

@@ -45,9 +45,27 @@ def test_tiny_workload_all_tokens():
     (2400, 256, 512, 37),    # 8 tokens per router CTA, ragged last CTA (2400 = 300 x 8)
     (1200, 7680, 256, 38),   # wide rows: 8 rows would not fit the router's shared memory, 4 do
     (600, 14464, 256, 39),   # wider still: 2 tokens per router CTA
+    (1300, 3072, 256, 40),   # persistent router (T >= 8 x SMs), 2 chunks of d per thread
+    (1200, 7040, 256, 41),   # persistent router, 4 chunks per thread (the widest gate it holds)
 ])
 def test_mid_shapes(T, d, F, seed):
     _full_check(synth.make_inputs(T, d, F, seed, name=f"mid{T}x{d}x{F}"))
+
+
+def test_persistent_router_matches_the_per_cta_router_bit_for_bit():
+    """T = 1184 = 8 x 148 takes the persistent router, T = 1183 the 2-token one;
+    both form every sum in the same order, so the first 1183 tokens route the same
+    to the last bit (expert pair and probabilities), as the kernels' comments say."""
+    inp = synth.make_inputs(1184, 256, 512, 43, name="router_pair")
+    layer = make_layer(inp)
+    x = bf16_tensor(inp.x)
+    _, idx_a, prob_a, _ = layer.forward(x, routing=True)
+    _, idx_b, prob_b, _ = layer.forward(x[:1183].contiguous(), routing=True)
+    torch.cuda.synchronize()
+    layer.sync_status()
+    assert torch.equal(idx_a[:1183], idx_b)
+    assert torch.equal(prob_a[:1183], prob_b)
+    layer.close()
 
 
 def test_skewed_bias_small():
