@@ -64,7 +64,9 @@ def kernel_function(role, inp):
                                                      "ptx_pair.cuh", "ptx_tmem.cuh", "common.cuh"]
         if inp.T <= DECODE_MAX_T:
             return f"decode_gemm_kernel<{epi}>", ["k_decode.cuh", "ptx.cuh", "common.cuh"]
-        return f"grouped_gemm_kernel<{epi}, {int(int8)}>", ["k_gemm.cuh", "ptx.cuh", "common.cuh"]
+        # the down projections run two m-blocks per tile (third template argument)
+        return f"grouped_gemm_kernel<{epi}, {int(int8)}, {1 if epi == 0 else 2}>", ["k_gemm.cuh", "ptx.cuh",
+                                                                                  "common.cuh"]
     src = {"router": "k_router.cuh", "permute": "k_permute.cuh", "gather": "k_permute.cuh",
            "combine": "k_combine.cuh"}[role]
     name = {"router": "router_kernel", "permute": "permute_kernel", "gather": "gather_rows_kernel",
@@ -548,8 +550,8 @@ def run_attn(args, rank, world, local_rank):
         roof = hbm_roofline(amount / dur_s / 1e9, pk, peak_kind)
     roof["kernel"] = dom
     roof["algorithmic_per_launch"] = amount
-    roof["kernel_function"] = {"attn": "attn_kernel", "qkv": "grouped_gemm_kernel<1, 0>",
-                               "oproj": "grouped_gemm_kernel<1, 0>"}.get(dom, dom)
+    roof["kernel_function"] = {"attn": "attn_kernel", "qkv": "grouped_gemm_kernel<1, 0, 1>",
+                               "oproj": "grouped_gemm_kernel<1, 0, 1>"}.get(dom, dom)
     roof["traffic"] = attn_recorded_traffic(inp) if dom == "attn" else None
     roof["traffic_note"] = ("ncu DRAM bytes of the T=2048 capture scaled by compulsory bytes; the context rows "
                             "written stay in L2 when the kernel ends, so the figure sits below the compulsory bytes")

@@ -121,12 +121,16 @@ static_assert(kGemmBM == 2 * kRowPad, "an expert's row block is full tiles and a
 //         1009, 3 + 6 883; 5 + 5 with one commit 1126-1144.  Loading the int8
 //         weights into the converters' registers straight from global memory,
 //         two k-blocks ahead, instead of staging them by TMA: 660.)
-template <bool WQ>
+//   MB = 2 (down projections): every tile is two m-blocks of one expert against
+//         one n-block, accumulated in TMEM columns [0, 256) and [256, 512), so
+//         each B k-block (converted once for int8) feeds twice the MMA work; the
+//         long reduction (K = F) hides the epilogue no longer overlapping the
+//         next tile.  Rings of 4 stages (A 2 x 16 KB + B).
+template <bool WQ, int MB = 1>
 struct GemmCfg {
-  static constexpr int kStages = WQ ? 5 : 6;    // TMA ring
-  static constexpr int kBStages = WQ ? 5 : 0;   // converted-B ring (same depth: one release for both)
-  static constexpr int kStageBytes = kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // TMA bytes per stage
-  static constexpr int kStageBytesHalf = kATileBytes / 2 + (WQ ? kB8TileBytes : kBTileBytes);  // half tile
+  static constexpr int kStages = MB == 2 ? 4 : (WQ ? 5 : 6);  // TMA ring
+  static constexpr int kBStages = WQ ? kStages : 0;           // converted-B ring (same depth: one release for both)
+  static constexpr int kStageBytes = MB * kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // smem per stage
   static constexpr int kThreads = 32 * (kConvWarp0 + (WQ ? kConvWarps : 0));
   // full, empty (TMA ring; empty also frees the converted buffer of the same index),
   // bfull (converted ring), tmem_full x2, tmem_empty x2, drain
@@ -136,6 +140,7 @@ struct GemmCfg {
       1024 + (size_t)kStages * kStageBytes + (size_t)kBStages * kBTileBytes + kNumBars * 8 + 16;
 };
 constexpr int kGemmThreads = GemmCfg<false>::kThreads;
+constexpr int kGemmMBDown = 2;  // m-blocks per tile of the layer's down projections
 constexpr size_t kGemmSmemBytes = GemmCfg<false>::kSmemBytes;
 
 struct GemmParams {
@@ -157,34 +162,47 @@ struct GemmParams {
   uint64_t timeout_ns;           // limit of every wait
 };
 
+// A tile: MB consecutive m-blocks of one expert (the last tile of an expert
+// may hold fewer) against one n-block.  An m-block is 256 rows, or 128 (a half
+// tile) at the end of the expert's block.
+template <int MB>
 struct TileCoord {
-  int e, row0, n_blk;
-  bool half;  // 128 rows (M = 128 MMAs) instead of 256
+  int e, n_blk, nm;  // nm: m-blocks in this tile
+  int row0[MB];
+  bool half[MB];     // 128 rows (M = 128 MMAs) instead of 256
 };
 
-// m-blocks (full or half tiles) of the experts before e: mb[e] =
-// sum_{q < e} ceil((off[q + 1] - off[q]) / 256).
+// Tiles along m of the experts before e: mb[e] = sum_{q < e} ceil(m-blocks of q / MB),
+// m-blocks of q = ceil((off[q + 1] - off[q]) / 256).
+template <int MB>
 __device__ __forceinline__ void mblock_prefix(const int (&off)[kNumExperts + 1], int (&mb)[kNumExperts + 1]) {
   mb[0] = 0;
 #pragma unroll
-  for (int q = 0; q < kNumExperts; ++q) mb[q + 1] = mb[q] + (off[q + 1] - off[q] + kGemmBM - 1) / kGemmBM;
+  for (int q = 0; q < kNumExperts; ++q)
+    mb[q + 1] = mb[q] + ((off[q + 1] - off[q] + kGemmBM - 1) / kGemmBM + MB - 1) / MB;
 }
 
-// Tile t -> (expert, first row, n-block, half); tiles of expert e are
-// [mb[e] * n_tiles, mb[e + 1] * n_tiles), m-block fastest.
-__device__ __forceinline__ TileCoord decode_tile(int t, const int (&off)[kNumExperts + 1],
-                                                 const int (&mb)[kNumExperts + 1], int n_tiles) {
+// Tile t -> (expert, n-block, its m-blocks); tiles of expert e are
+// [mb[e] * n_tiles, mb[e + 1] * n_tiles), the m position fastest.
+template <int MB>
+__device__ __forceinline__ TileCoord<MB> decode_tile(int t, const int (&off)[kNumExperts + 1],
+                                                     const int (&mb)[kNumExperts + 1], int n_tiles) {
   int e = 0;
 #pragma unroll
   for (int q = 1; q < kNumExperts; ++q)
     if (t >= mb[q] * n_tiles) e = q;
   const int mt = mb[e + 1] - mb[e];
   const int local = t - mb[e] * n_tiles;
-  TileCoord c;
+  const int first = (local % mt) * MB;
+  TileCoord<MB> c;
   c.e = e;
   c.n_blk = local / mt;
-  c.row0 = off[e] + (local % mt) * kGemmBM;
-  c.half = off[e + 1] - c.row0 < kGemmBM;
+  c.nm = MB == 1 ? 1 : min(MB, (off[e + 1] - off[e] + kGemmBM - 1) / kGemmBM - first);
+#pragma unroll
+  for (int j = 0; j < MB; ++j) {
+    c.row0[j] = off[e] + (first + j) * kGemmBM;
+    c.half[j] = off[e + 1] - c.row0[j] < kGemmBM;
+  }
   return c;
 }
 
@@ -215,22 +233,23 @@ __device__ __forceinline__ void load_scales8(const uint16_t* p, float (&s)[8]) {
   s[4] = bf16_lo(v.z); s[5] = bf16_hi(v.z); s[6] = bf16_lo(v.w); s[7] = bf16_hi(v.w);
 }
 
-template <int EPI, bool WQ>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThreads, 1)
+template <int EPI, bool WQ, int MB = 1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_ah,
                         const __grid_constant__ CUtensorMap tm_b0h, const __grid_constant__ CUtensorMap tm_b1h,
                         const GemmParams p) {
-  using C = GemmCfg<WQ>;
+  using C = GemmCfg<WQ, MB>;
+  static_assert(MB == 1 || EPI == kEpiDown, "paired m-blocks only for the down projections");
   extern __shared__ uint8_t smem_raw[];
   // The layout depends only on compile-time sizes, so the offsets are the same
   // in both CTAs of the pair (the MMA relies on that).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // sA [6][128 x 64] bf16 | sB [6][128 x 64] bf16                      (bf16 weights)
-  // sA [6][128 x 64] bf16 | sB8 [6][128 x 64] int8 | sB [3][128 x 64] bf16  (int8 weights)
+  // sA [stages][MB][128 x 64] | sB [stages][128 x 64]                (bf16 weights)
+  // sA [stages][MB][128 x 64] | sB8 [stages][128 x 64] int8 | sB [stages][128 x 64] fp16  (int8 weights)
   uint8_t* sA = smem;
-  uint8_t* sB8 = sA + C::kStages * kATileBytes;
-  uint8_t* sB = WQ ? sB8 + C::kStages * kB8TileBytes : sA + C::kStages * kATileBytes;
+  uint8_t* sB8 = sA + C::kStages * MB * kATileBytes;
+  uint8_t* sB = WQ ? sB8 + C::kStages * kB8TileBytes : sA + C::kStages * MB * kATileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (WQ ? C::kBStages : C::kStages) * kBTileBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -251,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
   int off[kNumExperts + 1], mb[kNumExperts + 1];
 #pragma unroll
   for (int q = 0; q <= kNumExperts; ++q) off[q] = p.sched[kNumExperts + q];
-  mblock_prefix(off, mb);
+  mblock_prefix<MB>(off, mb);
   const int num_tiles = mb[kNumExperts] * p.n_tiles;
   const int kb_count = p.K / kGemmBK;
 
@@ -301,28 +320,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
-        // this CTA's A rows: 128 of a full tile, 64 of a half tile
-        const int arow = tc.row0 + (int)rank * (tc.half ? kGemmBoxRows : kGemmHalfM);
+        const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
         // this CTA's 128 rows of B.  Up projection, full tile: 128 rows of W
         // (even) or Wv (odd), one box; half tile: the CTA's 64 rows of the
         // n-block from W, then the same 64 rows from Wv (two 64-row boxes).
         // Down projection: the first or second 128 output rows of W1, one box.
         const int nrow = tc.e * p.b_rows_per_expert;
-        const bool split_b = EPI == kEpiGeglu && tc.half;
-        const int brow = (EPI == kEpiGeglu) ? nrow + tc.n_blk * kGemmHalfN + (tc.half ? (int)rank * kGemmBoxRows : 0)
+        const bool split_b = EPI == kEpiGeglu && tc.half[0];
+        const int brow = (EPI == kEpiGeglu) ? nrow + tc.n_blk * kGemmHalfN + (tc.half[0] ? (int)rank * kGemmBoxRows : 0)
                                             : nrow + tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
         const CUtensorMap* bmap = (EPI == kEpiGeglu && !leader) ? &tm_b1 : &tm_b0;
         constexpr int kBBox = (WQ ? kB8TileBytes : kBTileBytes) / 2;
+        // bytes per stage: each m-block's A rows (128 per CTA, 64 in a half tile) and B
+        uint32_t tx = WQ ? kB8TileBytes : kBTileBytes;
+#pragma unroll
+        for (int j = 0; j < MB; ++j)
+          if (j < tc.nm) tx += tc.half[j] ? kATileBytes / 2 : kATileBytes;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, tc.half ? C::kStageBytesHalf : C::kStageBytes);
-          const uint32_t sa = smem_addr(sA + stage * kATileBytes);
-          tma_load_2d(sa, tc.half ? &tm_ah : &tm_a, fb, kb * kGemmBK, arow);
+          mbar_arrive_expect_tx(fb, tx);
+#pragma unroll
+          for (int j = 0; j < MB; ++j)  // this CTA's A rows of each m-block: 128, or 64 of a half tile
+            if (j < tc.nm)
+              tma_load_2d(smem_addr(sA + (stage * MB + j) * kATileBytes), tc.half[j] ? &tm_ah : &tm_a, fb,
+                          kb * kGemmBK, tc.row0[j] + (int)rank * (tc.half[j] ? kGemmBoxRows : kGemmHalfM));
           const uint32_t sb = smem_addr(WQ ? sB8 + stage * kB8TileBytes : sB + stage * kBTileBytes);
           if (split_b) {
             tma_load_2d(sb, &tm_b0h, fb, kb * kGemmBK, brow);
@@ -362,15 +387,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const bool half = decode_tile(t, off, mb, p.n_tiles).half;
+        const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
         if (!wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * kGemmBN;
-        const uint32_t idesc = (WQ || p.f16_operands) ? (half ? kGemmIdescF16Half : kGemmIdescF16)
-                                                      : (half ? kGemmIdescHalf : kGemmIdesc);
+        uint32_t idesc[MB];
+#pragma unroll
+        for (int j = 0; j < MB; ++j)
+          idesc[j] = (WQ || p.f16_operands) ? (tc.half[j] ? kGemmIdescF16Half : kGemmIdescF16)
+                                            : (tc.half[j] ? kGemmIdescHalf : kGemmIdesc);
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded_cluster(full_bar(stage), phase, abort_flag, p.timeout_ns) ||
               (WQ && !wait_bounded_cluster(bfull_bar(bstage), bphase, abort_flag, p.timeout_ns))) {
@@ -378,11 +405,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
             break;
           }
           tc_fence_after_sync();
-          const uint64_t adesc = smem_desc_k_sw128(smem_addr(sA + stage * kATileBytes));
           const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sB + (WQ ? bstage : stage) * kBTileBytes));
 #pragma unroll
-          for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
-            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int j = 0; j < MB; ++j) {
+            if (j >= tc.nm) break;
+            // MB = 1: accumulator acc (two, alternating per tile); MB = 2: m-block j in TMEM columns [256 j, +256)
+            const uint32_t d_tmem = tmem_base + (MB == 2 ? (uint32_t)j : acc) * kGemmBN;
+            const uint64_t adesc = smem_desc_k_sw128(smem_addr(sA + (stage * MB + j) * kATileBytes));
+#pragma unroll
+            for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes along K inside the swizzle row
+              umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc[j], (kb | kk) != 0);
+          }
           umma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == (uint32_t)C::kStages) {
             stage = 0;
@@ -397,8 +430,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         }
         if (!ok) break;
         umma_commit_pair(tfull_bar(acc), 0x3);  // both CTAs' epilogues may read
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (MB == 2) {  // one set of accumulators (all 512 columns) per tile
+          acc_phase ^= 1u;
+        } else {
+          acc ^= 1u;
+          if (acc == 0) acc_phase ^= 1u;
+        }
       }
       // all MMAs issued by this thread are complete before TMEM is freed
       umma_commit_pair(drain_bar, 0x1);
@@ -433,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
     const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are reachable from this warp
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < num_tiles; t += num_pairs) {
-      const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
+      const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
       bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -441,17 +478,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         break;
       }
       tc_fence_after_sync();
+#pragma unroll
+      for (int jm = 0; jm < MB; ++jm) {
+      if (jm >= tc.nm) break;
       // Full tile: lane = row of the CTA's 128, all 256 accumulator columns.
       // Half tile: lane % 64 = row of the CTA's 64, lanes >= 64 hold accumulator
       // columns [128, 256) in TMEM columns [0, 128).
-      const int hsel = tc.half ? (q >> 1) : 0;
-      const int row = tc.half ? tc.row0 + (int)rank * kGemmBoxRows + (q & 1) * 32 + lane
-                              : tc.row0 + (int)rank * kGemmHalfM + q * 32 + lane;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kGemmBN;
+      const bool thalf = tc.half[jm];
+      const int hsel = thalf ? (q >> 1) : 0;
+      const int row = thalf ? tc.row0[jm] + (int)rank * kGemmBoxRows + (q & 1) * 32 + lane
+                            : tc.row0[jm] + (int)rank * kGemmHalfM + q * 32 + lane;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (MB == 2 ? (uint32_t)jm : acc) * kGemmBN;
       if (EPI == kEpiGeglu) {
         // full tile: channels n0 + [0, 128), h in TMEM columns [0, 128), v in [128, 256);
         // half tile: channels n0 + 64 hsel + [0, 64), h in [0, 64), v in [64, 128)
-        const int nch = tc.half ? kGemmHalfN / 2 : kGemmHalfN;
+        const int nch = thalf ? kGemmHalfN / 2 : kGemmHalfN;
         const int n0 = tc.n_blk * kGemmHalfN + hsel * (kGemmHalfN / 2);
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.n_out + n0;
         bool sat = false;  // int8 layers, device checks: an activation past the fp16 range
@@ -492,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         // full tile: output columns n_blk 256 + [0, 256); half tile: n_blk 256 + 128 hsel + [0, 128)
         float* orow = static_cast<float*>(p.out) + (size_t)row * p.n_out;
         const float ps = p.row_scale[row];
-        const int ncol = tc.half ? kGemmBN / 2 : kGemmBN;
+        const int ncol = thalf ? kGemmBN / 2 : kGemmBN;
 #pragma unroll 1
         for (int c = 0; c < ncol / 32; ++c) {
           const int col0 = tc.n_blk * kGemmBN + hsel * (kGemmBN / 2) + c * 32;
@@ -521,6 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
                                  __uint_as_float(y[4 * k + 3]) * sc[4 * k + 3]);
         }
       }
+      }  // m-blocks of the tile
       // this warp's TMEM reads are complete: free the accumulator for the MMA warp
       tc_fence_before_sync();
       __syncwarp();
@@ -530,8 +573,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
         else
           mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
       }
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      if (MB == 2) {
+        acc_phase ^= 1u;
+      } else {
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
     }
   } else if constexpr (WQ) {
     // -------------------------------------------------- int8 -> fp16 converter
@@ -551,11 +598,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ>::kThread
       // grouped scales (G > 1): staged B row r is weight row nb + r of the matrix
       // whose scales are gsc; in an up-projection half tile rows [64, 128) are
       // the same channels of Wv as rows [0, 64) of W
-      const TileCoord tc = decode_tile(t, off, mb, p.n_tiles);
-      const bool split_wv = EPI == kEpiGeglu && tc.half;
-      const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN + (tc.half ? (int)rank * kGemmBoxRows : 0)
+      const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
+      const bool split_wv = EPI == kEpiGeglu && tc.half[0];
+      const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN + (tc.half[0] ? (int)rank * kGemmBoxRows : 0)
                                         : tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
-      const uint16_t* gsc = (EPI == kEpiGeglu && !leader && !tc.half) ? p.scale1 : p.scale0;
+      const uint16_t* gsc = (EPI == kEpiGeglu && !leader && !tc.half[0]) ? p.scale1 : p.scale0;
       const size_t gsc_e = (size_t)(p.scale_experts > 1 ? tc.e : 0) * p.scale_groups;
       for (int kb = 0; kb < kb_count; ++kb) {
         const int my = gk++;

@@ -324,10 +324,13 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
     if (int8)
-      grouped_gemm_kernel<kEpiDown, true><<<L->gemm_grid[kEpiDown][1], GemmCfg<true>::kThreads,
-                                            GemmCfg<true>::kSmemBytes, st>>>(L->tm_act, L->tm_w18, L->tm_w18, L->tm_act64, L->tm_w18, L->tm_w18, p);
+      grouped_gemm_kernel<kEpiDown, true, kGemmMBDown>
+          <<<L->gemm_grid[kEpiDown][1], GemmCfg<true, kGemmMBDown>::kThreads, GemmCfg<true, kGemmMBDown>::kSmemBytes,
+             st>>>(L->tm_act, L->tm_w18, L->tm_w18, L->tm_act64, L->tm_w18, L->tm_w18, p);
     else
-      grouped_gemm_kernel<kEpiDown, false><<<L->gemm_grid[kEpiDown][0], kGemmThreads, kGemmSmemBytes, st>>>(
+      grouped_gemm_kernel<kEpiDown, false, kGemmMBDown>
+          <<<L->gemm_grid[kEpiDown][0], GemmCfg<false, kGemmMBDown>::kThreads, GemmCfg<false, kGemmMBDown>::kSmemBytes,
+             st>>>(
           L->tm_act, L->tm_w1_128, L->tm_w1_128, L->tm_act64, L->tm_w1_128, L->tm_w1_128, p);
   }
   mark(5);
@@ -424,7 +427,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (!(prop.major == 10 && prop.minor == 3))
     return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
   const size_t smem_need =
-      std::max(std::max(kGemmSmemBytes, GemmCfg<true>::kSmemBytes),
+      std::max(std::max(std::max(kGemmSmemBytes, GemmCfg<true>::kSmemBytes),
+                        std::max(GemmCfg<false, kGemmMBDown>::kSmemBytes, GemmCfg<true, kGemmMBDown>::kSmemBytes)),
                std::max(std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes),
                         std::max(DecI8Cfg<kEpiGeglu>::kSmemBytes, DecI8Cfg<kEpiDown>::kSmemBytes)));
   if (prop.sharedMemPerBlockOptin < smem_need)
@@ -533,16 +537,18 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
                            (int)kGemmSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (up GEMM) failed");
   if (s == MOE_OK &&
-      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kGemmSmemBytes) != cudaSuccess)
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, false, kGemmMBDown>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<false, kGemmMBDown>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (down GEMM) failed");
   if (s == MOE_OK &&
       cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)GemmCfg<true>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 up GEMM) failed");
   if (s == MOE_OK &&
-      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)GemmCfg<true>::kSmemBytes) != cudaSuccess)
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, true, kGemmMBDown>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<true, kGemmMBDown>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 down GEMM) failed");
   if (s == MOE_OK &&
       cudaFuncSetAttribute(decode_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -564,12 +570,14 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   // pairs as can be resident at once (whole clusters only), at most one per SM pair.
   if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, false>, kGemmThreads,
                                   kGemmSmemBytes, &L->gemm_grid[kEpiGeglu][0]);
-  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, false>, kGemmThreads,
-                                  kGemmSmemBytes, &L->gemm_grid[kEpiDown][0]);
+  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, false, kGemmMBDown>,
+                                  GemmCfg<false, kGemmMBDown>::kThreads, GemmCfg<false, kGemmMBDown>::kSmemBytes,
+                                  &L->gemm_grid[kEpiDown][0]);
   if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, true>, GemmCfg<true>::kThreads,
                                   GemmCfg<true>::kSmemBytes, &L->gemm_grid[kEpiGeglu][1]);
-  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, true>, GemmCfg<true>::kThreads,
-                                  GemmCfg<true>::kSmemBytes, &L->gemm_grid[kEpiDown][1]);
+  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, true, kGemmMBDown>,
+                                  GemmCfg<true, kGemmMBDown>::kThreads, GemmCfg<true, kGemmMBDown>::kSmemBytes,
+                                  &L->gemm_grid[kEpiDown][1]);
   if (s == MOE_OK) {
     L->ring.resize(kProfRing);
     L->pending.assign(kProfRing, false);
