@@ -64,9 +64,10 @@ def kernel_function(role, inp):
                                                      "ptx_pair.cuh", "ptx_tmem.cuh", "common.cuh"]
         if inp.T <= DECODE_MAX_T:
             return f"decode_gemm_kernel<{epi}>", ["k_decode.cuh", "ptx.cuh", "common.cuh"]
-        # the down projections run two m-blocks per tile (third template argument)
-        return f"grouped_gemm_kernel<{epi}, {int(int8)}, {1 if epi == 0 else 2}>", ["k_gemm.cuh", "ptx.cuh",
-                                                                                  "common.cuh"]
+        # with F >= PAIR_MIN_F and T >= PAIR_MIN_T the grouped GEMMs run two m-blocks per tile
+        # (third template argument)
+        mb = 2 if inp.F >= PAIR_MIN_F and inp.T >= PAIR_MIN_T else 1
+        return f"grouped_gemm_kernel<{epi}, {int(int8)}, {mb}>", ["k_gemm.cuh", "ptx.cuh", "common.cuh"]
     src = {"router": "k_router.cuh", "permute": "k_permute.cuh", "gather": "k_permute.cuh",
            "combine": "k_combine.cuh"}[role]
     name = {"router": "router_kernel", "permute": "permute_kernel", "gather": "gather_rows_kernel",
@@ -96,6 +97,9 @@ def peaks():
 #   profile_small_int8   T=2048, F=4096, int8 weights (0.6 GB) + bf16 scales
 #   profile_decode_small T=8,    F=8192, bf16 weights (2.4 GB), the decode kernels
 #   profile_decode_small_int8   the same with int8 weights (1.2 GB)
+#   profile_pair         T=2048, F=16384, bf16 weights (4.8 GB): the grouped GEMMs with
+#                        two m-blocks per tile (taken from F = 16384 on)
+#   profile_pair_int8    the same with int8 weights (2.4 GB)
 #   profile_router       T=8192, F=512 (0.15 GB of weights): the router kernel at the
 #                        headline token count (8 tokens per CTA)
 PROFILE_CASES = {
@@ -103,6 +107,8 @@ PROFILE_CASES = {
     "profile_small_int8": dict(T=2048, d=6144, F=4096, seed=2001, weight_dtype="int8"),
     "profile_decode_small": dict(T=8, d=6144, F=8192, seed=2002, weight_dtype="bf16"),
     "profile_decode_small_int8": dict(T=8, d=6144, F=8192, seed=2003, weight_dtype="int8"),
+    "profile_pair": dict(T=2048, d=6144, F=16384, seed=2005, weight_dtype="bf16"),
+    "profile_pair_int8": dict(T=2048, d=6144, F=16384, seed=2006, weight_dtype="int8"),
     "profile_router": dict(T=8192, d=6144, F=512, seed=2004, weight_dtype="bf16"),
 }
 
@@ -131,6 +137,7 @@ def config_block(inp):
 
 DECODE_MAX_T = 16  # the library's weight-streaming path takes T <= 16
 ROW_PAD = 128  # each expert's permuted rows are padded to a multiple of this
+PAIR_MIN_F, PAIR_MIN_T = 16384, 2048  # the library's grouped GEMMs pair m-blocks from these F and T on
 
 
 def algorithmic_work(inp, counts):
@@ -142,7 +149,8 @@ def algorithmic_work(inp, counts):
     S = 2 * T
     wb = 1 if inp.weight_dtype == "int8" else 2
     work = {
-        "router": ("hbm", T * d * 2 * 2 + 8 * d * 4 + T * 16),
+        # x read once; gate and s_pre; per token idx/prob (16 B), r (4 B), p (32 B)
+        "router": ("hbm", T * d * 2 + 9 * d * 4 + T * 52),
         "permute": ("hbm", S * 4 * 2 + S * 4 * 3),
         "gather": ("hbm", S * d * 2 * 2),
         "up_geglu": ("tensor", 2.0 * 2 * d * F * S),

@@ -223,7 +223,8 @@ moe_status_t moe_layer_set_profiling(moe_layer_t* layer, int32_t enable);
  * reset != 0 clears the sums afterwards. */
 moe_status_t moe_layer_profile_read(moe_layer_t* layer, double* ms_total, int64_t* launches, int32_t reset);
 
-/* Grid sizes (CTAs) of the grouped-GEMM launches this handle makes:
+/* Grid sizes (CTAs) of the grouped-GEMM launches this handle makes at large T
+ * (T >= 2048; with d_ffn >= 16384 those launches pair two m-blocks per tile):
  * grid[0] up / bf16, grid[1] down / bf16, grid[2] up / int8, grid[3] down / int8.
  * Each is twice the number of CTA pairs that can be resident at once. */
 moe_status_t moe_layer_gemm_grid(const moe_layer_t* layer, int32_t grid[4]);
@@ -234,11 +235,13 @@ int64_t moe_layer_launch_count(const moe_layer_t* layer);
 /* Workspace introspection (DEVICE pointers into the handle's workspace, valid
  * until destroy; contents are those of the last forward once it completed). */
 typedef struct {
-  void* xn;             /* [max_tokens, d] bf16: pre-norm output */
+  float* rnorm;         /* [max_tokens] fp32: 1 / rms of each token's hidden row (the pre-norm's
+                           scale; the normed rows themselves exist only in xn_perm) */
   int32_t* counts;      /* [E] tokens per expert */
   int32_t* row_offset;  /* [E + 1] first permuted row of each expert (multiples of 128) */
   int32_t* row_of_slot; /* [max_tokens, 2] permuted row of (token, rank) */
-  void* xn_perm;        /* [rows_cap, d] bf16 (fp16 for int8 weights): normed rows in expert order */
+  void* xn_perm;        /* [rows_cap, d] bf16 (fp16 for int8 weights): normed rows in expert order,
+                           (x_j r) s_pre_j rounded; zero rows for padding */
   void* act;            /* [rows_cap, F] bf16 (fp16 for int8 weights): GELU(h) * v per permuted row */
   float* y_rows;        /* [rows_cap, d] fp32: p * (W1 act) per permuted row */
   int64_t rows_cap;     /* capacity in permuted rows */
@@ -286,6 +289,16 @@ moe_status_t moe_group_slots_noalloc(const int32_t* topk_idx, const float* topk_
  * true or did not latch the error; MOE_ERR_CUDA on a CUDA error.  The GPU
  * context stays usable afterwards. */
 moe_status_t moe_selftest_bounded_wait(int32_t mode, uint64_t limit_ns, uint64_t* elapsed_ns);
+
+/* The GELU (tanh approximation; "TevunahAi/Grok-1-BF16" model card, "Grok-1
+ * Specific Behaviors": GeGLU experts) that the GeGLU epilogues of the up
+ * projections apply, evaluated elementwise: y[i] = GELU(x[i]) for i < n.
+ *   x, y    DEVICE float buffers of n elements (caller-owned; y may equal x)
+ *   n       >= 0; n = 0 launches nothing
+ *   stream  cudaStream_t (as void*), asynchronous
+ * Exists so the device GELU can be checked against a reference over a sweep of
+ * arguments.  MOE_ERR_INVALID_ARG for n < 0 or a null buffer with n > 0. */
+moe_status_t moe_selftest_gelu(const float* x, float* y, int64_t n, void* stream);
 
 #ifdef __cplusplus
 }

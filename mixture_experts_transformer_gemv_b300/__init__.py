@@ -56,7 +56,7 @@ class AttnWeights(ctypes.Structure):
 
 
 class WorkspaceView(ctypes.Structure):
-    _fields_ = [("xn", ctypes.c_void_p), ("counts", ctypes.c_void_p), ("row_offset", ctypes.c_void_p),
+    _fields_ = [("rnorm", ctypes.c_void_p), ("counts", ctypes.c_void_p), ("row_offset", ctypes.c_void_p),
                 ("row_of_slot", ctypes.c_void_p), ("xn_perm", ctypes.c_void_p), ("act", ctypes.c_void_p),
                 ("y_rows", ctypes.c_void_p), ("rows_cap", ctypes.c_int64)]
 
@@ -107,6 +107,8 @@ def lib():
         L.moe_group_slots_noalloc.argtypes = [vp, vp, i32, vp, vp, vp]
         L.moe_selftest_bounded_wait.restype = i32
         L.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)]
+        L.moe_selftest_gelu.restype = i32
+        L.moe_selftest_gelu.argtypes = [vp, vp, i64, vp]
         L.attn_block_create.restype = i32
         L.attn_block_create.argtypes = [ctypes.POINTER(AttnConfig), ctypes.POINTER(AttnWeights), ctypes.POINTER(vp)]
         L.attn_block_forward.restype = i32
@@ -150,6 +152,19 @@ def selftest_bounded_wait(mode: int, limit_s: float) -> tuple:
     el = ctypes.c_uint64(0)
     st = lib().moe_selftest_bounded_wait(int(mode), int(limit_s * 1e9), ctypes.byref(el))
     return st, el.value / 1e9
+
+
+def selftest_gelu(x, stream=None):
+    """moe_selftest_gelu: the device GELU of the GeGLU epilogues applied to a
+    contiguous float32 CUDA tensor; returns a new tensor."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_selftest_gelu(x.data_ptr(), y.data_ptr(), x.numel(), _stream_handle(stream)),
+               "moe_selftest_gelu")
+    return y
 
 
 def _ptr(t) -> Optional[int]:

@@ -359,6 +359,15 @@ moe_status_t moe_selftest_bounded_wait(int32_t mode, uint64_t limit_ns, uint64_t
   return fail(MOE_ERR_DEVICE_CHECK, "the wait gave up but did not latch the error word");
 }
 
+moe_status_t moe_selftest_gelu(const float* x, float* y, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return fail(MOE_ERR_INVALID_ARG, "x and y must be device buffers of n >= 0 floats");
+  if (n == 0) return ok();
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  selftest_gelu_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
 moe_status_t attn_block_set_profiling(attn_block_t* B, int32_t enable) {
   if (!B) return fail(MOE_ERR_INVALID_ARG, "null block");
   B->profiling = enable != 0;

@@ -64,10 +64,20 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return v;
 }
 
-// GELU, tanh approximation: 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3))).
+// GELU, tanh approximation: 0.5 u (1 + tanh(z)), z = sqrt(2/pi) (u + 0.044715 u^3).
+// Evaluated through the identity 0.5 (1 + tanh z) = 1 / (1 + e^(-2z)) as
+// u / (1 + 2^(-2 z log2 e)): one ex2 and one reciprocal on the special-function
+// unit instead of a tanh sequence, and no cancellation for negative u, where
+// 1 + tanh z is small.  The limits are exact: for z << 0 the power overflows to
+// +inf and the result is u * 0 = -0; for z >> 0 it underflows to 0 and the
+// result is u.
 __device__ __forceinline__ float gelu_tanh(float u) {
-  const float c = 0.7978845608028654f;
-  return 0.5f * u * (1.0f + tanhf(c * fmaf(0.044715f * u, u * u, u)));
+  constexpr float kNeg2CLog2e = -2.0f * 0.7978845608028654f * 1.4426950408889634f;  // -2 sqrt(2/pi) log2(e)
+  const float t = kNeg2CLog2e * fmaf(0.044715f * u, u * u, u);
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return u * r;
 }
 
 }  // namespace moe

@@ -32,7 +32,8 @@
 //   warps 6-13  int8 weights only: int8 -> fp16 conversion of the CTA's B half,
 //               two groups of four warps on alternate k-blocks
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap the
-// mainloop of tile i+1.
+// mainloop of tile i+1 (one m-block per tile); with two m-blocks per tile (MB = 2,
+// below) the two accumulators belong to one tile.
 //
 // Tiles never mix experts: expert e owns permuted rows [row_offset[e],
 // row_offset[e+1]), a multiple of 128.  Its rows are cut into full tiles of 256
@@ -121,11 +122,14 @@ static_assert(kGemmBM == 2 * kRowPad, "an expert's row block is full tiles and a
 //         1009, 3 + 6 883; 5 + 5 with one commit 1126-1144.  Loading the int8
 //         weights into the converters' registers straight from global memory,
 //         two k-blocks ahead, instead of staging them by TMA: 660.)
-//   MB = 2 (down projections): every tile is two m-blocks of one expert against
-//         one n-block, accumulated in TMEM columns [0, 256) and [256, 512), so
-//         each B k-block (converted once for int8) feeds twice the MMA work; the
-//         long reduction (K = F) hides the epilogue no longer overlapping the
-//         next tile.  Rings of 4 stages (A 2 x 16 KB + B).
+//   MB = 2 (paired m-blocks, taken by the layer for F >= 16384): every tile is
+//         two m-blocks of one expert against one n-block, accumulated in TMEM
+//         columns [0, 256) and [256, 512), so each B k-block (converted once for
+//         int8) feeds twice the MMA work and B crosses L2 half as often; the
+//         epilogue no longer overlaps the next tile.  In the up projection a half
+//         block stays a tile of its own (its B is staged differently); in the
+//         down projection it pairs with the full block before it.  Rings of 4
+//         stages (A 2 x 16 KB + B).
 template <bool WQ, int MB = 1>
 struct GemmCfg {
   static constexpr int kStages = MB == 2 ? 4 : (WQ ? 5 : 6);  // TMA ring
@@ -140,7 +144,7 @@ struct GemmCfg {
       1024 + (size_t)kStages * kStageBytes + (size_t)kBStages * kBTileBytes + kNumBars * 8 + 16;
 };
 constexpr int kGemmThreads = GemmCfg<false>::kThreads;
-constexpr int kGemmMBDown = 2;  // m-blocks per tile of the layer's down projections
+constexpr int kGemmMBPair = 2;  // m-blocks per tile of the layer's GEMMs when they pair m-blocks
 constexpr size_t kGemmSmemBytes = GemmCfg<false>::kSmemBytes;
 
 struct GemmParams {
@@ -172,19 +176,32 @@ struct TileCoord {
   bool half[MB];     // 128 rows (M = 128 MMAs) instead of 256
 };
 
-// Tiles along m of the experts before e: mb[e] = sum_{q < e} ceil(m-blocks of q / MB),
-// m-blocks of q = ceil((off[q + 1] - off[q]) / 256).
-template <int MB>
+// Tiles along m of one expert with `rows` padded rows (a multiple of 128): its
+// m-blocks are rows / 256 full ones and, when rows % 256 = 128, one half block.
+// MB = 1: one m-block per tile.  MB = 2 with PH (down projection): consecutive
+// m-blocks in pairs, the half block included.  MB = 2 without PH (up projection,
+// whose half tiles stage B differently): the full blocks in pairs, the half
+// block a tile of its own.
+template <int MB, bool PH>
+__device__ __forceinline__ int mtiles(int rows) {
+  const int nblk = (rows + kGemmBM - 1) / kGemmBM;
+  if (MB == 1) return nblk;
+  if (PH) return (nblk + 1) / 2;
+  const int nfull = rows / kGemmBM;
+  return (nfull + 1) / 2 + (nblk - nfull);
+}
+
+// Tiles along m of the experts before e: mb[e] = sum_{q < e} mtiles(rows of q).
+template <int MB, bool PH>
 __device__ __forceinline__ void mblock_prefix(const int (&off)[kNumExperts + 1], int (&mb)[kNumExperts + 1]) {
   mb[0] = 0;
 #pragma unroll
-  for (int q = 0; q < kNumExperts; ++q)
-    mb[q + 1] = mb[q] + ((off[q + 1] - off[q] + kGemmBM - 1) / kGemmBM + MB - 1) / MB;
+  for (int q = 0; q < kNumExperts; ++q) mb[q + 1] = mb[q] + mtiles<MB, PH>(off[q + 1] - off[q]);
 }
 
 // Tile t -> (expert, n-block, its m-blocks); tiles of expert e are
 // [mb[e] * n_tiles, mb[e + 1] * n_tiles), the m position fastest.
-template <int MB>
+template <int MB, bool PH>
 __device__ __forceinline__ TileCoord<MB> decode_tile(int t, const int (&off)[kNumExperts + 1],
                                                      const int (&mb)[kNumExperts + 1], int n_tiles) {
   int e = 0;
@@ -193,11 +210,22 @@ __device__ __forceinline__ TileCoord<MB> decode_tile(int t, const int (&off)[kNu
     if (t >= mb[q] * n_tiles) e = q;
   const int mt = mb[e + 1] - mb[e];
   const int local = t - mb[e] * n_tiles;
-  const int first = (local % mt) * MB;
+  const int rows = off[e + 1] - off[e];
+  const int nblk = (rows + kGemmBM - 1) / kGemmBM;
+  const int nfull = rows / kGemmBM;
+  const int i = local % mt;
+  // first m-block of the tile and how many it holds
+  int first = i * MB, nm = 1;
+  if (MB == 2 && PH) nm = min(2, nblk - first);
+  if (MB == 2 && !PH) {
+    const int npair = (nfull + 1) / 2;
+    nm = i < npair ? min(2, nfull - first) : 1;
+    if (i >= npair) first = nfull;
+  }
   TileCoord<MB> c;
   c.e = e;
   c.n_blk = local / mt;
-  c.nm = MB == 1 ? 1 : min(MB, (off[e + 1] - off[e] + kGemmBM - 1) / kGemmBM - first);
+  c.nm = nm;
 #pragma unroll
   for (int j = 0; j < MB; ++j) {
     c.row0[j] = off[e] + (first + j) * kGemmBM;
@@ -240,7 +268,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
                         const __grid_constant__ CUtensorMap tm_b0h, const __grid_constant__ CUtensorMap tm_b1h,
                         const GemmParams p) {
   using C = GemmCfg<WQ, MB>;
-  static_assert(MB == 1 || EPI == kEpiDown, "paired m-blocks only for the down projections");
+  // Paired m-blocks: a half block pairs with a full one only in the down
+  // projection (its half-tile B is staged like a full tile's).
+  constexpr bool PH = EPI == kEpiDown;
   extern __shared__ uint8_t smem_raw[];
   // The layout depends only on compile-time sizes, so the offsets are the same
   // in both CTAs of the pair (the MMA relies on that).
@@ -270,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
   int off[kNumExperts + 1], mb[kNumExperts + 1];
 #pragma unroll
   for (int q = 0; q <= kNumExperts; ++q) off[q] = p.sched[kNumExperts + q];
-  mblock_prefix<MB>(off, mb);
+  mblock_prefix<MB, PH>(off, mb);
   const int num_tiles = mb[kNumExperts] * p.n_tiles;
   const int kb_count = p.K / kGemmBK;
 
@@ -320,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
+        const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
         // this CTA's 128 rows of B.  Up projection, full tile: 128 rows of W
         // (even) or Wv (odd), one box; half tile: the CTA's 64 rows of the
         // n-block from W, then the same 64 rows from Wv (two 64-row boxes).
@@ -387,7 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
+        const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
         if (!wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
@@ -470,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
     const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are reachable from this warp
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < num_tiles; t += num_pairs) {
-      const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
+      const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
       bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -598,7 +628,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       // grouped scales (G > 1): staged B row r is weight row nb + r of the matrix
       // whose scales are gsc; in an up-projection half tile rows [64, 128) are
       // the same channels of Wv as rows [0, 64) of W
-      const TileCoord<MB> tc = decode_tile<MB>(t, off, mb, p.n_tiles);
+      const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
       const bool split_wv = EPI == kEpiGeglu && tc.half[0];
       const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN + (tc.half[0] ? (int)rank * kGemmBoxRows : 0)
                                         : tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;

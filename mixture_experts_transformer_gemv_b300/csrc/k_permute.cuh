@@ -13,7 +13,8 @@
 // row past rows_cap is not written; each case also sets kErrCheck in *err
 // unless err is null.
 // A single CTA does the scan (it is a few microseconds even at T = 65536);
-// the gather of the normed rows into expert order runs on all SMs.
+// the gather, which forms the normed rows and puts them in expert order, runs
+// on all SMs.
 #pragma once
 #include "common.cuh"
 
@@ -113,14 +114,19 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
   if (tid <= kNumExperts) sched[kNumExperts + tid] = s_off[tid];
 }
 
-// xn_perm[row] = xn[token_of_row[row]] (zeros for padding rows); rows beyond
-// row_offset[E] are left alone.  Grid-stride over rows, 16-byte accesses.
-// to_f16 != 0 (int8 weights) stores the rows as fp16 instead of bf16: every
-// bf16 value of a normed row converts exactly unless it is below the fp16
-// normal range (|v| < 2^-14), where the error is under 2^-24, or beyond its
-// largest value (|v| > 65504, stored as infinity; with checks != 0 this sets
+// xn_perm[row] = xn of token token_of_row[row], formed here from the hidden
+// row x, the token's r = 1 / rms (written by the router) and s_pre: the fp32
+// product (x_j r) s_pre_j rounded to bf16 ("TevunahAi/Grok-1-BF16", "Grok-1
+// Specific Behaviors": the pre-MoE RMSNorm); zeros for padding rows.  Rows
+// beyond row_offset[E] are left alone.  Grid-stride over rows, 16-byte
+// accesses.  to_f16 != 0 (int8 weights) stores the rows as fp16 instead of
+// bf16: every bf16 value converts exactly unless it is below the fp16 normal
+// range (|v| < 2^-14), where the error is under 2^-24, or beyond its largest
+// value (|v| > 65504, stored as infinity; with checks != 0 this sets
 // kErrSaturate in *err).
-__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ xn,
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const float* __restrict__ rnorm,
+                                                          const float* __restrict__ s_pre,
                                                           const int32_t* __restrict__ token_of_row,
                                                           const int32_t* __restrict__ sched, int d, int to_f16,
                                                           __nv_bfloat16* __restrict__ xn_perm, int checks,
@@ -131,9 +137,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
     const int tok = token_of_row[row];
     uint4* dst = reinterpret_cast<uint4*>(xn_perm + (size_t)row * d);
     if (tok >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(xn + (size_t)tok * d);
+      const float r = rnorm[tok];
+      const __nv_bfloat16* src = x + (size_t)tok * d;
       for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-        uint4 v = src[c];
+        const uint4 xv = ld_nc_v4(src + (size_t)c * 8);
+        const float4 sa = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)c * 8));
+        const float4 sb = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)c * 8 + 4));
+        uint4 v;
+        v.x = pack_bf16x2(bf16_lo(xv.x) * r * sa.x, bf16_hi(xv.x) * r * sa.y);
+        v.y = pack_bf16x2(bf16_lo(xv.y) * r * sa.z, bf16_hi(xv.y) * r * sa.w);
+        v.z = pack_bf16x2(bf16_lo(xv.z) * r * sb.x, bf16_hi(xv.z) * r * sb.y);
+        v.w = pack_bf16x2(bf16_lo(xv.w) * r * sb.z, bf16_hi(xv.w) * r * sb.w);
         if (to_f16) {
           if (checks) {
             const float m = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),

@@ -1,26 +1,32 @@
-// K1: pre-MoE RMSNorm + router logits + softmax + top-2, fused.
+// K1: pre-MoE RMSNorm statistics + router logits + softmax + top-2, fused, one
+// read of x.
 //
 // Per token t ("TevunahAi/Grok-1-BF16" model card, "Grok-1 Specific Behaviors":
 // pre-MoE norm; "Grok-1: 314B Total Parameters, 25B Active Per Token (MoE Explained)",
 // "Expert Routing Details": softmax of the gate logits, then top_k(k=2) of the
 // softmax outputs):
 //   r      = 1 / sqrt(mean_j x_j^2 + eps)
-//   xn_j   = x_j * r * s_pre_j               (fp32; written out rounded to bf16)
-//   l_e    = sum_j xn_j G[e, j] + b_e        (from the fp32 xn, not the bf16 copy)
+//   xn_j   = x_j r s_pre_j                   (the normed row)
+//   l_e    = sum_j xn_j G[e, j] + b_e  =  r sum_j x_j (s_pre_j G[e, j]) + b_e
 //   p      = softmax(l)                      (max-subtracted, fp32)
 //   i0, i1 = two largest p, ties to the lower index; weights p_i0, p_i1
 //
-// Two kernels compute this.  For T >= 8 x SMs with a gate that fits shared
-// memory (d <= 7136), router_persistent_kernel: one CTA per SM holds the gate
-// and walks groups of 4 tokens.  Otherwise router_kernel: one CTA of 256
-// threads handles kRouterTok tokens (8 for large T at d <= 7168, fewer for wider
-// rows, 1 for small T, where more CTAs hide latency better).
-// Its x rows are copied once into shared memory (cp.async, 16 bytes per copy)
-// and both passes read them there, so every x byte crosses HBM once.  Every
-// gate value the CTA loads feeds all of its tokens (the gate is [8, d] fp32
-// and is read from L2 once per CTA, not once per token); the experts are taken
-// four (at 8 tokens, two) at a time so the gate values, the normed chunk and the
-// 8 x kRouterTok partial logits fit in registers at two CTAs per SM.
+// One pass over x takes both sums, fp32: sum_j x_j^2 and the 8 sums
+// sum_j x_j gs[e, j] with gs = s_pre (.) G (each product rounded to fp32 once);
+// r scales the finished sums.  The kernel writes r (rnorm[t]), not the normed
+// row: the row gather forms xn from x, r and s_pre as it copies the rows into
+// expert order, so x crosses HBM once here and once there.
+//
+// Work split: a warp owns a contiguous run of tokens (the grid's warps split T
+// evenly) and takes them 4 at a time; lane l owns the 16-byte chunks
+// c = l + 32 k of d (8 elements each) and keeps kRouterDepth chunks of all 4
+// tokens in flight.  Only the warp reduces (shuffles over its lanes): no block
+// barrier after the set-up.  gs lives in shared memory ([8, d] fp32, written
+// once per CTA) when it fits (GSMEM); otherwise each use multiplies G and s_pre
+// from global memory (L2), with the same products.  Every token's sums run in
+// the same order whatever T, the grid or the token's position in the batch
+// (chunks in order per lane, then the lanes' xor butterfly), so a token routes
+// the same bit for bit in any batch.
 #pragma once
 #include "common.cuh"
 #include "ptx.cuh"
@@ -28,15 +34,9 @@
 namespace moe {
 
 constexpr int kRouterThreads = 256;
-constexpr int kRouterTokMax = 8;             // tokens per CTA for large T
-constexpr int kRouterSmemMax = 112 * 1024;   // staged x rows per CTA (two CTAs per SM)
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
+constexpr int kRouterWarps = kRouterThreads / 32;
+constexpr int kRouterWTok = 4;   // tokens a warp takes at a time
+constexpr int kRouterDepth = 3;  // chunks of x per lane in flight
 
 // softmax + top-2 of one token's 8 logits (gate bias included in l): writes
 // the routing outputs of token t and leaves the probabilities in p.
@@ -85,342 +85,144 @@ __device__ __forceinline__ void softmax_top2(const float (&l)[kNumExperts], int 
   }
 }
 
-template <int kRouterTok>
-__global__ void __launch_bounds__(kRouterThreads, 2) router_kernel(
-    const __nv_bfloat16* __restrict__ x, int T, int d, const float* __restrict__ gate,
-    const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
-    __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
-    int32_t* __restrict__ user_idx, float* __restrict__ user_prob, float* __restrict__ p_part) {
-  extern __shared__ __align__(16) uint8_t router_smem[];  // x rows [kRouterTok][d] bf16
-  __shared__ float red[kRouterThreads / 32][kRouterTok * kNumExperts];
-  __shared__ float rnorm[kRouterTok];
-  __shared__ float s_p[kRouterTok][kNumExperts];
-  const int t0 = blockIdx.x * kRouterTok;
-  const int ntok = min(kRouterTok, T - t0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nchunk = d >> 3;  // 8 bf16 per 16-byte chunk
-  const uint32_t xs = smem_addr(router_smem);
-  auto xchunk = [&](int i, int c) {
-    return *reinterpret_cast<const uint4*>(router_smem + ((size_t)i * d + (size_t)c * 8) * 2);
-  };
-
-  // ---- the CTA's x rows into shared memory, one read of HBM
-  for (int i = 0; i < ntok; ++i)
-    for (int c = threadIdx.x; c < nchunk; c += kRouterThreads)
-      cp_async16(xs + (uint32_t)(((size_t)i * d + (size_t)c * 8) * 2), x + (size_t)(t0 + i) * d + c * 8);
-  cp_async_wait_all();
-  __syncthreads();
-
-  // ---- pass 1: sum of squares per token
-  float ss[kRouterTok];
-#pragma unroll
-  for (int i = 0; i < kRouterTok; ++i) ss[i] = 0.f;
-  for (int c = threadIdx.x; c < nchunk; c += kRouterThreads) {
-#pragma unroll
-    for (int i = 0; i < kRouterTok; ++i) {
-      if (i < ntok) {
-        const uint4 v = xchunk(i, c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
-          ss[i] = fmaf(a, a, ss[i]);
-          ss[i] = fmaf(b, b, ss[i]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kRouterTok; ++i) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
-    if (lane == 0) red[warp][i] = ss[i];
-  }
-  __syncthreads();
-  if (threadIdx.x < kRouterTok) {
-    float s = 0.f;
-    for (int w = 0; w < kRouterThreads / 32; ++w) s += red[w][threadIdx.x];
-    rnorm[threadIdx.x] = 1.0f / sqrtf(s / (float)d + eps);
-  }
-  __syncthreads();
-  float r[kRouterTok];
-#pragma unroll
-  for (int i = 0; i < kRouterTok; ++i) r[i] = rnorm[i];
-
-  // ---- pass 2: xn (bf16 copy out) and the 8 logits of every token, experts
-  // in groups of four (two at 8 tokens per CTA); the normed chunk is recomputed
-  // from shared memory for every group: the same fp32 products
-  constexpr int kEPer = kRouterTok >= 8 ? 2 : 4;
-  float lg[kRouterTok][kNumExperts];
-#pragma unroll
-  for (int i = 0; i < kRouterTok; ++i)
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) lg[i][e] = 0.f;
-
-  for (int c = threadIdx.x; c < nchunk; c += kRouterThreads) {
-    const float4 sa = *reinterpret_cast<const float4*>(s_pre + c * 8);
-    const float4 sb = *reinterpret_cast<const float4*>(s_pre + c * 8 + 4);
-    const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-#pragma unroll
-    for (int h = 0; h < kNumExperts / kEPer; ++h) {
-      float g[kEPer][8];
-#pragma unroll
-      for (int e = 0; e < kEPer; ++e) {
-        const float4 ga = *reinterpret_cast<const float4*>(gate + (size_t)(kEPer * h + e) * d + c * 8);
-        const float4 gb = *reinterpret_cast<const float4*>(gate + (size_t)(kEPer * h + e) * d + c * 8 + 4);
-        g[e][0] = ga.x; g[e][1] = ga.y; g[e][2] = ga.z; g[e][3] = ga.w;
-        g[e][4] = gb.x; g[e][5] = gb.y; g[e][6] = gb.z; g[e][7] = gb.w;
-      }
-#pragma unroll
-      for (int i = 0; i < kRouterTok; ++i) {
-        if (i < ntok) {
-          const uint4 v = xchunk(i, c);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          float xn[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            xn[2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
-            xn[2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
-          }
-          if (h == 0) {
-            uint4 o;
-            o.x = pack_bf16x2(xn[0], xn[1]);
-            o.y = pack_bf16x2(xn[2], xn[3]);
-            o.z = pack_bf16x2(xn[4], xn[5]);
-            o.w = pack_bf16x2(xn[6], xn[7]);
-            *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
-          }
-#pragma unroll
-          for (int e = 0; e < kEPer; ++e)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) lg[i][kEPer * h + e] = fmaf(xn[j], g[e][j], lg[i][kEPer * h + e]);
-        }
-      }
-    }
-  }
-  // block reduction of the kRouterTok x 8 partial logits
-#pragma unroll
-  for (int i = 0; i < kRouterTok; ++i)
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) {
-      float v = lg[i][e];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      lg[i][e] = v;
-    }
-  __syncthreads();  // red[] is reused
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kRouterTok; ++i)
-#pragma unroll
-      for (int e = 0; e < kNumExperts; ++e) red[warp][i * kNumExperts + e] = lg[i][e];
-  }
-  __syncthreads();
-
-  // ---- softmax + top-2, one thread per token
-  if (threadIdx.x < ntok) {
-    const int i = threadIdx.x, t = t0 + i;
-    float l[kNumExperts], p[kNumExperts];
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) {
-      float s = 0.f;
-      for (int w = 0; w < kRouterThreads / 32; ++w) s += red[w][i * kNumExperts + e];
-      l[e] = s + (gate_bias ? gate_bias[e] : 0.f);
-    }
-    softmax_top2(l, t, idx_out, prob_out, user_idx, user_prob, p);
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) s_p[i][e] = p[e];
-  } else if (threadIdx.x < kRouterTok) {
-#pragma unroll
-    for (int e = 0; e < kNumExperts; ++e) s_p[threadIdx.x][e] = 0.f;
-  }
-  // this CTA's sum of the router probabilities, per expert, in token order
-  // (the routing diagnostics reduce these partial sums in block order)
-  __syncthreads();
-  if (threadIdx.x < kNumExperts) {
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < kRouterTok; ++i) s += s_p[i][threadIdx.x];
-    p_part[blockIdx.x * kNumExperts + threadIdx.x] = s;
-  }
+__device__ __forceinline__ void load4(const float* p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Persistent router for large T: one CTA per SM copies the gate [8, d] fp32 into
-// shared memory once and walks groups of kRouterPTok tokens (group g =
-// blockIdx.x, blockIdx.x + gridDim.x, ...), each token's x chunks read once
-// into registers.  A thread owns the same 16-byte chunks of d (c = tid + 256 k)
-// for every token, and every sum runs in the same order as in router_kernel
-// (over the thread's chunks, then the lanes of the warp, then the warps), so
-// xn, the logits and the routing are the same bit for bit; only the gate no
-// longer streams from L2 once per CTA of 8 tokens, and the next group's rows
-// are loaded while the current group is computed.
-constexpr int kRouterPTok = 4;
-
-template <int CH>  // 16-byte chunks of d per thread: d <= 2048 CH
-__global__ void __launch_bounds__(kRouterThreads, 1) router_persistent_kernel(
+// Outputs per token t: idx_out / prob_out [T, 2] (and the caller's copies when
+// given), rnorm_out[t] = r, p_part[t, e] = p_t,e (for the routing diagnostics).
+template <bool GSMEM>
+__global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(
     const __nv_bfloat16* __restrict__ x, int T, int d, const float* __restrict__ gate,
-    const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps,
-    __nv_bfloat16* __restrict__ xn_out, int32_t* __restrict__ idx_out, float* __restrict__ prob_out,
-    int32_t* __restrict__ user_idx, float* __restrict__ user_prob, float* __restrict__ p_part) {
-  extern __shared__ __align__(16) uint8_t router_smem[];  // gate [8][d] fp32
-  __shared__ float red[kRouterThreads / 32][kRouterPTok * kNumExperts];
-  __shared__ float rnorm[kRouterPTok];
-  __shared__ float s_p[kRouterPTok][kNumExperts];
-  const float* gsm = reinterpret_cast<const float*>(router_smem);
+    const float* __restrict__ gate_bias, const float* __restrict__ s_pre, float eps, float* __restrict__ rnorm_out,
+    int32_t* __restrict__ idx_out, float* __restrict__ prob_out, int32_t* __restrict__ user_idx,
+    float* __restrict__ user_prob, float* __restrict__ p_part) {
+  extern __shared__ __align__(16) uint8_t router_smem[];  // GSMEM: gs [8][d] fp32
+  float* gsm = reinterpret_cast<float*>(router_smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = d >> 3;
-  for (int i = threadIdx.x; i < 2 * d; i += kRouterThreads)  // 8 d floats = 2 d chunks of 16 bytes
-    cp_async16(smem_addr(router_smem) + (uint32_t)i * 16u, gate + (size_t)i * 4);
-  cp_async_wait_all();
-  __syncthreads();
-
-  const int ngroups = (T + kRouterPTok - 1) / kRouterPTok;
-  // this thread's x chunks of group g (zeros past T or d)
-  auto load_group = [&](int g, uint4 (&v)[kRouterPTok][CH]) {
-    const int nt = min(kRouterPTok, T - g * kRouterPTok);
+  if (GSMEM) {
+    // 8 d floats = 2 d float4, kRouterPre of them per thread in flight at once
+    constexpr int kRouterPre = 8;
+    for (int i0 = threadIdx.x; i0 < 2 * d; i0 += kRouterPre * kRouterThreads) {
+      float4 g[kRouterPre], sv[kRouterPre];
 #pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i)
-#pragma unroll
-      for (int k = 0; k < CH; ++k) {
-        const int c = threadIdx.x + k * kRouterThreads;
-        v[i][k] = (i < nt && c < nchunk) ? ld_nc_v4(x + (size_t)(g * kRouterPTok + i) * d + c * 8)
-                                         : make_uint4(0, 0, 0, 0);
-      }
-  };
-  // the next group's rows are loaded while this group is computed
-  uint4 xnext[kRouterPTok][CH];
-  if (blockIdx.x < ngroups) load_group(blockIdx.x, xnext);
-  for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
-    const int t0 = grp * kRouterPTok;
-    const int ntok = min(kRouterPTok, T - t0);
-    uint4 xv[kRouterPTok][CH];
-#pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i)
-#pragma unroll
-      for (int k = 0; k < CH; ++k) xv[i][k] = xnext[i][k];
-    if (grp + (int)gridDim.x < ngroups) load_group(grp + gridDim.x, xnext);
-    // ---- sum of squares per token
-    float ss[kRouterPTok];
-#pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i) ss[i] = 0.f;
-#pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      if (threadIdx.x + k * kRouterThreads < nchunk) {
-#pragma unroll
-        for (int i = 0; i < kRouterPTok; ++i) {
-          if (i < ntok) {
-            const uint32_t w[4] = {xv[i][k].x, xv[i][k].y, xv[i][k].z, xv[i][k].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
-              ss[i] = fmaf(a, a, ss[i]);
-              ss[i] = fmaf(b, b, ss[i]);
-            }
-          }
+      for (int u = 0; u < kRouterPre; ++u) {
+        const int i = i0 + u * kRouterThreads;
+        if (i < 2 * d) {
+          g[u] = __ldg(reinterpret_cast<const float4*>(gate) + i);
+          sv[u] = __ldg(reinterpret_cast<const float4*>(s_pre + (4 * i) % d));
         }
       }
-    }
 #pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
-      if (lane == 0) red[warp][i] = ss[i];
-    }
-    __syncthreads();
-    if (threadIdx.x < kRouterPTok) {
-      float sum = 0.f;
-      for (int w = 0; w < kRouterThreads / 32; ++w) sum += red[w][threadIdx.x];
-      rnorm[threadIdx.x] = 1.0f / sqrtf(sum / (float)d + eps);
+      for (int u = 0; u < kRouterPre; ++u) {
+        const int i = i0 + u * kRouterThreads;
+        if (i < 2 * d)
+          reinterpret_cast<float4*>(gsm)[i] =
+              make_float4(sv[u].x * g[u].x, sv[u].y * g[u].y, sv[u].z * g[u].z, sv[u].w * g[u].w);
+      }
     }
     __syncthreads();
-    float r[kRouterPTok];
+  }
+  const int nwarps = gridDim.x * kRouterWarps;
+  const int gw = blockIdx.x * kRouterWarps + warp;
+  const int lo = (int)((int64_t)gw * T / nwarps), hi = (int)((int64_t)(gw + 1) * T / nwarps);
+  const int nk = (nchunk + 31) / 32;  // chunk steps per lane
+  for (int t0 = lo; t0 < hi; t0 += kRouterWTok) {
+    const int nt = min(kRouterWTok, hi - t0);
+    // chunk k of the 4 tokens (zeros past the run or past d)
+    auto load = [&](int k, uint4 (&v)[kRouterWTok]) {
+      const int c = lane + 32 * k;
 #pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i) r[i] = rnorm[i];
-
-    // ---- xn (bf16 copy out) and the 8 logits of every token
-    float lg[kRouterPTok][kNumExperts];
+      for (int i = 0; i < kRouterWTok; ++i)
+        v[i] = (i < nt && c < nchunk) ? ld_nc_v4(x + (size_t)(t0 + i) * d + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
+    };
+    float ss[kRouterWTok], lg[kRouterWTok][kNumExperts];
 #pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i)
+    for (int i = 0; i < kRouterWTok; ++i) {
+      ss[i] = 0.f;
 #pragma unroll
       for (int e = 0; e < kNumExperts; ++e) lg[i][e] = 0.f;
+    }
+    uint4 buf[kRouterDepth][kRouterWTok];
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int c = threadIdx.x + k * kRouterThreads;
-      if (c < nchunk) {
-        const float4 sa = *reinterpret_cast<const float4*>(s_pre + c * 8);
-        const float4 sb = *reinterpret_cast<const float4*>(s_pre + c * 8 + 4);
-        const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-        float xn[kRouterPTok][8];
+    for (int q = 0; q < kRouterDepth; ++q) load(q, buf[q]);
+    for (int k0 = 0; k0 < nk; k0 += kRouterDepth) {
 #pragma unroll
-        for (int i = 0; i < kRouterPTok; ++i) {
-          const uint32_t w[4] = {xv[i][k].x, xv[i][k].y, xv[i][k].z, xv[i][k].w};
+      for (int q = 0; q < kRouterDepth; ++q) {
+        const int c = lane + 32 * (k0 + q);
+        if (c < nchunk) {
+          float xf[kRouterWTok][8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            xn[i][2 * q] = bf16_lo(w[q]) * r[i] * s8[2 * q];
-            xn[i][2 * q + 1] = bf16_hi(w[q]) * r[i] * s8[2 * q + 1];
+          for (int i = 0; i < kRouterWTok; ++i) {
+            const uint32_t w[4] = {buf[q][i].x, buf[q][i].y, buf[q][i].z, buf[q][i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              xf[i][2 * h] = bf16_lo(w[h]);
+              xf[i][2 * h + 1] = bf16_hi(w[h]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss[i] = fmaf(xf[i][j], xf[i][j], ss[i]);
           }
-          if (i < ntok) {
-            uint4 o;
-            o.x = pack_bf16x2(xn[i][0], xn[i][1]);
-            o.y = pack_bf16x2(xn[i][2], xn[i][3]);
-            o.z = pack_bf16x2(xn[i][4], xn[i][5]);
-            o.w = pack_bf16x2(xn[i][6], xn[i][7]);
-            *reinterpret_cast<uint4*>(xn_out + (size_t)(t0 + i) * d + c * 8) = o;
+          float s8[8];
+          if (!GSMEM) load4(s_pre + (size_t)c * 8, s8);
+#pragma unroll
+          for (int e = 0; e < kNumExperts; ++e) {
+            float g[8];
+            if (GSMEM) {
+              const float4 a = *reinterpret_cast<const float4*>(gsm + (size_t)e * d + (size_t)c * 8);
+              const float4 b = *reinterpret_cast<const float4*>(gsm + (size_t)e * d + (size_t)c * 8 + 4);
+              g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+              g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+            } else {
+              load4(gate + (size_t)e * d + (size_t)c * 8, g);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) g[j] = s8[j] * g[j];
+            }
+#pragma unroll
+            for (int i = 0; i < kRouterWTok; ++i)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xf[i][j], g[j], lg[i][e]);
           }
         }
-#pragma unroll
-        for (int e = 0; e < kNumExperts; ++e) {
-          const float4 ga = *reinterpret_cast<const float4*>(gsm + (size_t)e * d + c * 8);
-          const float4 gb = *reinterpret_cast<const float4*>(gsm + (size_t)e * d + c * 8 + 4);
-          const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-#pragma unroll
-          for (int i = 0; i < kRouterPTok; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xn[i][j], g[j], lg[i][e]);
-        }
+        load(k0 + q + kRouterDepth, buf[q]);
       }
     }
-    // ---- block reduction of the partial logits, then softmax + top-2 per token
+    // the warp's sums (every lane ends with all of them)
 #pragma unroll
-    for (int i = 0; i < kRouterPTok; ++i)
+    for (int i = 0; i < kRouterWTok; ++i) {
 #pragma unroll
-      for (int e = 0; e < kNumExperts; ++e) {
-        float v = lg[i][e];
+      for (int o = 16; o > 0; o >>= 1) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        lg[i][e] = v;
-      }
-    __syncthreads();  // red[] is reused
-    if (lane == 0) {
+      for (int e = 0; e < kNumExperts; ++e)
 #pragma unroll
-      for (int i = 0; i < kRouterPTok; ++i)
-#pragma unroll
-        for (int e = 0; e < kNumExperts; ++e) red[warp][i * kNumExperts + e] = lg[i][e];
+        for (int o = 16; o > 0; o >>= 1) lg[i][e] += __shfl_xor_sync(0xffffffffu, lg[i][e], o);
     }
-    __syncthreads();
-    if (threadIdx.x < ntok) {
-      const int i = threadIdx.x;
-      float l[kNumExperts], pr[kNumExperts];
+    // lane i finishes token t0 + i
+    float mss = ss[0], ml[kNumExperts];
 #pragma unroll
-      for (int e = 0; e < kNumExperts; ++e) {
-        float sum = 0.f;
-        for (int w = 0; w < kRouterThreads / 32; ++w) sum += red[w][i * kNumExperts + e];
-        l[e] = sum + (gate_bias ? gate_bias[e] : 0.f);
+    for (int e = 0; e < kNumExperts; ++e) ml[e] = lg[0][e];
+#pragma unroll
+    for (int i = 1; i < kRouterWTok; ++i)
+      if (lane == i) {
+        mss = ss[i];
+#pragma unroll
+        for (int e = 0; e < kNumExperts; ++e) ml[e] = lg[i][e];
       }
-      softmax_top2(l, t0 + i, idx_out, prob_out, user_idx, user_prob, pr);
+    if (lane < nt) {
+      const int t = t0 + lane;
+      const float r = 1.0f / sqrtf(mss / (float)d + eps);
+      float l[kNumExperts], p[kNumExperts];
 #pragma unroll
-      for (int e = 0; e < kNumExperts; ++e) s_p[i][e] = pr[e];
-    } else if (threadIdx.x < kRouterPTok) {
-#pragma unroll
-      for (int e = 0; e < kNumExperts; ++e) s_p[threadIdx.x][e] = 0.f;
-    }
-    // this group's sum of the router probabilities, per expert, in token order
-    __syncthreads();
-    if (threadIdx.x < kNumExperts) {
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < kRouterPTok; ++i) sum += s_p[i][threadIdx.x];
-      p_part[grp * kNumExperts + threadIdx.x] = sum;
+      for (int e = 0; e < kNumExperts; ++e) l[e] = r * ml[e] + (gate_bias ? gate_bias[e] : 0.f);
+      softmax_top2(l, t, idx_out, prob_out, user_idx, user_prob, p);
+      rnorm_out[t] = r;
+      float4* pp = reinterpret_cast<float4*>(p_part + (size_t)t * kNumExperts);
+      pp[0] = make_float4(p[0], p[1], p[2], p[3]);
+      pp[1] = make_float4(p[4], p[5], p[6], p[7]);
     }
   }
 }
@@ -431,7 +233,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_persistent_kernel(
 //   stats[e]  = (1/T) sum_t p_t,e                mean router probability of expert e
 //   stats[8]  = -sum_e stats[e] ln stats[e]      routing entropy, nats (max ln 8 = 2.079)
 //   stats[9]  = 1 - stats[8] / ln 8              collapse index (0 uniform, 1 one expert)
-// One CTA; warp e sums the per-CTA partial sums of expert e in a fixed order.
+// One CTA; warp e sums p_part[t, e] over the tokens in a fixed order.
 __global__ void __launch_bounds__(32 * kNumExperts) router_stats_kernel(const float* __restrict__ p_part,
                                                                        int n_part, int T, float* __restrict__ stats) {
   __shared__ float mean[kNumExperts];

@@ -1,6 +1,7 @@
-// Self-test of the library's bounded waits: one thread waits on an mbarrier
-// phase that nothing completes and must give up after its time limit (or at
-// once when the abort flag is already raised), leaving the GPU context usable.
+// Self-tests: the library's bounded waits (one thread waits on an mbarrier
+// phase that nothing completes and must give up after its time limit, or at
+// once when the abort flag is already raised, leaving the GPU context usable),
+// and the device GELU of the GeGLU epilogues evaluated on a buffer.
 #pragma once
 #include <cstdint>
 
@@ -32,6 +33,12 @@ __global__ void selftest_wait_kernel(int mode, uint64_t limit_ns, uint32_t* err,
   out[1] = global_timer_ns() - t0;
   out[0] = got ? 1u : 0u;
   if (!got) atomicOr(err, kErrTimeout);
+}
+
+// The GELU every GeGLU epilogue uses, elementwise: y[i] = gelu_tanh(x[i]).
+__global__ void selftest_gelu_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    y[i] = gelu_tanh(x[i]);
 }
 
 }  // namespace moe

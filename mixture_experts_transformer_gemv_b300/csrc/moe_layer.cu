@@ -65,6 +65,18 @@ moe_status_t make_tmap_i8(CUtensorMap* m, const void* base, uint64_t inner, uint
 
 constexpr int kProfRing = 64;
 
+// The grouped GEMMs pair two m-blocks per tile when F >= kPairMinF and
+// T >= kPairMinT.  Measured at F = 32768 and T >= 2048: faster (half the
+// weight-tile traffic, and for int8 half the conversions, per MMA, and less
+// power, so a higher clock under the cap).  At F = 4096 the paired kernels were
+// slower (up projection 22 %: few tiles of short mainloops, each epilogue
+// exposed), and at T <= 512 (at most one m-block per expert, so no pairs) the
+// up projection ran 14 % slower with the paired kernel's shallower ring and
+// un-overlapped epilogue.  T = 2048 gives each expert 512 rows on average: two
+// full m-blocks.
+constexpr int kPairMinF = 16384;
+constexpr int kPairMinT = 2048;
+
 }  // namespace
 
 struct moe_layer {
@@ -72,11 +84,11 @@ struct moe_layer {
   moe_weights_t w{};
   int device = 0;
   int num_sms = 0;
-  int gemm_grid[2][2] = {};  // [epilogue][int8]: CTAs of a grouped GEMM launch (whole resident pairs)
+  int gemm_grid[2][2][2] = {};  // [epilogue][int8][paired m-blocks]: CTAs of a grouped GEMM launch
   int64_t rows_cap = 0;
 
   void* ws = nullptr;
-  __nv_bfloat16* xn = nullptr;
+  float* rnorm = nullptr;  // [max_T] 1 / rms of each token's hidden row (router)
   int32_t* idx = nullptr;
   float* prob = nullptr;
   int32_t* sched = nullptr;
@@ -89,10 +101,10 @@ struct moe_layer {
   float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
   float* p_part = nullptr;  // [router CTAs (<= max_T)][E] per-router-CTA sums of p
   int last_T = 0;           // tokens of the last forward enqueued (routing diagnostics)
-  int last_router_ctas = 0; // router CTAs of that forward
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
-  int router_persistent_ch = 0;  // chunks per thread of the persistent router (0: not usable at this d)
+  bool router_gsmem = false;     // the router's scaled gate s_pre (.) G fits one CTA's shared memory
+  bool pair_mblocks = false;     // F >= kPairMinF: forwards with T >= kPairMinT pair two m-blocks per tile
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
   CUtensorMap tm_xn_perm{}, tm_act{}, tm_w{}, tm_wv{}, tm_w1_128{};  // boxes of 128 rows x 64
@@ -159,51 +171,25 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
 
   const bool int8 = L->cfg.weight_dtype == MOE_WEIGHT_INT8;
   const bool decode = (L->cfg.flags & MOE_FLAG_FORCE_GEMV) || (!(L->cfg.flags & MOE_FLAG_FORCE_TC) && T <= kDecNS);
+  const bool pair = L->pair_mblocks && T >= kPairMinT;  // grouped GEMMs: two m-blocks per tile
   mark(0);
-  // Large T with a gate that fits shared memory: the persistent router (one CTA
-  // per SM, the gate staged once, groups of 4 tokens).  Otherwise tokens per
-  // router CTA: the most (8, 4 or 2) whose x rows fit the CTA's shared memory
-  // while there are enough CTAs to fill the GPU twice over, else 1.
-  if (L->router_persistent_ch > 0 && T >= 8 * L->num_sms) {
-    const int groups = (T + kRouterPTok - 1) / kRouterPTok;
-    const int grid = std::min(groups, L->num_sms);
-    const size_t gsm = (size_t)kNumExperts * d * 4;
+  // Router: 8 warps per CTA, each warp a contiguous run of tokens.  With the
+  // scaled gate in shared memory: one CTA per SM at most (the gate is staged once
+  // per CTA), and one CTA per token below that, so small batches spread over as
+  // many SMs as they have tokens.  Otherwise the gate is read from L2 at every
+  // use, and the CTAs get 4 tokens per warp (fewer reads).
+  {
     const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
-    auto launch = [&](auto kern) {
-      kern<<<grid, kRouterThreads, gsm, st>>>(xh, T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale, L->cfg.eps,
-                                              L->xn, L->idx, L->prob, topk_idx, topk_prob, L->p_part);
-    };
-    switch (L->router_persistent_ch) {
-      case 1: launch(router_persistent_kernel<1>); break;
-      case 2: launch(router_persistent_kernel<2>); break;
-      case 3: launch(router_persistent_kernel<3>); break;
-      default: launch(router_persistent_kernel<4>); break;
-    }
-    L->last_router_ctas = groups;  // one routing-statistics partial sum per group
-  } else {
-    int rtok = 1;
-    for (int k = kRouterTokMax; k > 1; k /= 2)
-      if (T >= 2 * k * L->num_sms && (size_t)k * d * 2 <= (size_t)kRouterSmemMax) {
-        rtok = k;
-        break;
-      }
-    L->last_router_ctas = (T + rtok - 1) / rtok;
-    {
-      const size_t rsm = (size_t)rtok * d * 2;
-      const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
-      auto launch = [&](auto kern) {
-        kern<<<L->last_router_ctas, kRouterThreads, rsm, st>>>(xh, T, d, L->w.gate, L->w.gate_bias,
-                                                               L->w.pre_norm_scale, L->cfg.eps, L->xn, L->idx,
-                                                               L->prob, topk_idx, topk_prob, L->p_part);
-      };
-      if (rtok == 8)
-        launch(router_kernel<8>);
-      else if (rtok == 4)
-        launch(router_kernel<4>);
-      else if (rtok == 2)
-        launch(router_kernel<2>);
-      else
-        launch(router_kernel<1>);
+    if (L->router_gsmem) {
+      const int grid = std::min(L->num_sms, T);
+      router_kernel<true><<<grid, kRouterThreads, (size_t)kNumExperts * d * 4, st>>>(
+          xh, T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx, L->prob, topk_idx,
+          topk_prob, L->p_part);
+    } else {
+      const int grid = (int)((T + kRouterWarps * kRouterWTok - 1) / (kRouterWarps * kRouterWTok));
+      router_kernel<false><<<grid, kRouterThreads, 0, st>>>(xh, T, d, L->w.gate, L->w.gate_bias,
+                                                           L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx,
+                                                           L->prob, topk_idx, topk_prob, L->p_part);
     }
   }
   mark(1);
@@ -214,8 +200,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     const int grid = (int)std::min<int64_t>(L->rows_cap, (int64_t)L->num_sms * 8);
     // int8 layers multiply in fp16 (int8 -> fp16 is one shuffle and one
     // subtraction), so their activation rows are fp16
-    gather_rows_kernel<<<grid, 256, 0, st>>>(L->xn, L->token_of_row, L->sched, d, int8 ? 1 : 0, L->xn_perm,
-                                             checks, L->err);
+    gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(hidden), L->rnorm,
+                                             L->w.pre_norm_scale, L->token_of_row, L->sched, d, int8 ? 1 : 0,
+                                             L->xn_perm, checks, L->err);
   }
   mark(3);
   if (decode && int8) {
@@ -267,12 +254,21 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.checks = checks;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
-    if (int8)
-      grouped_gemm_kernel<kEpiGeglu, true><<<L->gemm_grid[kEpiGeglu][1], GemmCfg<true>::kThreads,
+    if (int8 && pair)
+      grouped_gemm_kernel<kEpiGeglu, true, kGemmMBPair>
+          <<<L->gemm_grid[kEpiGeglu][1][1], GemmCfg<true, kGemmMBPair>::kThreads, GemmCfg<true, kGemmMBPair>::kSmemBytes,
+             st>>>(L->tm_xn_perm, L->tm_w8, L->tm_wv8, L->tm_xn_perm64, L->tm_w8h, L->tm_wv8h, p);
+    else if (int8)
+      grouped_gemm_kernel<kEpiGeglu, true><<<L->gemm_grid[kEpiGeglu][1][0], GemmCfg<true>::kThreads,
                                              GemmCfg<true>::kSmemBytes, st>>>(
           L->tm_xn_perm, L->tm_w8, L->tm_wv8, L->tm_xn_perm64, L->tm_w8h, L->tm_wv8h, p);
+    else if (pair)
+      grouped_gemm_kernel<kEpiGeglu, false, kGemmMBPair>
+          <<<L->gemm_grid[kEpiGeglu][0][1], GemmCfg<false, kGemmMBPair>::kThreads,
+             GemmCfg<false, kGemmMBPair>::kSmemBytes, st>>>(L->tm_xn_perm, L->tm_w, L->tm_wv, L->tm_xn_perm64,
+                                                            L->tm_w64, L->tm_wv64, p);
     else
-      grouped_gemm_kernel<kEpiGeglu, false><<<L->gemm_grid[kEpiGeglu][0], kGemmThreads, kGemmSmemBytes, st>>>(
+      grouped_gemm_kernel<kEpiGeglu, false><<<L->gemm_grid[kEpiGeglu][0][0], kGemmThreads, kGemmSmemBytes, st>>>(
           L->tm_xn_perm, L->tm_w, L->tm_wv, L->tm_xn_perm64, L->tm_w64, L->tm_wv64, p);
   }
   mark(4);
@@ -323,13 +319,20 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.group_kb = F / L->cfg.scale_groups / kGemmBK;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
-    if (int8)
-      grouped_gemm_kernel<kEpiDown, true, kGemmMBDown>
-          <<<L->gemm_grid[kEpiDown][1], GemmCfg<true, kGemmMBDown>::kThreads, GemmCfg<true, kGemmMBDown>::kSmemBytes,
+    if (int8 && pair)
+      grouped_gemm_kernel<kEpiDown, true, kGemmMBPair>
+          <<<L->gemm_grid[kEpiDown][1][1], GemmCfg<true, kGemmMBPair>::kThreads, GemmCfg<true, kGemmMBPair>::kSmemBytes,
              st>>>(L->tm_act, L->tm_w18, L->tm_w18, L->tm_act64, L->tm_w18, L->tm_w18, p);
+    else if (int8)
+      grouped_gemm_kernel<kEpiDown, true><<<L->gemm_grid[kEpiDown][1][0], GemmCfg<true>::kThreads,
+                                            GemmCfg<true>::kSmemBytes, st>>>(L->tm_act, L->tm_w18, L->tm_w18,
+                                                                             L->tm_act64, L->tm_w18, L->tm_w18, p);
+    else if (!pair)
+      grouped_gemm_kernel<kEpiDown, false><<<L->gemm_grid[kEpiDown][0][0], kGemmThreads, kGemmSmemBytes, st>>>(
+          L->tm_act, L->tm_w1_128, L->tm_w1_128, L->tm_act64, L->tm_w1_128, L->tm_w1_128, p);
     else
-      grouped_gemm_kernel<kEpiDown, false, kGemmMBDown>
-          <<<L->gemm_grid[kEpiDown][0], GemmCfg<false, kGemmMBDown>::kThreads, GemmCfg<false, kGemmMBDown>::kSmemBytes,
+      grouped_gemm_kernel<kEpiDown, false, kGemmMBPair>
+          <<<L->gemm_grid[kEpiDown][0][1], GemmCfg<false, kGemmMBPair>::kThreads, GemmCfg<false, kGemmMBPair>::kSmemBytes,
              st>>>(
           L->tm_act, L->tm_w1_128, L->tm_w1_128, L->tm_act64, L->tm_w1_128, L->tm_w1_128, p);
   }
@@ -428,7 +431,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
   const size_t smem_need =
       std::max(std::max(std::max(kGemmSmemBytes, GemmCfg<true>::kSmemBytes),
-                        std::max(GemmCfg<false, kGemmMBDown>::kSmemBytes, GemmCfg<true, kGemmMBDown>::kSmemBytes)),
+                        std::max(GemmCfg<false, kGemmMBPair>::kSmemBytes, GemmCfg<true, kGemmMBPair>::kSmemBytes)),
                std::max(std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes),
                         std::max(DecI8Cfg<kEpiGeglu>::kSmemBytes, DecI8Cfg<kEpiDown>::kSmemBytes)));
   if (prop.sharedMemPerBlockOptin < smem_need)
@@ -449,7 +452,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
 
   // one workspace block, every buffer 1 KB aligned
   size_t offs[13], total = 0;
-  const size_t sizes[13] = {(size_t)(T * d * 2), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
+  const size_t sizes[13] = {(size_t)(T * 4), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
                             (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
                             (size_t)(R * F * 2), (size_t)(R * d * 4), 256,
                             (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4,
@@ -465,7 +468,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     return fail(MOE_ERR_OOM, "workspace of %zu bytes: %s", total, cudaGetErrorString(e));
   }
   char* b = static_cast<char*>(L->ws);
-  L->xn = reinterpret_cast<__nv_bfloat16*>(b + offs[0]);
+  L->rnorm = reinterpret_cast<float*>(b + offs[0]);
   L->idx = reinterpret_cast<int32_t*>(b + offs[1]);
   L->prob = reinterpret_cast<float*>(b + offs[2]);
   L->sched = reinterpret_cast<int32_t*>(b + offs[3]);
@@ -511,44 +514,51 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
   {
-    // the persistent router holds the gate (32 d bytes) in shared memory: d <= 8192 and the gate must fit
-    const int ch = (int)((d / 8 + kRouterThreads - 1) / kRouterThreads);
+    // the router keeps the scaled gate (32 d bytes) in shared memory where it fits
     const size_t gsm = (size_t)kNumExperts * d * 4;
-    if (ch <= 4 && gsm + 4096 <= (size_t)prop.sharedMemPerBlockOptin) {
-      const void* pk[4] = {(const void*)router_persistent_kernel<1>, (const void*)router_persistent_kernel<2>,
-                           (const void*)router_persistent_kernel<3>, (const void*)router_persistent_kernel<4>};
-      if (cudaFuncSetAttribute(pk[ch - 1], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm) == cudaSuccess)
-        L->router_persistent_ch = ch;
+    if (gsm + 1024 <= (size_t)prop.sharedMemPerBlockOptin) {
+      if (cudaFuncSetAttribute(router_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm) ==
+          cudaSuccess)
+        L->router_gsmem = true;
       else
         cudaGetLastError();
-    }
-  }
-  {
-    const void* rk[4] = {(const void*)router_kernel<1>, (const void*)router_kernel<2>, (const void*)router_kernel<4>,
-                         (const void*)router_kernel<8>};
-    for (int i = 0; i < 4 && s == MOE_OK; ++i) {
-      const size_t need = std::min<size_t>((size_t)(1 << i) * d * 2, (size_t)kRouterSmemMax);
-      if (cudaFuncSetAttribute(rk[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need) != cudaSuccess)
-        s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (router) failed");
     }
   }
   if (s == MOE_OK &&
       cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (up GEMM, one m-block per tile) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, false, kGemmMBPair>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<false, kGemmMBPair>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (up GEMM) failed");
   if (s == MOE_OK &&
-      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, false, kGemmMBDown>,
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, false, kGemmMBPair>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)GemmCfg<false, kGemmMBDown>::kSmemBytes) != cudaSuccess)
+                           (int)GemmCfg<false, kGemmMBPair>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (down GEMM) failed");
   if (s == MOE_OK &&
       cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)GemmCfg<true>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 up GEMM, one m-block per tile) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGeglu, true, kGemmMBPair>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<true, kGemmMBPair>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 up GEMM) failed");
   if (s == MOE_OK &&
-      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, true, kGemmMBDown>,
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kGemmSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (down GEMM, one m-block per tile) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)GemmCfg<true>::kSmemBytes) != cudaSuccess)
+    s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 down GEMM, one m-block per tile) failed");
+  if (s == MOE_OK &&
+      cudaFuncSetAttribute(grouped_gemm_kernel<kEpiDown, true, kGemmMBPair>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)GemmCfg<true, kGemmMBDown>::kSmemBytes) != cudaSuccess)
+                           (int)GemmCfg<true, kGemmMBPair>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 down GEMM) failed");
   if (s == MOE_OK &&
       cudaFuncSetAttribute(decode_gemm_kernel<kEpiGeglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -568,16 +578,31 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 decode down) failed");
   // Grouped GEMMs run one CTA pair per two SMs, persistent: launch as many
   // pairs as can be resident at once (whole clusters only), at most one per SM pair.
-  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, false>, kGemmThreads,
-                                  kGemmSmemBytes, &L->gemm_grid[kEpiGeglu][0]);
-  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, false, kGemmMBDown>,
-                                  GemmCfg<false, kGemmMBDown>::kThreads, GemmCfg<false, kGemmMBDown>::kSmemBytes,
-                                  &L->gemm_grid[kEpiDown][0]);
-  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiGeglu, true>, GemmCfg<true>::kThreads,
-                                  GemmCfg<true>::kSmemBytes, &L->gemm_grid[kEpiGeglu][1]);
-  if (s == MOE_OK) s = gemm_pairs(L, (const void*)grouped_gemm_kernel<kEpiDown, true, kGemmMBDown>,
-                                  GemmCfg<true, kGemmMBDown>::kThreads, GemmCfg<true, kGemmMBDown>::kSmemBytes,
-                                  &L->gemm_grid[kEpiDown][1]);
+  L->pair_mblocks = F >= kPairMinF;
+  {
+    struct {
+      const void* k;
+      int threads;
+      size_t smem;
+      int* grid;
+    } g[8] = {
+        {(const void*)grouped_gemm_kernel<kEpiGeglu, false>, kGemmThreads, kGemmSmemBytes, &L->gemm_grid[0][0][0]},
+        {(const void*)grouped_gemm_kernel<kEpiDown, false>, kGemmThreads, kGemmSmemBytes, &L->gemm_grid[1][0][0]},
+        {(const void*)grouped_gemm_kernel<kEpiGeglu, true>, GemmCfg<true>::kThreads, GemmCfg<true>::kSmemBytes,
+         &L->gemm_grid[0][1][0]},
+        {(const void*)grouped_gemm_kernel<kEpiDown, true>, GemmCfg<true>::kThreads, GemmCfg<true>::kSmemBytes,
+         &L->gemm_grid[1][1][0]},
+        {(const void*)grouped_gemm_kernel<kEpiGeglu, false, kGemmMBPair>, GemmCfg<false, kGemmMBPair>::kThreads,
+         GemmCfg<false, kGemmMBPair>::kSmemBytes, &L->gemm_grid[0][0][1]},
+        {(const void*)grouped_gemm_kernel<kEpiDown, false, kGemmMBPair>, GemmCfg<false, kGemmMBPair>::kThreads,
+         GemmCfg<false, kGemmMBPair>::kSmemBytes, &L->gemm_grid[1][0][1]},
+        {(const void*)grouped_gemm_kernel<kEpiGeglu, true, kGemmMBPair>, GemmCfg<true, kGemmMBPair>::kThreads,
+         GemmCfg<true, kGemmMBPair>::kSmemBytes, &L->gemm_grid[0][1][1]},
+        {(const void*)grouped_gemm_kernel<kEpiDown, true, kGemmMBPair>, GemmCfg<true, kGemmMBPair>::kThreads,
+         GemmCfg<true, kGemmMBPair>::kSmemBytes, &L->gemm_grid[1][1][1]},
+    };
+    for (int i = 0; i < 8 && s == MOE_OK; ++i) s = gemm_pairs(L, g[i].k, g[i].threads, g[i].smem, g[i].grid);
+  }
   if (s == MOE_OK) {
     L->ring.resize(kProfRing);
     L->pending.assign(kProfRing, false);
@@ -788,8 +813,8 @@ moe_status_t moe_layer_router_stats(moe_layer_t* L, float* stats, void* stream) 
   if (L->last_T < 1) return fail(MOE_ERR_INVALID_ARG, "no forward with T > 0 has been enqueued on this handle");
   DeviceGuard g(L->device);
   if (!g.ok) return fail(MOE_ERR_CUDA, "cannot select device %d", L->device);
-  router_stats_kernel<<<1, 32 * kNumExperts, 0, static_cast<cudaStream_t>(stream)>>>(L->p_part, L->last_router_ctas,
-                                                                                      L->last_T, stats);
+  router_stats_kernel<<<1, 32 * kNumExperts, 0, static_cast<cudaStream_t>(stream)>>>(L->p_part, L->last_T, L->last_T,
+                                                                                      stats);
   L->launches += 1;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -798,10 +823,11 @@ moe_status_t moe_layer_router_stats(moe_layer_t* L, float* stats, void* stream) 
 
 moe_status_t moe_layer_gemm_grid(const moe_layer_t* L, int32_t grid[4]) {
   if (!L || !grid) return fail(MOE_ERR_INVALID_ARG, "null argument");
-  grid[0] = L->gemm_grid[kEpiGeglu][0];
-  grid[1] = L->gemm_grid[kEpiDown][0];
-  grid[2] = L->gemm_grid[kEpiGeglu][1];
-  grid[3] = L->gemm_grid[kEpiDown][1];
+  const int pr = L->pair_mblocks ? 1 : 0;  // the kernels a forward with T >= kPairMinT launches
+  grid[0] = L->gemm_grid[kEpiGeglu][0][pr];
+  grid[1] = L->gemm_grid[kEpiDown][0][pr];
+  grid[2] = L->gemm_grid[kEpiGeglu][1][pr];
+  grid[3] = L->gemm_grid[kEpiDown][1][pr];
   return ok();
 }
 
@@ -809,7 +835,7 @@ int64_t moe_layer_launch_count(const moe_layer_t* L) { return L ? L->launches.lo
 
 moe_status_t moe_layer_workspace(const moe_layer_t* L, moe_workspace_view_t* v) {
   if (!L || !v) return fail(MOE_ERR_INVALID_ARG, "null argument");
-  v->xn = L->xn;
+  v->rnorm = L->rnorm;
   v->counts = L->sched;
   v->row_offset = L->sched + kNumExperts;
   v->row_of_slot = L->row_of_slot;

@@ -41,30 +41,38 @@ def test_tiny_workload_all_tokens():
     (1000, 256, 640, 32),    # two row blocks per expert, F/128 = 5
     (200, 384, 512, 33),     # d = 384: the last down-projection tile is half outside d
     (7, 256, 512, 34),       # fewer slots than a tile in every expert
-    (1500, 256, 512, 36),    # 4 tokens per router CTA (below the 8-token threshold of 2 x 8 x SMs)
-    (2400, 256, 512, 37),    # 8 tokens per router CTA, ragged last CTA (2400 = 300 x 8)
-    (1200, 7680, 256, 38),   # wide rows: 8 rows would not fit the router's shared memory, 4 do
-    (600, 14464, 256, 39),   # wider still: 2 tokens per router CTA
-    (1300, 3072, 256, 40),   # persistent router (T >= 8 x SMs), 2 chunks of d per thread
-    (1200, 7040, 256, 41),   # persistent router, 4 chunks per thread (the widest gate it holds)
+    (1500, 256, 512, 36),    # router: 148 CTAs, 1184 warps, runs of 1-2 tokens
+    (2400, 256, 512, 37),    # router: runs of 2-3 tokens per warp
+    (1200, 7680, 256, 38),   # wide rows: the scaled gate (8 x d fp32) exceeds shared memory, read from L2
+    (600, 14464, 256, 39),   # wider still, 57 chunks per lane (a ragged last step)
+    (1300, 3072, 256, 40),   # the gate in shared memory, 12 chunks per lane
+    (1200, 7040, 256, 41),   # near the widest gate shared memory holds (220 KB)
+    (2400, 256, 16384, 42),  # F >= 16384, T >= 2048: two m-blocks per tile; ~600 rows per expert = a
+                             # pair of full m-blocks and a half block alone
+    (2047, 256, 16384, 45),  # one token below the pairing threshold: one m-block per tile
 ])
 def test_mid_shapes(T, d, F, seed):
     _full_check(synth.make_inputs(T, d, F, seed, name=f"mid{T}x{d}x{F}"))
 
 
-def test_persistent_router_matches_the_per_cta_router_bit_for_bit():
-    """T = 1184 = 8 x 148 takes the persistent router, T = 1183 the 2-token one;
-    both form every sum in the same order, so the first 1183 tokens route the same
-    to the last bit (expert pair and probabilities), as the kernels' comments say."""
-    inp = synth.make_inputs(1184, 256, 512, 43, name="router_pair")
+@pytest.mark.parametrize("T,d,seed", [(1184, 256, 43), (40, 7680, 44)])
+def test_routing_does_not_depend_on_the_batch(T, d, seed):
+    """Every token's router sums run in the same order whatever the batch (the
+    warp that takes it, its position, T), with the gate in shared memory (d =
+    256) or read from L2 (d = 7680): a token routes the same to the last bit
+    (expert pair and probabilities) in the whole batch, in a prefix, in a suffix
+    and alone (T = 1, the decode path's size)."""
+    inp = synth.make_inputs(T, d, 256, seed, name=f"router_batch{T}x{d}")
     layer = make_layer(inp)
     x = bf16_tensor(inp.x)
     _, idx_a, prob_a, _ = layer.forward(x, routing=True)
-    _, idx_b, prob_b, _ = layer.forward(x[:1183].contiguous(), routing=True)
-    torch.cuda.synchronize()
+    idx_a, prob_a = idx_a.clone(), prob_a.clone()
+    for lo, hi in ((0, T - 1), (T - 37, T), (T // 2, T // 2 + 1)):
+        _, idx_b, prob_b, _ = layer.forward(x[lo:hi].contiguous(), routing=True)
+        torch.cuda.synchronize()
+        assert torch.equal(idx_a[lo:hi], idx_b), (lo, hi)
+        assert torch.equal(prob_a[lo:hi], prob_b), (lo, hi)
     layer.sync_status()
-    assert torch.equal(idx_a[:1183], idx_b)
-    assert torch.equal(prob_a[:1183], prob_b)
     layer.close()
 
 
@@ -187,14 +195,21 @@ def test_intermediates_match_oracle():
     ws = layer.workspace()
     R = ws.rows_cap
     T, d, F = inp.T, inp.d, inp.F
-    xn = read_device(ws.xn, (inp.T, d), torch.bfloat16)
+    rnorm = read_device(ws.rnorm, (inp.T,), torch.float32)
+    xn_perm = read_device(ws.xn_perm, (R, d), torch.bfloat16)
     counts = read_device(ws.counts, (8,), torch.int32)
     off = read_device(ws.row_offset, (9,), torch.int32)
     ros = read_device(ws.row_of_slot, (T, 2), torch.int32)
     act = read_device(ws.act, (R, F), torch.bfloat16)
     yr = read_device(ws.y_rows, (R, d), torch.float32)
     r = oracle.route(inp, keep_xn=True)
-    np.testing.assert_allclose(xn, r.xn, rtol=2 ** -8, atol=1e-6)
+    # the router's 1 / rms, and the normed rows the gather formed from it
+    xs = synth.bf16_bits_to_f32(inp.x).astype(np.float64)
+    np.testing.assert_allclose(rnorm, 1.0 / np.sqrt(np.mean(xs * xs, axis=1) + inp.eps), rtol=1e-5)
+    for k in range(2):
+        np.testing.assert_allclose(xn_perm[ros[:, k]], r.xn, rtol=2 ** -8, atol=1e-6)
+    pad = np.setdiff1d(np.arange(int(off[8])), ros.ravel())
+    assert pad.size == int(off[8]) - 2 * T and np.all(xn_perm[pad] == 0)
     np.testing.assert_array_equal(counts, np.bincount(r.idx.ravel(), minlength=8))
     # each expert's block is its slots padded to the next multiple of 128 rows
     assert off[0] == 0 and np.all(off % 128 == 0)
@@ -276,6 +291,16 @@ def test_int8_weights(T, d, F, seed):
     _full_check(inp)
 
 
+def test_int8_paired_mblocks_skewed():
+    """F >= 16384 and T >= 2048: two m-blocks per tile.  The skewed router gives
+    experts of 9.5, 4.5, 1.5 and 0.5 m-blocks: full pairs, a full block with a
+    half one in one down tile (alone in the up projection), lone half blocks;
+    ragged d (1.5 down n-blocks)."""
+    inp = synth.make_inputs(2400, 384, 16384, 80, name="int8_pair_skew", weight_dtype="int8",
+                            bias=synth.SKEW_BIAS)
+    _full_check(inp, flags=moe.MOE_FLAG_DEVICE_CHECKS)
+
+
 @pytest.mark.parametrize("T,d,F,seed", [
     (1, 256, 512, 76),
     (5, 384, 640, 77),      # ragged: d/128 = 3 weight blocks, F/64 = 10 -> 2-way split
@@ -334,6 +359,31 @@ def test_int8_fp16_saturation_is_reported(T):
     assert ei.value.status == moe.MOE_ERR_DEVICE_CHECK and "65504" in str(ei.value)
     layer.sync_status()  # cleared by the read
     layer.close()
+
+
+def test_device_gelu_matches_the_oracle():
+    """The GeGLU epilogues' GELU (evaluated as u / (1 + 2^(-2 z log2 e)), z the
+    tanh argument, on the ex2 and reciprocal instructions) against the oracle's
+    fp64 tanh form: a dense sweep of [-16, 16], both tails out to the fp32 range,
+    and +-0.  Bound: relative 2e-6 + 3e-7 |t|, t = 2 z log2 e the exponent (its
+    rounding error grows with |t|, and 2^t is flushed past |t| ~ 126); plus the
+    oracle's own cancellation in 1 + tanh z for u << 0 (2.3e-16 |u|) and 1e-37
+    where the device result is flushed to zero."""
+    import torch
+    xs = np.concatenate([np.linspace(-16.0, 16.0, 100001), -np.logspace(-30, 38, 400), np.logspace(-30, 38, 400),
+                         [0.0, -0.0]]).astype(np.float32)
+    y = moe.selftest_gelu(torch.from_numpy(xs).cuda()).cpu().numpy().astype(np.float64)
+    u = xs.astype(np.float64)
+    ref = np.array([oracle.gelu_tanh(float(v)) for v in u])
+    t = np.abs(2.0 * 0.7978845608028654 / np.log(2.0) * (u + 0.044715 * u ** 3))
+    bound = (2e-6 + 3e-7 * np.minimum(t, 128.0)) * np.abs(ref) + 2.3e-16 * np.abs(u) + 1e-37
+    err = np.abs(y - ref)
+    worst = int(np.argmax(err / bound))
+    assert np.all(err <= bound), f"u={u[worst]!r}: device {y[worst]!r} oracle {ref[worst]!r}"
+    assert np.all(np.isfinite(y))
+    assert y[-2] == 0.0 and y[-1] == 0.0
+    # the ends: GELU(u) = u for u >> 0, -0 for u << 0
+    assert y[np.argmax(u)] == u.max() and y[np.argmin(u)] == 0.0
 
 
 def test_int8_intermediates_match_oracle():
