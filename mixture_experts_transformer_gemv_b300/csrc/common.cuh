@@ -23,7 +23,11 @@ constexpr float kF16Max = 65504.f;
 //   [0, E)        counts[e]       slots routed to expert e
 //   [E, 2E + 1)   row_offset[e]   first permuted row of expert e (multiple of kRowPad);
 //                                 row_offset[E] = total padded rows
+//   [24, 26)      tile counters of the up and down grouped GEMMs (dynamic tile
+//                 schedule), zeroed by K2 before the GEMMs run
 constexpr int kSchedInts = 2 * kNumExperts + 1;
+constexpr int kSchedTileCtr = 24;
+static_assert(kSchedTileCtr >= kSchedInts && kSchedTileCtr + 2 <= 64, "the block is 256 bytes");
 
 // Epilogues of the expert GEMMs: GeGLU of the up projections, or the
 // combine-weight scaling of the down projection.

@@ -130,6 +130,10 @@ static_assert(kGemmBM == 2 * kRowPad, "an expert's row block is full tiles and a
 //         block stays a tile of its own (its B is staged differently); in the
 //         down projection it pairs with the full block before it.  Rings of 4
 //         stages (A 2 x 16 KB + B).
+// Dynamic tile schedule: slots of the ring through which the even CTA's
+// producer thread hands each tile index to every other role of the pair.
+constexpr int kTileRing = 8;
+
 template <bool WQ, int MB = 1>
 struct GemmCfg {
   static constexpr int kStages = MB == 2 ? 4 : (WQ ? 5 : 6);  // TMA ring
@@ -137,11 +141,16 @@ struct GemmCfg {
   static constexpr int kStageBytes = MB * kATileBytes + (WQ ? kB8TileBytes : kBTileBytes);  // smem per stage
   static constexpr int kThreads = 32 * (kConvWarp0 + (WQ ? kConvWarps : 0));
   // full, empty (TMA ring; empty also frees the converted buffer of the same index),
-  // bfull (converted ring), tmem_full x2, tmem_empty x2, drain
-  static constexpr int kNumBars = 2 * kStages + kBStages + 5;
+  // bfull (converted ring), tmem_full x2, tmem_empty x2, drain, tile ring fill / free
+  static constexpr int kNumBars = 2 * kStages + kBStages + 5 + 2 * kTileRing;
+  // readers of each tile-ring slot: even CTA MMA thread, epilogue warps,
+  // converter warps; odd CTA producer thread, forwarding thread (bf16),
+  // epilogue warps, converter warps
+  static constexpr int kTileReaders = 1 + kEpiWarps + (WQ ? kConvWarps : 0) + 1 + (WQ ? 0 : 1) + kEpiWarps +
+                                      (WQ ? kConvWarps : 0);
   static_assert(!WQ || kBStages == kStages, "one release frees a TMA stage and its converted buffer");
   static constexpr size_t kSmemBytes =
-      1024 + (size_t)kStages * kStageBytes + (size_t)kBStages * kBTileBytes + kNumBars * 8 + 16;
+      1024 + (size_t)kStages * kStageBytes + (size_t)kBStages * kBTileBytes + kNumBars * 8 + 16 + kTileRing * 4;
 };
 constexpr int kGemmThreads = GemmCfg<false>::kThreads;
 constexpr int kGemmMBPair = 2;  // m-blocks per tile of the layer's GEMMs when they pair m-blocks
@@ -162,6 +171,7 @@ struct GemmParams {
   int group_kb;                  // int8, G > 1: k-blocks of 64 per group
   int f16_operands;              // bf16 path: A and B hold fp16 instead of bf16 (both the same type)
   int checks;                    // int8 up projection: report activations past the fp16 range
+  int* tile_counter;             // dynamic tile schedule: a counter that is 0 at launch; nullptr: static
   uint32_t* err;                 // device error word
   uint64_t timeout_ns;           // limit of every wait
 };
@@ -283,6 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (WQ ? C::kBStages : C::kStages) * kBTileBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [kTileRing]
   const uint32_t bar0 = smem_addr(bars);
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (C::kStages + s); };
@@ -291,6 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
   auto tfull_bar = [&](uint32_t a) { return bar_t + 8u * a; };
   auto tempty_bar = [&](uint32_t a) { return bar_t + 8u * (2 + a); };
   const uint32_t drain_bar = bar_t + 8u * 4;
+  auto tfill_bar = [&](uint32_t i) { return bar_t + 8u * (5 + i); };
+  auto tfree_bar = [&](uint32_t i) { return bar_t + 8u * (5 + kTileRing + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its partner
@@ -319,6 +332,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       mbar_init(tempty_bar(a), 2 * kEpiWarps);  // one arrival per epilogue warp of either CTA
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(tfill_bar(i), 1);                  // the even CTA's scheduler
+      mbar_init(tfree_bar(i), C::kTileReaders);    // used in the even CTA only
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -341,6 +358,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
+  // ---- the pair's tile sequence
+  // Static (p.tile_counter == nullptr): tiles pair, pair + num_pairs, ...
+  // Dynamic: the pair's first tile is `pair`, every later one num_pairs +
+  // atomicAdd(counter, 1), taken by the even CTA's producer thread when it
+  // starts the tile and published in slot i % kTileRing of both CTAs' tile
+  // rings; every other role of both CTAs reads the same sequence from its own
+  // CTA's ring and frees the slot on the even CTA's tfree barrier.  A pair that
+  // finishes early takes the next tile, so the tiles in flight stay a window of
+  // consecutive indices (m-block fastest) whose weight tiles and A rows are
+  // shared through L2; under the static order pairs drift apart over a long
+  // launch and re-read both from DRAM.
+  const bool dyn = p.tile_counter != nullptr;
+  // the even CTA's producer thread: tile i of the pair, or -1 when none is left
+  auto sched_tile = [&](int i, bool& ok) -> int {
+    if (!dyn) {
+      const int t = pair + i * num_pairs;
+      return t < num_tiles ? t : -1;
+    }
+    const uint32_t slot = (uint32_t)(i % kTileRing), ph = (uint32_t)(i / kTileRing) & 1u;
+    if (!wait_bounded_cluster(tfree_bar(slot), ph ^ 1u, abort_flag, p.timeout_ns)) {
+      ok = false;
+      return -1;
+    }
+    int t = i == 0 ? pair : num_pairs + atomicAdd(p.tile_counter, 1);
+    if (t >= num_tiles) t = -1;
+    tile_ring[slot] = t;
+    st_cluster_u32(map_to_cta(smem_addr(const_cast<int*>(&tile_ring[slot])), 1), (uint32_t)t);
+    mbar_arrive(tfill_bar(slot));
+    mbar_arrive_cluster(map_to_cta(tfill_bar(slot), 1));
+    return t;
+  };
+  // every other role: tile i of the pair, or -1 (every lane of a warp role calls it)
+  auto next_tile = [&](int i, bool warp_role, bool& ok) -> int {
+    if (!dyn) {
+      const int t = pair + i * num_pairs;
+      return t < num_tiles ? t : -1;
+    }
+    const uint32_t slot = (uint32_t)(i % kTileRing), ph = (uint32_t)(i / kTileRing) & 1u;
+    bool got = leader ? wait_bounded(tfill_bar(slot), ph, abort_flag, p.timeout_ns)
+                      : wait_bounded_cluster(tfill_bar(slot), ph, abort_flag, p.timeout_ns);
+    if (warp_role) got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      ok = false;
+      return -1;
+    }
+    const int t = tile_ring[slot];
+    if (warp_role) __syncwarp();
+    if (!warp_role || lane == 0) {
+      if (leader)
+        mbar_arrive(tfree_bar(slot));
+      else
+        mbar_arrive_cluster(map_to_cta(tfree_bar(slot), 0));
+    }
+    return t;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -349,7 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
 #pragma unroll
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      for (int i = 0; ok; ++i) {
+        const int t = leader ? sched_tile(i, ok) : next_tile(i, false, ok);
+        if (t < 0) break;
         const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
         // this CTA's 128 rows of B.  Up projection, full tile: 128 rows of W
         // (even) or Wv (odd), one box; half tile: the CTA's 64 rows of the
@@ -416,7 +491,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       // --------------------------------------------------- MMA issuer (even CTA)
       uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      for (int i = 0; ok; ++i) {
+        const int t = next_tile(i, false, ok);
+        if (t < 0) break;
         const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
         if (!wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
@@ -477,7 +554,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       // k-block once this CTA's copies of it have landed.
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      for (int i = 0; ok; ++i) {
+        if (next_tile(i, false, ok) < 0) break;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             ok = false;
@@ -499,9 +577,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
     // --------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are reachable from this warp
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = pair; t < num_tiles; t += num_pairs) {
+    for (int i = 0;; ++i) {
+      bool ok = true;
+      const int t = next_tile(i, true, ok);
+      if (t < 0) {
+        if (!ok && lane == 0) raise_abort(abort_flag, p.err);
+        break;
+      }
       const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
-      bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
+      ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         if (lane == 0) raise_abort(abort_flag, p.err);
@@ -624,7 +708,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
     const int ct = threadIdx.x - (kConvWarp0 + grp * (kConvWarps / kConvGroups)) * 32;
     int gk = 0;  // running k-block count over this CTA's tiles
     bool ok = true;
-    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+    for (int i = 0; ok; ++i) {
+      const int t = next_tile(i, true, ok);
+      if (t < 0) break;
       // grouped scales (G > 1): staged B row r is weight row nb + r of the matrix
       // whose scales are gsc; in an up-projection half tile rows [64, 128) are
       // the same channels of Wv as rows [0, 64) of W

@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(
     if (user_counts) user_counts[tid] = s_counts[tid];
   }
   if (tid <= kNumExperts) sched[kNumExperts + tid] = s_off[tid];
+  if (tid < 2) sched[kSchedTileCtr + tid] = 0;  // the grouped GEMMs' tile counters
 }
 
 // xn_perm[row] = xn of token token_of_row[row], formed here from the hidden

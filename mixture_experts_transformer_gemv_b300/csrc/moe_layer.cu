@@ -186,7 +186,8 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
           xh, T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx, L->prob, topk_idx,
           topk_prob, L->p_part);
     } else {
-      const int grid = (int)((T + kRouterWarps * kRouterWTok - 1) / (kRouterWarps * kRouterWTok));
+      constexpr int kTokPerCta = kRouterWarps * kRouterWTok;
+      const int grid = (T + kTokPerCta - 1) / kTokPerCta;
       router_kernel<false><<<grid, kRouterThreads, 0, st>>>(xh, T, d, L->w.gate, L->w.gate_bias,
                                                            L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx,
                                                            L->prob, topk_idx, topk_prob, L->p_part);
@@ -242,6 +243,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.sched = L->sched;
     p.K = d;
     p.n_tiles = F / kGemmHalfN;
+    p.tile_counter = L->sched + kSchedTileCtr;  // dynamic tile schedule (zeroed by K2)
     p.b_rows_per_expert = F;
     p.n_out = F;
     p.out = L->act;
@@ -308,6 +310,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.sched = L->sched;
     p.K = F;
     p.n_tiles = (d + kGemmBN - 1) / kGemmBN;
+    p.tile_counter = L->sched + kSchedTileCtr + 1;  // dynamic tile schedule (zeroed by K2)
     p.b_rows_per_expert = d;
     p.n_out = d;
     p.out = L->y_rows;
