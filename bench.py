@@ -68,9 +68,9 @@ def kernel_function(role, inp):
         # (third template argument)
         mb = 2 if inp.F >= PAIR_MIN_F and inp.T >= PAIR_MIN_T else 1
         return f"grouped_gemm_kernel<{epi}, {int(int8)}, {mb}>", ["k_gemm.cuh", "ptx.cuh", "common.cuh"]
-    src = {"router": "k_router.cuh", "permute": "k_permute.cuh", "gather": "k_permute.cuh",
+    src = {"router": "k_router.cuh", "group": "k_permute.cuh",
            "combine": "k_combine.cuh"}[role]
-    name = {"router": "router_kernel", "permute": "permute_kernel", "gather": "gather_rows_kernel",
+    name = {"router": "router_kernel", "group": "group_rows_kernel",
             "combine": "combine_kernel"}[role]
     return name, [src, "common.cuh"]
 
@@ -151,8 +151,8 @@ def algorithmic_work(inp, counts):
     work = {
         # x read once; gate and s_pre; per token idx/prob (16 B), r (4 B), p (32 B)
         "router": ("hbm", T * d * 2 + 9 * d * 4 + T * 52),
-        "permute": ("hbm", S * 4 * 2 + S * 4 * 3),
-        "gather": ("hbm", S * d * 2 * 2),
+        # idx / prob in, row_of_slot / token_of_row / prob_of_row out, x read once, S normed rows out
+        "group": ("hbm", S * 4 * 2 + S * 4 * 3 + T * d * 2 + S * d * 2),
         "up_geglu": ("tensor", 2.0 * 2 * d * F * S),
         "down": ("tensor", 2.0 * d * F * S),
         "combine": ("hbm", S * d * 4 + T * d * 2 * 2),

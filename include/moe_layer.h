@@ -204,13 +204,13 @@ moe_status_t moe_layer_router_stats(moe_layer_t* layer, float* stats, void* stre
 
 /* Kernels of one forward, in launch order (indices of the profiling arrays). */
 typedef enum {
-  MOE_K_ROUTER = 0,   /* pre-norm + router logits + softmax + top-2 */
-  MOE_K_PERMUTE = 1,  /* per-expert counts, padded offsets, stable slot order */
-  MOE_K_GATHER = 2,   /* copy of normed rows into expert-contiguous order */
-  MOE_K_UP = 3,       /* expert up-projections W, Wv with the GeGLU epilogue */
-  MOE_K_DOWN = 4,     /* expert down-projection W1, scaled by the combine weight */
-  MOE_K_COMBINE = 5,  /* combine of the two expert rows + post-norm + residual */
-  MOE_K_COUNT = 6
+  MOE_K_ROUTER = 0,   /* pre-norm statistics + router logits + softmax + top-2 */
+  MOE_K_GROUP = 1,    /* per-expert counts, padded offsets, stable slot order, and the
+                         normed rows written in expert-contiguous order */
+  MOE_K_UP = 2,       /* expert up-projections W, Wv with the GeGLU epilogue */
+  MOE_K_DOWN = 3,     /* expert down-projection W1, scaled by the combine weight */
+  MOE_K_COMBINE = 4,  /* combine of the two expert rows + post-norm + residual */
+  MOE_K_COUNT = 5
 } moe_kernel_id_t;
 
 /* Turn per-kernel CUDA-event timing of later forwards on (1) or off (0).

@@ -4,16 +4,17 @@
 // pointers, encodes the TMA descriptors of the expert weights and of the two
 // GEMM activation buffers, and allocates one workspace block.
 // moe_layer_forward enqueues, on the caller's stream and without any host wait:
-//   K1 router_kernel        pre-norm, router logits, softmax, top-2
-//   K2 permute_kernel       counts, padded row offsets, stable slot -> row map
-//      gather_rows_kernel   normed rows into expert-contiguous order
+//   K1 router_kernel        pre-norm statistics, router logits, softmax, top-2
+//   K2 group_rows_kernel    counts, padded row offsets, stable slot -> row map,
+//                           and the normed rows written in expert order
 //   K3 grouped_gemm<geglu>  act = GELU(A W^T) * (A Wv^T)        (tcgen05)
 //   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
 //   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
 // For T <= 16 (or MOE_FLAG_FORCE_GEMV) K3/K4 are replaced by the weight-streaming
 // decode kernels (k_decode.cuh for bf16 weights, k_decode_i8.cuh for int8) and K5
-// sums their split-K partials.  int8 weights are converted to bf16 on chip and
-// their per-channel scales applied in the epilogues.
+// sums their split-K partials.  int8 weights are converted to fp16 on chip and
+// their per-channel scales applied in the epilogues.  The allocation-free
+// grouping entry point (end of file) runs permute_kernel, K2's grouping alone.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -194,18 +195,16 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     }
   }
   mark(1);
-  permute_kernel<<<1, kPermuteThreads, 0, st>>>(L->idx, L->prob, T, L->sched, L->row_of_slot, L->token_of_row,
-                                               L->prob_of_row, counts, (int)L->rows_cap, checks, L->err);
+  // grouping + normed rows in expert order; int8 layers multiply in fp16 (int8 ->
+  // fp16 is one shuffle and one subtraction), so their activation rows are fp16
+  // 4 CTAs per SM (memory parallelism for the row copies, and every SM zeroing
+  // padding rows even for a few tokens); every CTA reads all of idx, so beyond
+  // 16384 tokens one CTA per SM
+  group_rows_kernel<<<T <= 16384 ? 4 * L->num_sms : L->num_sms, kGroupThreads, 0, st>>>(
+      L->idx, L->prob, T, static_cast<const __nv_bfloat16*>(hidden), L->rnorm, L->w.pre_norm_scale, d,
+      int8 ? 1 : 0, L->sched, L->row_of_slot, L->token_of_row, L->prob_of_row, L->xn_perm, counts,
+      (int)L->rows_cap, checks, L->err);
   mark(2);
-  {
-    const int grid = (int)std::min<int64_t>(L->rows_cap, (int64_t)L->num_sms * 8);
-    // int8 layers multiply in fp16 (int8 -> fp16 is one shuffle and one
-    // subtraction), so their activation rows are fp16
-    gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(hidden), L->rnorm,
-                                             L->w.pre_norm_scale, L->token_of_row, L->sched, d, int8 ? 1 : 0,
-                                             L->xn_perm, checks, L->err);
-  }
-  mark(3);
   if (decode && int8) {
     DecI8Params p{};
     p.sched = L->sched;
@@ -273,7 +272,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
       grouped_gemm_kernel<kEpiGeglu, false><<<L->gemm_grid[kEpiGeglu][0][0], kGemmThreads, kGemmSmemBytes, st>>>(
           L->tm_xn_perm, L->tm_w, L->tm_wv, L->tm_xn_perm64, L->tm_w64, L->tm_wv64, p);
   }
-  mark(4);
+  mark(3);
   if (decode && int8) {
     DecI8Params p{};
     p.sched = L->sched;
@@ -339,7 +338,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
              st>>>(
           L->tm_act, L->tm_w1_128, L->tm_w1_128, L->tm_act64, L->tm_w1_128, L->tm_w1_128, p);
   }
-  mark(5);
+  mark(4);
   {
     const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
@@ -362,7 +361,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
                                                L->w.post_norm_scale, L->cfg.eps, d, rc, checks, L->err, o);
     }
   }
-  mark(6);
+  mark(5);
   L->launches += MOE_K_COUNT;
   L->last_T = T;
   cudaError_t e = cudaGetLastError();
