@@ -189,9 +189,9 @@ struct TileCoord {
 // Tiles along m of one expert with `rows` padded rows (a multiple of 128): its
 // m-blocks are rows / 256 full ones and, when rows % 256 = 128, one half block.
 // MB = 1: one m-block per tile.  MB = 2 with PH (down projection): consecutive
-// m-blocks in pairs, the half block included.  MB = 2 without PH (up projection,
-// whose half tiles stage B differently): the full blocks in pairs, the half
-// block a tile of its own.
+// m-blocks in pairs, the half block included (ordered in two phases, see
+// mblock_prefix).  MB = 2 without PH (up projection, whose half tiles stage B
+// differently): the full blocks in pairs, the half block a tile of its own.
 template <int MB, bool PH>
 __device__ __forceinline__ int mtiles(int rows) {
   const int nblk = (rows + kGemmBM - 1) / kGemmBM;
@@ -202,31 +202,67 @@ __device__ __forceinline__ int mtiles(int rows) {
 }
 
 // Tiles along m of the experts before e: mb[e] = sum_{q < e} mtiles(rows of q).
+// Paired down projection (MB = 2, PH): two phases.  mb[] counts each expert's
+// uniform tiles (two full m-blocks), pb[] its last tile when that holds less
+// (a full block with a half one, or one block alone): every uniform tile of every
+// expert first, so the long tiles in flight have the same length and stay in step,
+// then the shorter ones.
 template <int MB, bool PH>
-__device__ __forceinline__ void mblock_prefix(const int (&off)[kNumExperts + 1], int (&mb)[kNumExperts + 1]) {
+__device__ __forceinline__ void mblock_prefix(const int (&off)[kNumExperts + 1], int (&mb)[kNumExperts + 1],
+                                              int (&pb)[kNumExperts + 1]) {
   mb[0] = 0;
+  pb[0] = 0;
 #pragma unroll
-  for (int q = 0; q < kNumExperts; ++q) mb[q + 1] = mb[q] + mtiles<MB, PH>(off[q + 1] - off[q]);
+  for (int q = 0; q < kNumExperts; ++q) {
+    const int rows = off[q + 1] - off[q];
+    if (MB == 2 && PH) {
+      const int nblk = (rows + kGemmBM - 1) / kGemmBM, u = (rows / kGemmBM) / 2;
+      mb[q + 1] = mb[q] + u;
+      pb[q + 1] = pb[q] + (nblk > 2 * u ? 1 : 0);
+    } else {
+      mb[q + 1] = mb[q] + mtiles<MB, PH>(rows);
+      pb[q + 1] = 0;
+    }
+  }
 }
 
 // Tile t -> (expert, n-block, its m-blocks); tiles of expert e are
 // [mb[e] * n_tiles, mb[e + 1] * n_tiles), the m position fastest.
 template <int MB, bool PH>
 __device__ __forceinline__ TileCoord<MB> decode_tile(int t, const int (&off)[kNumExperts + 1],
-                                                     const int (&mb)[kNumExperts + 1], int n_tiles) {
+                                                     const int (&mb)[kNumExperts + 1],
+                                                     const int (&pb)[kNumExperts + 1], int n_tiles) {
+  if (MB == 2 && PH && t >= mb[kNumExperts] * n_tiles) {  // phase 2: the experts' last, shorter tiles
+    const int t2 = t - mb[kNumExperts] * n_tiles;
+    int e = 0;
+#pragma unroll
+    for (int q = 1; q < kNumExperts; ++q)
+      if (t2 >= pb[q] * n_tiles) e = q;
+    const int rows = off[e + 1] - off[e];
+    const int nblk = (rows + kGemmBM - 1) / kGemmBM;
+    const int first = ((rows / kGemmBM) / 2) * 2;
+    TileCoord<MB> c;
+    c.e = e;
+    c.n_blk = t2 - pb[e] * n_tiles;
+    c.nm = nblk - first;
+#pragma unroll
+    for (int j = 0; j < MB; ++j) {
+      c.row0[j] = off[e] + (first + j) * kGemmBM;
+      c.half[j] = off[e + 1] - c.row0[j] < kGemmBM;
+    }
+    return c;
+  }
   int e = 0;
 #pragma unroll
   for (int q = 1; q < kNumExperts; ++q)
     if (t >= mb[q] * n_tiles) e = q;
   const int mt = mb[e + 1] - mb[e];
   const int local = t - mb[e] * n_tiles;
-  const int rows = off[e + 1] - off[e];
-  const int nblk = (rows + kGemmBM - 1) / kGemmBM;
-  const int nfull = rows / kGemmBM;
+  const int nfull = (off[e + 1] - off[e]) / kGemmBM;
   const int i = local % mt;
   // first m-block of the tile and how many it holds
   int first = i * MB, nm = 1;
-  if (MB == 2 && PH) nm = min(2, nblk - first);
+  if (MB == 2 && PH) nm = 2;  // phase 1: two full m-blocks
   if (MB == 2 && !PH) {
     const int npair = (nfull + 1) / 2;
     nm = i < npair ? min(2, nfull - first) : 1;
@@ -310,11 +346,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
   const bool leader = rank == 0;
   const int pair = (int)cluster_id_x(), num_pairs = (int)num_clusters_x();
 
-  int off[kNumExperts + 1], mb[kNumExperts + 1];
+  int off[kNumExperts + 1], mb[kNumExperts + 1], pb[kNumExperts + 1];
 #pragma unroll
   for (int q = 0; q <= kNumExperts; ++q) off[q] = p.sched[kNumExperts + q];
-  mblock_prefix<MB, PH>(off, mb);
-  const int num_tiles = mb[kNumExperts] * p.n_tiles;
+  mblock_prefix<MB, PH>(off, mb, pb);
+  const int num_tiles = (mb[kNumExperts] + pb[kNumExperts]) * p.n_tiles;
   const int kb_count = p.K / kGemmBK;
 
   if (threadIdx.x == 0) {
@@ -425,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       for (int i = 0; ok; ++i) {
         const int t = leader ? sched_tile(i, ok) : next_tile(i, false, ok);
         if (t < 0) break;
-        const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
+        const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, pb, p.n_tiles);
         // this CTA's 128 rows of B.  Up projection, full tile: 128 rows of W
         // (even) or Wv (odd), one box; half tile: the CTA's 64 rows of the
         // n-block from W, then the same 64 rows from Wv (two 64-row boxes).
@@ -494,7 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       for (int i = 0; ok; ++i) {
         const int t = next_tile(i, false, ok);
         if (t < 0) break;
-        const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
+        const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, pb, p.n_tiles);
         if (!wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
@@ -584,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
         if (!ok && lane == 0) raise_abort(abort_flag, p.err);
         break;
       }
-      const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
+      const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, pb, p.n_tiles);
       ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -714,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<WQ, MB>::kTh
       // grouped scales (G > 1): staged B row r is weight row nb + r of the matrix
       // whose scales are gsc; in an up-projection half tile rows [64, 128) are
       // the same channels of Wv as rows [0, 64) of W
-      const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, p.n_tiles);
+      const TileCoord<MB> tc = decode_tile<MB, PH>(t, off, mb, pb, p.n_tiles);
       const bool split_wv = EPI == kEpiGeglu && tc.half[0];
       const int nb = (EPI == kEpiGeglu) ? tc.n_blk * kGemmHalfN + (tc.half[0] ? (int)rank * kGemmBoxRows : 0)
                                         : tc.n_blk * kGemmBN + (int)rank * kGemmHalfN;
