@@ -59,6 +59,9 @@ def kernel_function(role, inp):
     int8 = inp.weight_dtype == "int8"
     if role in ("up_geglu", "down"):
         epi = 0 if role == "up_geglu" else 1
+        if inp.T <= GEMV_I8_MAX_T and int8:
+            grouped = "true" if inp.scale_groups > 1 else "false"
+            return f"gemv_i8_kernel<{epi}, {grouped}>", ["k_gemv_i8.cuh", "k_decode.cuh", "ptx.cuh", "common.cuh"]
         if inp.T <= DECODE_MAX_T and int8:
             return f"decode_gemm_i8_kernel<{epi}>", ["k_decode_i8.cuh", "k_decode.cuh", "k_gemm.cuh", "ptx.cuh",
                                                      "ptx_pair.cuh", "ptx_tmem.cuh", "common.cuh"]
@@ -136,6 +139,7 @@ def config_block(inp):
 
 
 DECODE_MAX_T = 16  # the library's weight-streaming path takes T <= 16
+GEMV_I8_MAX_T = 8  # int8 weights at T <= 8: the CUDA-core GEMV kernels
 ROW_PAD = 128  # each expert's permuted rows are padded to a multiple of this
 PAIR_MIN_F, PAIR_MIN_T = 16384, 2048  # the library's grouped GEMMs pair m-blocks from these F and T on
 

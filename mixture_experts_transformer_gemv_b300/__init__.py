@@ -22,7 +22,7 @@ ATTN_HEADER_PATH = os.path.join(_ROOT, "include", "attn_block.h")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_TIMEOUT = 4, 5, 6
 MOE_WEIGHT_BF16, MOE_WEIGHT_INT8 = 0, 1
-MOE_FLAG_DEVICE_CHECKS, MOE_FLAG_FORCE_TC, MOE_FLAG_FORCE_GEMV = 0x1, 0x2, 0x4
+MOE_FLAG_DEVICE_CHECKS, MOE_FLAG_FORCE_TC, MOE_FLAG_FORCE_GEMV, MOE_FLAG_DECODE_TC = 0x1, 0x2, 0x4, 0x8
 KERNEL_NAMES = ("router", "group", "up_geglu", "down", "combine")
 ATTN_KERNEL_NAMES = ("prenorm", "qkv", "rope", "attn", "oproj", "post")
 

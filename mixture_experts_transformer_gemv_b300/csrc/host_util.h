@@ -96,6 +96,22 @@ inline moe_status_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t in
   return MOE_OK;
 }
 
+// Row-major 2-D tensor [rows, inner] of esize-byte elements, box [box_rows, box_inner],
+// no swizzle (rows land in shared memory as they are in global memory).
+inline moe_status_t make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base,
+                                 uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (%u-byte elements) failed (%d)", esize, (int)r);
+  return MOE_OK;
+}
+
 // CTAs of a persistent cluster launch of `kernel` (clusters of 2): twice the
 // clusters that can be resident at once, at most one CTA per SM.
 inline moe_status_t cluster_pair_grid(int num_sms, const void* kernel, int threads, size_t smem, int* grid) {

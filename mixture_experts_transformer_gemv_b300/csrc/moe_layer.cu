@@ -11,8 +11,9 @@
 //   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
 //   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
 // For T <= 16 (or MOE_FLAG_FORCE_GEMV) K3/K4 are replaced by the weight-streaming
-// decode kernels (k_decode.cuh for bf16 weights, k_decode_i8.cuh for int8) and K5
-// sums their split-K partials.  int8 weights are converted to fp16 on chip and
+// decode kernels (k_decode.cuh for bf16 weights, k_decode_i8.cuh for int8; int8 at
+// T <= 8 by the CUDA-core GEMV kernels of k_gemv_i8.cuh unless MOE_FLAG_DECODE_TC)
+// and K5 sums their split-K partials.  int8 weights are converted to fp16 on chip and
 // their per-channel scales applied in the epilogues.  The allocation-free
 // grouping entry point (end of file) runs permute_kernel, K2's grouping alone.
 #include <cuda.h>
@@ -34,6 +35,7 @@
 #include "k_combine.cuh"
 #include "k_decode.cuh"
 #include "k_decode_i8.cuh"
+#include "k_gemv_i8.cuh"
 #include "k_gemm.cuh"
 #include "k_permute.cuh"
 #include "k_router.cuh"
@@ -101,6 +103,8 @@ struct moe_layer {
   float* y_rows = nullptr;
   float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
   float* p_part = nullptr;  // [router CTAs (<= max_T)][E] per-router-CTA sums of p
+  int16_t* xq = nullptr;    // int8 GEMV path: [E * 8][max(d, F)] slot rows in 16-bit fixed point
+  float* xqs = nullptr;     //                 [max(d, F) / 128][E * 8] their block scales
   int last_T = 0;           // tokens of the last forward enqueued (routing diagnostics)
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
@@ -114,6 +118,7 @@ struct moe_layer {
   CUtensorMap tm_w8{}, tm_wv8{}, tm_w18{};              // int8 weights (staging boxes of 128 rows)
   CUtensorMap tm_w8h{}, tm_wv8h{};                      // int8 weights, half tiles (64 rows)
   CUtensorMap tm_w8d{}, tm_wv8d{}, tm_w18d{};           // int8 weights, 64-byte swizzle (decode)
+  CUtensorMap tm_xq_d{}, tm_xq_f{}, tm_xqs_d{}, tm_xqs_f{};  // int8 GEMV: quantised rows and scales, K = d or F
 
   void* host_stage = nullptr;  // device staging for moe_layer_forward_host
   size_t host_stage_bytes = 0;
@@ -152,6 +157,14 @@ void harvest(moe_layer* L, int slot) {
     }
   }
   L->pending[slot] = false;
+}
+
+// int8 GEMV path: the 2T slot rows (fp16, K wide) into 16-bit fixed point, one
+// warp per slot row and 128-element block, 8 warps per CTA.
+void launch_quantize_slots(moe_layer* L, int T, const void* rows, int K, cudaStream_t st) {
+  const int S = 2 * T, warps = S * (K / kGv8BK);
+  quantize_slots_kernel<<<(warps + 7) / 8, 256, 0, st>>>(static_cast<const uint16_t*>(rows), K, L->row_of_slot,
+                                                         L->idx, L->sched, S, L->xq, L->xqs);
 }
 
 moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T, cudaStream_t st,
@@ -205,6 +218,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
       int8 ? 1 : 0, L->sched, L->row_of_slot, L->token_of_row, L->prob_of_row, L->xn_perm, counts,
       (int)L->rows_cap, checks, L->err);
   mark(2);
+  // int8 weights at T <= 8: integer dot products on the CUDA cores (k_gemv_i8.cuh)
+  const bool gemv8 = decode && int8 && T <= kGv8MaxT && !(L->cfg.flags & MOE_FLAG_DECODE_TC);
+  const bool grouped8 = L->cfg.scale_groups > 1;
   if (decode && int8) {
     DecI8Params p{};
     p.sched = L->sched;
@@ -222,8 +238,16 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.checks = checks;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
-    decode_gemm_i8_kernel<kEpiGeglu><<<L->num_sms, DecI8Cfg<kEpiGeglu>::kThreads, DecI8Cfg<kEpiGeglu>::kSmemBytes,
-                                       st>>>(L->tm_w8d, L->tm_wv8d, L->tm_xn_perm16, p);
+    if (gemv8) launch_quantize_slots(L, T, L->xn_perm, d, st);
+    if (gemv8 && grouped8)
+      gemv_i8_kernel<kEpiGeglu, true><<<L->num_sms, GvI8Cfg<kEpiGeglu>::kThreads, GvI8Cfg<kEpiGeglu>::kSmemBytes,
+                                        st>>>(L->tm_w8d, L->tm_wv8d, L->tm_xq_d, L->tm_xqs_d, p);
+    else if (gemv8)
+      gemv_i8_kernel<kEpiGeglu, false><<<L->num_sms, GvI8Cfg<kEpiGeglu>::kThreads, GvI8Cfg<kEpiGeglu>::kSmemBytes,
+                                         st>>>(L->tm_w8d, L->tm_wv8d, L->tm_xq_d, L->tm_xqs_d, p);
+    else
+      decode_gemm_i8_kernel<kEpiGeglu><<<L->num_sms, DecI8Cfg<kEpiGeglu>::kThreads, DecI8Cfg<kEpiGeglu>::kSmemBytes,
+                                         st>>>(L->tm_w8d, L->tm_wv8d, L->tm_xn_perm16, p);
   } else if (decode) {
     DecParams p{};
     p.sched = L->sched;
@@ -289,8 +313,16 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     p.group_kb = F / L->cfg.scale_groups / kDq8BK;
     p.err = L->err;
     p.timeout_ns = kWaitLimitNs;
-    decode_gemm_i8_kernel<kEpiDown><<<L->num_sms, DecI8Cfg<kEpiDown>::kThreads, DecI8Cfg<kEpiDown>::kSmemBytes,
-                                      st>>>(L->tm_w18d, L->tm_w18d, L->tm_act16, p);
+    if (gemv8) launch_quantize_slots(L, T, L->act, F, st);
+    if (gemv8 && grouped8)
+      gemv_i8_kernel<kEpiDown, true><<<L->num_sms, GvI8Cfg<kEpiDown>::kThreads, GvI8Cfg<kEpiDown>::kSmemBytes, st>>>(
+          L->tm_w18d, L->tm_w18d, L->tm_xq_f, L->tm_xqs_f, p);
+    else if (gemv8)
+      gemv_i8_kernel<kEpiDown, false><<<L->num_sms, GvI8Cfg<kEpiDown>::kThreads, GvI8Cfg<kEpiDown>::kSmemBytes, st>>>(
+          L->tm_w18d, L->tm_w18d, L->tm_xq_f, L->tm_xqs_f, p);
+    else
+      decode_gemm_i8_kernel<kEpiDown><<<L->num_sms, DecI8Cfg<kEpiDown>::kThreads, DecI8Cfg<kEpiDown>::kSmemBytes,
+                                        st>>>(L->tm_w18d, L->tm_w18d, L->tm_act16, p);
   } else if (decode) {
     DecParams p{};
     p.sched = L->sched;
@@ -362,7 +394,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
     }
   }
   mark(5);
-  L->launches += MOE_K_COUNT;
+  L->launches += MOE_K_COUNT + (gemv8 ? 2 : 0);  // + the two row quantisations of the int8 GEMV path
   L->last_T = T;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -435,7 +467,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
       std::max(std::max(std::max(kGemmSmemBytes, GemmCfg<true>::kSmemBytes),
                         std::max(GemmCfg<false, kGemmMBPair>::kSmemBytes, GemmCfg<true, kGemmMBPair>::kSmemBytes)),
                std::max(std::max(DecCfg<kEpiGeglu>::kSmemBytes, DecCfg<kEpiDown>::kSmemBytes),
-                        std::max(DecI8Cfg<kEpiGeglu>::kSmemBytes, DecI8Cfg<kEpiDown>::kSmemBytes)));
+                        std::max(std::max(DecI8Cfg<kEpiGeglu>::kSmemBytes, DecI8Cfg<kEpiDown>::kSmemBytes),
+                                 std::max(GvI8Cfg<kEpiGeglu>::kSmemBytes, GvI8Cfg<kEpiDown>::kSmemBytes))));
   if (prop.sharedMemPerBlockOptin < smem_need)
     return fail(MOE_ERR_UNSUPPORTED, "device offers %zu B shared memory per block, need %zu",
                 (size_t)prop.sharedMemPerBlockOptin, smem_need);
@@ -453,13 +486,17 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   const int64_t R = L->rows_cap;
 
   // one workspace block, every buffer 1 KB aligned
-  size_t offs[13], total = 0;
-  const size_t sizes[13] = {(size_t)(T * 4), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
+  const int64_t kq = std::max(d, F);
+  const bool i8 = c.weight_dtype == MOE_WEIGHT_INT8;
+  size_t offs[15], total = 0;
+  const size_t sizes[15] = {(size_t)(T * 4), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
                             (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
                             (size_t)(R * F * 2), (size_t)(R * d * 4), 256,
                             (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4,
-                            (size_t)T * kNumExperts * 4};
-  for (int i = 0; i < 13; ++i) {
+                            (size_t)T * kNumExperts * 4,
+                            i8 ? (size_t)kGv8QRows * kq * 2 : 0,
+                            i8 ? (size_t)(kq / kGv8BK) * kGv8QRows * 4 : 0};
+  for (int i = 0; i < 15; ++i) {
     offs[i] = total;
     total = align_up(total + sizes[i], 1024);
   }
@@ -483,6 +520,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   L->err = reinterpret_cast<uint32_t*>(b + offs[10]);
   L->part = reinterpret_cast<float*>(b + offs[11]);
   L->p_part = reinterpret_cast<float*>(b + offs[12]);
+  L->xq = reinterpret_cast<int16_t*>(b + offs[13]);
+  L->xqs = reinterpret_cast<float*>(b + offs[14]);
   // decode-path split of the F reduction: up to kDecMaxSplit chunks of whole 64-wide blocks
   L->ksplit = kDecMaxSplit;
   while (L->ksplit > 1 && (F / kDecBK) % L->ksplit) L->ksplit /= 2;
@@ -512,6 +551,16 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
       s = make_tmap_i8(&L->tm_wv8d, w->wv, d, kNumExperts * F, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == MOE_OK)
       s = make_tmap_i8(&L->tm_w18d, w->w1, F, kNumExperts * d, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (i8) {  // int8 GEMV: an expert's 8 quantised rows of a block (256 B each) and their 8 scales
+    if (s == MOE_OK)
+      s = make_tmap_2d(&L->tm_xq_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, L->xq, d, kGv8QRows, kGv8BK, kGv8NS);
+    if (s == MOE_OK)
+      s = make_tmap_2d(&L->tm_xq_f, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, L->xq, F, kGv8QRows, kGv8BK, kGv8NS);
+    if (s == MOE_OK)
+      s = make_tmap_2d(&L->tm_xqs_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L->xqs, kGv8QRows, d / kGv8BK, kGv8NS, 1);
+    if (s == MOE_OK)
+      s = make_tmap_2d(&L->tm_xqs_f, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L->xqs, kGv8QRows, F / kGv8BK, kGv8NS, 1);
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
@@ -578,6 +627,19 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
       cudaFuncSetAttribute(decode_gemm_i8_kernel<kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)DecI8Cfg<kEpiDown>::kSmemBytes) != cudaSuccess)
     s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 decode down) failed");
+  {
+    const struct {
+      const void* k;
+      size_t smem;
+    } gv[4] = {{(const void*)gemv_i8_kernel<kEpiGeglu, false>, GvI8Cfg<kEpiGeglu>::kSmemBytes},
+               {(const void*)gemv_i8_kernel<kEpiGeglu, true>, GvI8Cfg<kEpiGeglu>::kSmemBytes},
+               {(const void*)gemv_i8_kernel<kEpiDown, false>, GvI8Cfg<kEpiDown>::kSmemBytes},
+               {(const void*)gemv_i8_kernel<kEpiDown, true>, GvI8Cfg<kEpiDown>::kSmemBytes}};
+    for (const auto& k : gv)
+      if (s == MOE_OK &&
+          cudaFuncSetAttribute(k.k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess)
+        s = fail(MOE_ERR_CUDA, "cudaFuncSetAttribute (int8 GEMV) failed");
+  }
   // Grouped GEMMs run one CTA pair per two SMs, persistent: launch as many
   // pairs as can be resident at once (whole clusters only), at most one per SM pair.
   L->pair_mblocks = F >= kPairMinF;

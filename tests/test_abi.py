@@ -35,6 +35,13 @@ def test_library_is_built_for_sm_103a():
     assert os.path.exists(moe.LIB_PATH)
 
 
+def test_header_flag_values_match_the_binding():
+    import re
+    text = open(moe.HEADER_PATH).read()
+    found = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define (MOE_FLAG_\w+) (0x[0-9a-f]+)u", text)}
+    assert found == {k: getattr(moe, k) for k in found} and len(found) == 4
+
+
 def test_status_strings(lib):
     assert lib.moe_status_string(0) == b"MOE_OK"
     assert lib.moe_status_string(1) == b"MOE_ERR_INVALID_ARG"

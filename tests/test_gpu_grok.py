@@ -68,17 +68,21 @@ def test_skew_shares_reported(grok):
 
 def test_int8_decode_full_shape():
     """int8 weights at the Grok-1 shape with T = 8 (the int8 workload's first 8
-    tokens): the int8 weight-streaming kernels against the oracle on every token."""
+    tokens): the CUDA-core GEMV kernels (the default at T <= 8) and the
+    tensor-core weight-streaming kernels (MOE_FLAG_DECODE_TC) against the oracle
+    on every token."""
     from mixture_experts_transformer_gemv_b300 import build
+    import mixture_experts_transformer_gemv_b300 as moe
     build.build()
     inp = synth.workload("int8", T=8)
     weights = device_weights(inp)
-    layer = make_layer(inp, weights=weights)
-    y, idx, prob, counts = run(layer, inp)
     ref = oracle.moe_tokens(inp)
-    assert_routing(idx, prob, counts, ref, "int8 decode")
-    rep = assert_values(y, ref.y, "int8 decode")
-    print("int8 decode T=8 values", rep)
-    layer.close()
+    for flags, name in ((0, "int8 decode (GEMV)"), (moe.MOE_FLAG_DECODE_TC, "int8 decode (tensor cores)")):
+        layer = make_layer(inp, weights=weights, flags=flags)
+        y, idx, prob, counts = run(layer, inp)
+        assert_routing(idx, prob, counts, ref, name)
+        rep = assert_values(y, ref.y, name)
+        print(name, "T=8 values", rep)
+        layer.close()
     del weights
     torch.cuda.empty_cache()

@@ -307,10 +307,12 @@ def test_int8_paired_mblocks_skewed():
     (9, 512, 1024, 73),
     (16, 256, 512, 78),     # the largest T the decode path takes
 ])
-@pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_FORCE_TC])
+@pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_FORCE_TC, moe.MOE_FLAG_DECODE_TC])
 def test_int8_decode_path_and_forced_tensor_core_path(T, d, F, seed, flags):
-    """int8 weights at T <= 16 run the int8 weight-streaming kernels (weights
-    converted into Tensor Memory) unless the grouped GEMMs are forced."""
+    """int8 weights at T <= 16 run the int8 weight-streaming kernels unless the
+    grouped GEMMs are forced: at T <= 8 the CUDA-core GEMV kernels (integer dot
+    products), or with MOE_FLAG_DECODE_TC the tensor-core kernels (weights
+    converted into Tensor Memory), which T = 9..16 always take."""
     inp = synth.make_inputs(T, d, F, seed, name=f"int8dec{T}x{d}x{F}", weight_dtype="int8")
     _full_check(inp, flags=flags)
 
@@ -327,6 +329,22 @@ def test_int8_decode_one_expert_heavy_batch():
         y, idx, prob, counts = run(layer, inp)
         assert counts[6] == 16
         assert_values(y, ref.y, f"int8dec_onehot flags={flags}")
+        layer.close()
+
+
+def test_int8_gemv_eight_slots_on_one_expert():
+    """T = 8 with every token's first choice on expert 6: eight slot rows on one
+    expert, the most the CUDA-core GEMV kernels take; both int8 decode kernels."""
+    inp = synth.make_inputs(8, 384, 640, 85, name="int8gemv_onehot", weight_dtype="int8")
+    b = np.zeros(8, np.float32)
+    b[6] = 1e4
+    inp.bias = b
+    ref = oracle.moe_tokens(inp)
+    for flags in (0, moe.MOE_FLAG_DECODE_TC):
+        layer = make_layer(inp, flags=flags)
+        y, idx, prob, counts = run(layer, inp)
+        assert counts[6] == 8
+        assert_values(y, ref.y, f"int8gemv_onehot flags={flags}")
         layer.close()
 
 
@@ -413,6 +431,7 @@ def test_int8_intermediates_match_oracle():
     (200, "bf16", 0),                         # grouped GEMMs on CTA pairs
     (200, "int8", 0),                         # int8 grouped GEMMs
     (8, "int8", moe.MOE_FLAG_FORCE_TC),
+    (8, "int8", moe.MOE_FLAG_DECODE_TC),
 ])
 def test_back_to_back_forwards_are_deterministic(T, weights, flags):
     """Forty forwards queued back to back on one stream: no device wait may run
@@ -489,7 +508,7 @@ def test_router_stats_needs_a_forward():
 # bf16 or fp16 rounding); G == 1 scales multiply the fp32 result.
 
 @pytest.mark.parametrize("shape", [(8, 8), (1, 1), (1, 8), (8, 2)])
-@pytest.mark.parametrize("T,flags", [(200, 0), (8, 0), (8, moe.MOE_FLAG_FORCE_TC)])
+@pytest.mark.parametrize("T,flags", [(200, 0), (8, 0), (8, moe.MOE_FLAG_FORCE_TC), (8, moe.MOE_FLAG_DECODE_TC)])
 def test_int8_scale_shapes(shape, T, flags):
     inp = synth.make_inputs(T, 1024, 1024, 90 + shape[0] + shape[1], name=f"int8_scales_{shape}",
                             weight_dtype="int8", int8_scale_shape=shape)
