@@ -60,8 +60,7 @@ def kernel_function(role, inp):
     if role in ("up_geglu", "down"):
         epi = 0 if role == "up_geglu" else 1
         if inp.T <= GEMV_I8_MAX_T and int8:
-            grouped = "true" if inp.scale_groups > 1 else "false"
-            return f"gemv_i8_kernel<{epi}, {grouped}>", ["k_gemv_i8.cuh", "k_decode.cuh", "ptx.cuh", "common.cuh"]
+            return f"gemv_i8_kernel<{epi}, {int(inp.scale_groups > 1)}>", ["k_gemv_i8.cuh", "k_decode.cuh", "ptx.cuh", "common.cuh"]
         if inp.T <= DECODE_MAX_T and int8:
             return f"decode_gemm_i8_kernel<{epi}>", ["k_decode_i8.cuh", "k_decode.cuh", "k_gemm.cuh", "ptx.cuh",
                                                      "ptx_pair.cuh", "ptx_tmem.cuh", "common.cuh"]
