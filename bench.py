@@ -14,11 +14,13 @@ One JSON line on rank 0: the base keys plus roofline (dominant kernel), cpu_base
 (SM clock, power and throttle reasons sampled every 10 ms over the timed region)
 and gpu_launches.  A tensor-bound roofline divides by the measured burst bf16
 rate when the timed region is shorter than 2 s (else the sustained rate) and
-keeps both fractions.  The default single-GPU run adds two keys: "band" (the
+keeps both fractions.  The default single-GPU run adds three keys: "band" (the
 same weights at T = 16 ... 1024 tokens, across the switch from the
-weight-streaming decode kernels to the grouped tensor-core GEMMs) and "configs"
+weight-streaming decode kernels to the grouped tensor-core GEMMs), "configs"
 (one line each for the decode T=8, int8 T=2048, int8 decode T=8 and skewed
-T=4096 workloads, each with its own step time, roofline and clocks).  With N > 1
+T=4096 workloads, each with its own step time, roofline and clocks) and
+"int8_band" (the int8 workload's weights at T = 1, 4, 12 and 16 tokens, the
+other token counts of the int8 GEMV kernels).  With N > 1
 (torchrun) every rank runs its own replica of the workload on its own GPU: the
 layer is token-parallel with no exchange, so scaling is weak and value = N * T
 / max-over-ranks step time.
@@ -138,7 +140,7 @@ def config_block(inp):
 
 
 DECODE_MAX_T = 16  # the library's weight-streaming path takes T <= 16
-GEMV_I8_MAX_T = 8  # int8 weights at T <= 8: the CUDA-core GEMV kernels
+GEMV_I8_MAX_T = 16  # int8 weights at T <= 16: the CUDA-core GEMV kernels
 ROW_PAD = 128  # each expert's permuted rows are padded to a multiple of this
 PAIR_MIN_F, PAIR_MIN_T = 16384, 2048  # the library's grouped GEMMs pair m-blocks from these F and T on
 
@@ -722,14 +724,16 @@ def sub_line(inp, layer, x, steps, warmup, local_rank):
 # Token counts of the sweep across the switch from the weight-streaming decode
 # kernels (T <= 16) to the grouped tensor-core GEMMs, up to the compute-bound knee.
 BAND_TOKENS = (16, 17, 32, 64, 128, 256, 512, 1024)
+# int8 weights at decode token counts (the CUDA-core GEMV kernels take T <= 16)
+INT8_BAND_TOKENS = (1, 4, 12, 16)
 
 
-def band_sweep(inp, layer, x_all, steps, warmup, local_rank):
-    """The prefill weights at small token counts: step time, expert-weight bytes
-    per second (HBM-bound side) and flops per second (tensor-bound side)."""
+def band_sweep(inp, layer, x_all, steps, warmup, local_rank, tokens=BAND_TOKENS):
+    """The workload's weights at small token counts: step time, expert-weight
+    bytes per second (HBM-bound side) and flops per second (tensor-bound side)."""
     pk, _ = peaks()
     rows = []
-    for T in BAND_TOKENS:
+    for T in tokens:
         sub = synth_subset(inp, T)
         x = x_all[:T].contiguous()
         r = sub_line(sub, layer, x, steps, warmup, local_rank)
@@ -855,6 +859,17 @@ def run_ours(args, rank, world, local_rank):
                                scale_shape=(sub_inp.scale_experts, sub_inp.scale_groups))
             lines[name] = sub_line(sub_inp, lay, xs, args.steps, args.warmup, local_rank)
             lay.close()
+            if name == "int8_decode" and int8_dev is not None:
+                # the same int8 weights at the other decode token counts
+                band_inp = synth_subset(int8_dev[0], max(INT8_BAND_TOKENS))
+                xb = torch.from_numpy(band_inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+                lay = moe.MoeLayer(band_inp.d, band_inp.F, band_inp.T, w_dev, eps=band_inp.eps,
+                                   weight_dtype=band_inp.weight_dtype,
+                                   scale_shape=(band_inp.scale_experts, band_inp.scale_groups))
+                result["int8_band"] = band_sweep(band_inp, lay, xb, max(5, args.steps // 2), args.warmup,
+                                                 local_rank, tokens=INT8_BAND_TOKENS)
+                lay.close()
+                del xb
             if name == "int8":
                 int8_dev = (sub_inp, w_dev)
             elif name == "int8_decode":

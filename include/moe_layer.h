@@ -63,7 +63,7 @@ typedef enum { MOE_WEIGHT_BF16 = 0, MOE_WEIGHT_INT8 = 1 } moe_weight_dtype_t;
                                       also report fp16 saturation of their activations */
 #define MOE_FLAG_FORCE_TC 0x2u      /* always use the tensor-core grouped GEMM path */
 #define MOE_FLAG_FORCE_GEMV 0x4u    /* always use the weight-streaming decode path */
-#define MOE_FLAG_DECODE_TC 0x8u     /* int8 weights at T <= 8: run the tensor-core weight-streaming
+#define MOE_FLAG_DECODE_TC 0x8u     /* int8 weights at T <= 16: run the tensor-core weight-streaming
                                       kernels instead of the CUDA-core GEMV kernels */
 
 typedef struct {

@@ -1,9 +1,9 @@
-// Decode path with int8 weights for T <= 8: the expert GEMVs on the CUDA cores.
+// Decode path with int8 weights for T <= 16: the expert GEMVs on the CUDA cores.
 //
 // int8 weights with bf16 scales, one per expert and output channel
 // ("TevunahAi/Grok-1-BF16", "Conversion Details"; the (8, 1, N) scale shape).
-// With T <= 8 an expert holds at most 8 slot rows, so every weight byte is
-// used by at most 8 products.  The tensor-core form of this step (weights as
+// With T <= 16 an expert holds at most 16 slot rows, so every weight byte is
+// used by at most 16 products.  The tensor-core form of this step (weights as
 // the M = 128 operand, converted to fp16 in Tensor Memory, slots as N = 16)
 // is bounded by its MMA rate: each MMA moves 4 KB of fp16 A for 2 K weights
 // whatever N is.  Here each weight byte stays an int8 and is multiplied in the
@@ -29,10 +29,12 @@
 //
 // The slot rows are quantised once per forward, before each GEMV, by
 // quantize_slots_kernel (one warp per slot row and 128-element block), into a
-// compact buffer of 8 rows per expert (row 8 e + j: the expert's j-th slot),
+// compact buffer of 16 rows per expert (row 16 e + j: the expert's j-th slot),
 // each block stored in the order the compute lanes read it, and the block
-// scales transposed ([block][row]), so one TMA box brings an expert's 8 rows of
-// a block and another its 8 scales.
+// scales transposed ([block][row]).  A unit takes a group of up to 8 of an
+// expert's slots (slots 0-7, and 8-15 when the expert has more than 8, which
+// then reads its weights twice), so one TMA box brings the group's 8 rows of a
+// block and another their 8 scales.
 //
 // Data path per k-block of 128: TMA brings the int8 weight tile(s) (128 x 128,
 // 128-byte swizzle), the expert's 8 quantised rows (8 x 256 bytes) and their 8
@@ -51,15 +53,16 @@
 
 namespace moe {
 
-constexpr int kGv8NS = 8;                        // slot rows per expert (T <= 8)
+constexpr int kGv8NS = 8;                        // slot rows per unit (a group of an expert's slots)
+constexpr int kGv8SlotsPerExpert = 16;           // T <= 16: at most 16 slots on one expert
 constexpr int kGv8BK = 128;                      // K per stage: one 128-byte int8 row per weight row
 constexpr int kGv8Tile = 128 * kGv8BK;           // 16 KB: one int8 weight tile, 128 rows x 128
 constexpr int kGv8QRow = kGv8BK * 2;             // 256 B: one quantised block of a slot row, int16
-constexpr int kGv8QTile = kGv8NS * kGv8QRow;     // 2 KB: an expert's 8 rows
-constexpr int kGv8QRows = kNumExperts * kGv8NS;  // rows of the quantised buffer
+constexpr int kGv8QTile = kGv8NS * kGv8QRow;     // 2 KB: a slot group's 8 rows
+constexpr int kGv8QRows = kNumExperts * kGv8SlotsPerExpert;  // rows of the quantised buffer
 constexpr int kGv8CompWarp0 = 1;
 constexpr int kGv8CompWarps = 16;
-constexpr int kGv8MaxT = kGv8NS;
+constexpr int kGv8MaxT = kGv8SlotsPerExpert;
 constexpr int kGv8R = 4;  // weight rows per compute lane: two adjacent rows of each of the stage's two tiles
 
 // A unit's two 128-row weight tiles per k-block: up W and Wv rows [128 blk, +128)
@@ -97,8 +100,8 @@ __global__ void __launch_bounds__(256) quantize_slots_kernel(const uint16_t* __r
   const int row = row_of_slot[s], e = idx[s];
   if (e < 0 || e >= kNumExperts) return;  // (a routing index the grouping rejected)
   const int j = row - sched[kNumExperts + e];
-  if (j < 0 || j >= kGv8NS) return;
-  const int qrow = e * kGv8NS + j;
+  if (j < 0 || j >= kGv8SlotsPerExpert) return;
+  const int qrow = e * kGv8SlotsPerExpert + j;
   const uint2 raw = *reinterpret_cast<const uint2*>(rows + (size_t)row * K + kb * kGv8BK + 4 * lane);
   const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
   const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
@@ -184,27 +187,29 @@ __global__ void __launch_bounds__(GvI8Cfg<EPI>::kThreads, 1)
   auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (C::kStages + s); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // active experts (counts > 0), in expert order
-  int act_e[kNumExperts], n_act = 0;
+  // active slot groups 2 e + h (expert e has more than 8 h slots), in order
+  int grp[2 * kNumExperts], n_grp = 0;
 #pragma unroll
-  for (int e = 0; e < kNumExperts; ++e) act_e[e] = 0;
-  for (int e = 0; e < kNumExperts; ++e)
-    if (p.sched[e] > 0) act_e[n_act++] = e;
+  for (int q = 0; q < 2 * kNumExperts; ++q) grp[q] = 0;
+  for (int q = 0; q < 2 * kNumExperts; ++q)
+    if (p.sched[q >> 1] > kGv8NS * (q & 1)) grp[n_grp++] = q;
   const int blocks = (p.rows_per_expert + C::kUnitRows - 1) / C::kUnitRows;
-  const int num_units = n_act * blocks * p.ksplit;
+  const int num_units = n_grp * blocks * p.ksplit;
   const int kb_per_unit = p.K / kGv8BK / p.ksplit;
-  auto unit_of = [&](int u) {
+  // unit: expert e, its slots [s0, s0 + cnt) (s0 = 0 or 8), rows row0 = row_offset[e] + s0
+  auto unit_of = [&](int u, int& s0) {
     DecUnit d;
     const int kc = u % p.ksplit;
     const int rest = u / p.ksplit;
     d.blk = rest % blocks;
-    int ai = rest / blocks, e = 0;
-    for (int q = 0; q < kNumExperts; ++q)
-      if (q == ai) e = act_e[q];
-    d.e = e;
+    int ai = rest / blocks, g = 0;
+    for (int q = 0; q < 2 * kNumExperts; ++q)
+      if (q == ai) g = grp[q];
+    d.e = g >> 1;
+    s0 = kGv8NS * (g & 1);
     d.kc = kc;
-    d.row0 = p.sched[kNumExperts + e];
-    d.cnt = min(p.sched[e], kGv8NS);
+    d.row0 = p.sched[kNumExperts + d.e] + s0;
+    d.cnt = min(p.sched[d.e] - s0, kGv8NS);
     return d;
   };
 
@@ -232,8 +237,10 @@ __global__ void __launch_bounds__(GvI8Cfg<EPI>::kThreads, 1)
       int n_issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const DecUnit d = unit_of(u);
+        int s0;
+        const DecUnit d = unit_of(u, s0);
         const int wrow = d.e * p.rows_per_expert + d.blk * C::kUnitRows;
+        const int qrow = d.e * kGv8SlotsPerExpert + s0;
         for (int i = 0; i < kb_per_unit; ++i) {
           const int kb = d.kc * kb_per_unit + i;
           const int kx = kb * kGv8BK;
@@ -250,8 +257,8 @@ __global__ void __launch_bounds__(GvI8Cfg<EPI>::kThreads, 1)
           else
             tma_load_2d_hint(smem_addr(sb + kGv8Tile), &tm_w0, fb, kx, wrow + 128, stream_policy);
           uint8_t* qs = sb + 2 * kGv8Tile;
-          tma_load_2d(smem_addr(qs), &tm_xq, fb, kx, d.e * kGv8NS);
-          tma_load_2d(smem_addr(qs + kGv8QTile), &tm_xs, fb, d.e * kGv8NS, kb);
+          tma_load_2d(smem_addr(qs), &tm_xq, fb, kx, qrow);
+          tma_load_2d(smem_addr(qs + kGv8QTile), &tm_xs, fb, qrow, kb);
           ++n_issued;
           if (++stage == (uint32_t)C::kStages) {
             stage = 0;
@@ -282,7 +289,8 @@ __global__ void __launch_bounds__(GvI8Cfg<EPI>::kThreads, 1)
     bool ok = true;
     bool sat = false;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const DecUnit d = unit_of(u);
+      int s0;
+      const DecUnit d = unit_of(u, s0);
       // weight row (within the expert) of lane row r = 2 cb + tile, and whether it exists
       auto wrow_of = [&](int r) {
         return (EPI == kEpiGeglu) ? d.blk * 128 + col0 + (r >> 1) : d.blk * 256 + (r & 1) * 128 + col0 + (r >> 1);
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(GvI8Cfg<EPI>::kThreads, 1)
         const float keep = hi ? b2[v + kGv8R] : b2[v], send = hi ? b2[v] : b2[v + kGv8R];
         y[v] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
       }
-      const int t = c;  // this lane's slot
+      const int t = c;  // this lane's slot in the group
       const size_t se = (size_t)(p.scale_experts > 1 ? d.e : 0) * p.rows_per_expert;
       if (t < d.cnt) {
         if (EPI == kEpiGeglu) {  // columns n, n + 1: GELU(s_W h) * (s_Wv v)
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(GvI8Cfg<EPI>::kThreads, 1)
           *reinterpret_cast<uint32_t*>(out + (size_t)(d.row0 + t) * p.n_out + n) = pack_f16x2_sat(o[0], o[1]);
         } else {  // rows j, j + 1 of each tile: p * s_W1 * y
           const float ps = p.row_scale[d.row0 + t];
-          float* out = static_cast<float*>(p.out) + ((size_t)(d.kc * kNumExperts + d.e) * kDecNS + t) * p.n_out;
+          float* out = static_cast<float*>(p.out) + ((size_t)(d.kc * kNumExperts + d.e) * kDecNS + s0 + t) * p.n_out;
 #pragma unroll
           for (int tile = 0; tile < 2; ++tile) {
             const int j = wrow_of(tile);

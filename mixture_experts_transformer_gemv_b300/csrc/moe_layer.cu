@@ -11,8 +11,8 @@
 //   K4 grouped_gemm<down>   Y = p * (act W1^T)                   (tcgen05)
 //   K5 combine_kernel       out = x + RMSNorm_post(Y[r0] + Y[r1])
 // For T <= 16 (or MOE_FLAG_FORCE_GEMV) K3/K4 are replaced by the weight-streaming
-// decode kernels (k_decode.cuh for bf16 weights, k_decode_i8.cuh for int8; int8 at
-// T <= 8 by the CUDA-core GEMV kernels of k_gemv_i8.cuh unless MOE_FLAG_DECODE_TC)
+// decode kernels (k_decode.cuh for bf16 weights; for int8 the CUDA-core GEMV kernels
+// of k_gemv_i8.cuh, or with MOE_FLAG_DECODE_TC the tensor-core ones of k_decode_i8.cuh)
 // and K5 sums their split-K partials.  int8 weights are converted to fp16 on chip and
 // their per-channel scales applied in the epilogues.  The allocation-free
 // grouping entry point (end of file) runs permute_kernel, K2's grouping alone.
@@ -103,8 +103,8 @@ struct moe_layer {
   float* y_rows = nullptr;
   float* part = nullptr;  // decode path: [kDecMaxSplit][E][16][d] fp32 split-K partials
   float* p_part = nullptr;  // [router CTAs (<= max_T)][E] per-router-CTA sums of p
-  int16_t* xq = nullptr;    // int8 GEMV path: [E * 8][max(d, F)] slot rows in 16-bit fixed point
-  float* xqs = nullptr;     //                 [max(d, F) / 128][E * 8] their block scales
+  int16_t* xq = nullptr;    // int8 GEMV path: [E * 16][max(d, F)] slot rows in 16-bit fixed point
+  float* xqs = nullptr;     //                 [max(d, F) / 128][E * 16] their block scales
   int last_T = 0;           // tokens of the last forward enqueued (routing diagnostics)
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
@@ -218,7 +218,7 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
       int8 ? 1 : 0, L->sched, L->row_of_slot, L->token_of_row, L->prob_of_row, L->xn_perm, counts,
       (int)L->rows_cap, checks, L->err);
   mark(2);
-  // int8 weights at T <= 8: integer dot products on the CUDA cores (k_gemv_i8.cuh)
+  // int8 weights at T <= 16: integer dot products on the CUDA cores (k_gemv_i8.cuh)
   const bool gemv8 = decode && int8 && T <= kGv8MaxT && !(L->cfg.flags & MOE_FLAG_DECODE_TC);
   const bool grouped8 = L->cfg.scale_groups > 1;
   if (decode && int8) {
@@ -552,7 +552,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
     if (s == MOE_OK)
       s = make_tmap_i8(&L->tm_w18d, w->w1, F, kNumExperts * d, kDecBM, kDq8BK, CU_TENSOR_MAP_SWIZZLE_128B);
   }
-  if (i8) {  // int8 GEMV: an expert's 8 quantised rows of a block (256 B each) and their 8 scales
+  if (i8) {  // int8 GEMV: a slot group's 8 quantised rows of a block (256 B each) and their 8 scales
     if (s == MOE_OK)
       s = make_tmap_2d(&L->tm_xq_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, L->xq, d, kGv8QRows, kGv8BK, kGv8NS);
     if (s == MOE_OK)

@@ -68,7 +68,7 @@ def test_skew_shares_reported(grok):
 
 def test_int8_decode_full_shape():
     """int8 weights at the Grok-1 shape with T = 8 (the int8 workload's first 8
-    tokens): the CUDA-core GEMV kernels (the default at T <= 8) and the
+    tokens): the CUDA-core GEMV kernels (the default at T <= 16) and the
     tensor-core weight-streaming kernels (MOE_FLAG_DECODE_TC) against the oracle
     on every token."""
     from mixture_experts_transformer_gemv_b300 import build

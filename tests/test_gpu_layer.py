@@ -310,21 +310,23 @@ def test_int8_paired_mblocks_skewed():
 @pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_FORCE_TC, moe.MOE_FLAG_DECODE_TC])
 def test_int8_decode_path_and_forced_tensor_core_path(T, d, F, seed, flags):
     """int8 weights at T <= 16 run the int8 weight-streaming kernels unless the
-    grouped GEMMs are forced: at T <= 8 the CUDA-core GEMV kernels (integer dot
-    products), or with MOE_FLAG_DECODE_TC the tensor-core kernels (weights
-    converted into Tensor Memory), which T = 9..16 always take."""
+    grouped GEMMs are forced: the CUDA-core GEMV kernels (integer dot products),
+    or with MOE_FLAG_DECODE_TC the tensor-core kernels (weights converted into
+    Tensor Memory).  T = 9 and 16 can put more than 8 slots on one expert (two
+    slot groups in the GEMV)."""
     inp = synth.make_inputs(T, d, F, seed, name=f"int8dec{T}x{d}x{F}", weight_dtype="int8")
     _full_check(inp, flags=flags)
 
 
 def test_int8_decode_one_expert_heavy_batch():
-    """All 16 tokens to expert 6, int8 weights: decode and grouped-GEMM paths."""
+    """All 16 tokens to expert 6, int8 weights (two full slot groups of 8 in the
+    GEMV kernels): GEMV, tensor-core decode and grouped-GEMM paths."""
     inp = synth.make_inputs(16, 384, 640, 79, name="int8dec_onehot", weight_dtype="int8")
     b = np.zeros(8, np.float32)
     b[6] = 1e4
     inp.bias = b
     ref = oracle.moe_tokens(inp)
-    for flags in (0, moe.MOE_FLAG_FORCE_TC, moe.MOE_FLAG_FORCE_GEMV):
+    for flags in (0, moe.MOE_FLAG_FORCE_TC, moe.MOE_FLAG_FORCE_GEMV, moe.MOE_FLAG_DECODE_TC):
         layer = make_layer(inp, flags=flags)
         y, idx, prob, counts = run(layer, inp)
         assert counts[6] == 16
@@ -334,7 +336,8 @@ def test_int8_decode_one_expert_heavy_batch():
 
 def test_int8_gemv_eight_slots_on_one_expert():
     """T = 8 with every token's first choice on expert 6: eight slot rows on one
-    expert, the most the CUDA-core GEMV kernels take; both int8 decode kernels."""
+    expert, one full slot group of the CUDA-core GEMV kernels; both int8 decode
+    kernels."""
     inp = synth.make_inputs(8, 384, 640, 85, name="int8gemv_onehot", weight_dtype="int8")
     b = np.zeros(8, np.float32)
     b[6] = 1e4
