@@ -185,10 +185,12 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(
 #pragma unroll
               for (int j = 0; j < 8; ++j) g[j] = s8[j] * g[j];
             }
+            // element-major over the tokens: the 4 tokens' sums advance together
+            // (each still takes the elements in order)
 #pragma unroll
-            for (int i = 0; i < kRouterWTok; ++i)
+            for (int j = 0; j < 8; ++j)
 #pragma unroll
-              for (int j = 0; j < 8; ++j) lg[i][e] = fmaf(xf[i][j], g[j], lg[i][e]);
+              for (int i = 0; i < kRouterWTok; ++i) lg[i][e] = fmaf(xf[i][j], g[j], lg[i][e]);
           }
         }
         load(k0 + q + kRouterDepth, buf[q]);
@@ -227,6 +229,111 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(
       pp[0] = make_float4(p[0], p[1], p[2], p[3]);
       pp[1] = make_float4(p[4], p[5], p[6], p[7]);
     }
+  }
+}
+
+// Small batches (T <= kRouterSmallT, d <= 32 * 8 * kRouterSmallK): one warp
+// per token and CTA, with exactly the arithmetic of router_kernel (same chunks
+// per lane in the same order, the same products s_pre_j G[e, j], the same
+// butterfly), so a token routes the same to the last bit in any batch.  The
+// difference is latency: the lane issues the loads of all its chunks of x at
+// once, and the gate and s_pre arrive in shared memory by bulk copies (no
+// staging loop); the products s_pre_j G[e, j] are formed as they are used.
+constexpr int kRouterSmallT = 16;
+constexpr int kRouterSmallK = 24;  // chunks per lane held in registers (d <= 6144)
+
+// Shared memory of router_small_kernel: G [8][d], s_pre [d] (fp32), one mbarrier.
+__host__ __device__ constexpr size_t router_small_smem(int d) { return (size_t)(kNumExperts + 1) * d * 4 + 16; }
+
+__global__ void __launch_bounds__(32, 1) router_small_kernel(
+    const __nv_bfloat16* __restrict__ x, int d, const float* __restrict__ gate, const float* __restrict__ gate_bias,
+    const float* __restrict__ s_pre, float eps, float* __restrict__ rnorm_out, int32_t* __restrict__ idx_out,
+    float* __restrict__ prob_out, int32_t* __restrict__ user_idx, float* __restrict__ user_prob,
+    float* __restrict__ p_part, uint32_t* __restrict__ err, uint64_t timeout_ns) {
+  extern __shared__ __align__(16) uint8_t router_smem[];
+  const float* gm = reinterpret_cast<const float*>(router_smem);   // G [8][d]
+  const float* sm = gm + (size_t)kNumExperts * d;                   // s_pre [d]
+  const uint32_t bar = smem_addr(router_smem + (size_t)(kNumExperts + 1) * d * 4);
+  const int lane = threadIdx.x;
+  const int t = blockIdx.x;
+  const int nchunk = d >> 3;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    constexpr uint32_t kPiece = 16384;
+    const uint32_t gbytes = (uint32_t)kNumExperts * d * 4, sbytes = (uint32_t)d * 4;
+    mbar_arrive_expect_tx(bar, gbytes + sbytes);
+    for (uint32_t o = 0; o < gbytes; o += kPiece)
+      bulk_load(smem_addr(router_smem) + o, reinterpret_cast<const uint8_t*>(gate) + o, min(kPiece, gbytes - o), bar);
+    for (uint32_t o = 0; o < sbytes; o += kPiece)
+      bulk_load(smem_addr(router_smem) + gbytes + o, reinterpret_cast<const uint8_t*>(s_pre) + o,
+                min(kPiece, sbytes - o), bar);
+  }
+  uint4 xv[kRouterSmallK];
+#pragma unroll
+  for (int k = 0; k < kRouterSmallK; ++k) {
+    const int c = lane + 32 * k;
+    xv[k] = c < nchunk ? ld_nc_v4(x + (size_t)t * d + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
+  }
+  if (!__all_sync(0xffffffffu, wait_bounded(bar, 0, nullptr, timeout_ns))) {
+    if (lane == 0) atomicOr(err, kErrTimeout);
+    wait_bounded(bar, 0, nullptr, timeout_ns);  // the copies land before the CTA exits
+    return;
+  }
+  float ss = 0.f, lg[kNumExperts];
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) lg[e] = 0.f;
+#pragma unroll
+  for (int k = 0; k < kRouterSmallK; ++k) {
+    const int c = lane + 32 * k;
+    if (c < nchunk) {
+      float xf[8];
+      const uint32_t w[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        xf[2 * h] = bf16_lo(w[h]);
+        xf[2 * h + 1] = bf16_hi(w[h]);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(xf[j], xf[j], ss);
+      const float4 sa = *reinterpret_cast<const float4*>(sm + (size_t)c * 8);
+      const float4 sb = *reinterpret_cast<const float4*>(sm + (size_t)c * 8 + 4);
+      const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+      float g[kNumExperts][8];
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) {
+        const float4 a = *reinterpret_cast<const float4*>(gm + (size_t)e * d + (size_t)c * 8);
+        const float4 b = *reinterpret_cast<const float4*>(gm + (size_t)e * d + (size_t)c * 8 + 4);
+        g[e][0] = a.x; g[e][1] = a.y; g[e][2] = a.z; g[e][3] = a.w;
+        g[e][4] = b.x; g[e][5] = b.y; g[e][6] = b.z; g[e][7] = b.w;
+      }
+      // element-major: the 8 experts' sums advance together (each sum still
+      // takes the elements in order), so consecutive FMAs are independent
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < kNumExperts; ++e) lg[e] = fmaf(xf[j], s8[j] * g[e][j], lg[e]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lg[e] += __shfl_xor_sync(0xffffffffu, lg[e], o);
+  if (lane == 0) {
+    const float r = 1.0f / sqrtf(ss / (float)d + eps);
+    float l[kNumExperts], p[kNumExperts];
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) l[e] = r * lg[e] + (gate_bias ? gate_bias[e] : 0.f);
+    softmax_top2(l, t, idx_out, prob_out, user_idx, user_prob, p);
+    rnorm_out[t] = r;
+    float4* pp = reinterpret_cast<float4*>(p_part + (size_t)t * kNumExperts);
+    pp[0] = make_float4(p[0], p[1], p[2], p[3]);
+    pp[1] = make_float4(p[4], p[5], p[6], p[7]);
   }
 }
 

@@ -109,6 +109,7 @@ struct moe_layer {
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
   bool router_gsmem = false;     // the router's scaled gate s_pre (.) G fits one CTA's shared memory
+  bool router_small = false;     // T <= kRouterSmallT: router_small_kernel (G and s_pre fit shared memory)
   bool pair_mblocks = false;     // F >= kPairMinF: forwards with T >= kPairMinT pair two m-blocks per tile
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
@@ -194,7 +195,12 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   // use, and the CTAs get 4 tokens per warp (fewer reads).
   {
     const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
-    if (L->router_gsmem) {
+    if (L->router_small && T <= kRouterSmallT) {
+      router_small_kernel<<<T, 32, router_small_smem(d), st>>>(xh, d, L->w.gate, L->w.gate_bias,
+                                                              L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx,
+                                                              L->prob, topk_idx, topk_prob, L->p_part, L->err,
+                                                              kWaitLimitNs);
+    } else if (L->router_gsmem) {
       const int grid = std::min(L->num_sms, T);
       router_kernel<true><<<grid, kRouterThreads, (size_t)kNumExperts * d * 4, st>>>(
           xh, T, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx, L->prob, topk_idx,
@@ -210,10 +216,13 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   mark(1);
   // grouping + normed rows in expert order; int8 layers multiply in fp16 (int8 ->
   // fp16 is one shuffle and one subtraction), so their activation rows are fp16
-  // 4 CTAs per SM (memory parallelism for the row copies, and every SM zeroing
-  // padding rows even for a few tokens); every CTA reads all of idx, so beyond
-  // 16384 tokens one CTA per SM
-  group_rows_kernel<<<T <= 16384 ? 4 * L->num_sms : L->num_sms, kGroupThreads, 0, st>>>(
+  // 4 CTAs per SM (memory parallelism for the row copies); every CTA reads all of
+  // idx and does the counting, so beyond 16384 tokens one CTA per SM, and for a
+  // decode-sized batch one CTA per two SMs (a few rows to copy, up to 8 x 127
+  // padding rows to zero: at T = 8 the 592-CTA grid spent 20 us on its per-CTA
+  // counting)
+  const int group_grid = T <= 64 ? std::max(1, L->num_sms / 2) : (T <= 16384 ? 4 * L->num_sms : L->num_sms);
+  group_rows_kernel<<<group_grid, kGroupThreads, 0, st>>>(
       L->idx, L->prob, T, static_cast<const __nv_bfloat16*>(hidden), L->rnorm, L->w.pre_norm_scale, d,
       int8 ? 1 : 0, L->sched, L->row_of_slot, L->token_of_row, L->prob_of_row, L->xn_perm, counts,
       (int)L->rows_cap, checks, L->err);
@@ -564,6 +573,17 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
+  {
+    // small batches: G and s_pre (36 d bytes) bulk-copied into shared memory, d <= 6144
+    const size_t ssm = router_small_smem((int)d);
+    if (d <= 32 * 8 * kRouterSmallK && ssm <= (size_t)prop.sharedMemPerBlockOptin) {
+      if (cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm) ==
+          cudaSuccess)
+        L->router_small = true;
+      else
+        cudaGetLastError();
+    }
+  }
   {
     // the router keeps the scaled gate (32 d bytes) in shared memory where it fits
     const size_t gsm = (size_t)kNumExperts * d * 4;

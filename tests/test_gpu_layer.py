@@ -61,13 +61,15 @@ def test_routing_does_not_depend_on_the_batch(T, d, seed):
     warp that takes it, its position, T), with the gate in shared memory (d =
     256) or read from L2 (d = 7680): a token routes the same to the last bit
     (expert pair and probabilities) in the whole batch, in a prefix, in a suffix
-    and alone (T = 1, the decode path's size)."""
+    and alone (T = 1, the decode path's size); up to 16 tokens the router runs
+    as one CTA per token (router_small_kernel, the 12-token run), beyond that
+    as warps over runs of tokens."""
     inp = synth.make_inputs(T, d, 256, seed, name=f"router_batch{T}x{d}")
     layer = make_layer(inp)
     x = bf16_tensor(inp.x)
     _, idx_a, prob_a, _ = layer.forward(x, routing=True)
     idx_a, prob_a = idx_a.clone(), prob_a.clone()
-    for lo, hi in ((0, T - 1), (T - 37, T), (T // 2, T // 2 + 1)):
+    for lo, hi in ((0, T - 1), (T - 37, T), (T // 2, T // 2 + 1), (5, 17)):
         _, idx_b, prob_b, _ = layer.forward(x[lo:hi].contiguous(), routing=True)
         torch.cuda.synchronize()
         assert torch.equal(idx_a[lo:hi], idx_b), (lo, hi)
