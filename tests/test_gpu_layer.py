@@ -547,3 +547,22 @@ def test_forward_captured_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out_static, direct)
     layer.close()
+
+
+@pytest.mark.parametrize("shape", [(8, 8), (8, 1)])
+def test_int8_gemv_two_slot_groups(shape):
+    """T = 13 with every first choice on expert 3: 13 slots on one expert, two
+    slot groups (8 + 5) in the int8 GEMV kernels, with per-channel and grouped
+    scales; both int8 decode kernels against the oracle."""
+    inp = synth.make_inputs(13, 1024, 1024, 97 + shape[1], name=f"int8gemv_groups_{shape}", weight_dtype="int8",
+                            int8_scale_shape=shape)
+    b = np.zeros(8, np.float32)
+    b[3] = 1e4
+    inp.bias = b
+    ref = oracle.moe_tokens(inp)
+    for flags in (0, moe.MOE_FLAG_DECODE_TC):
+        layer = make_layer(inp, flags=flags)
+        y, idx, prob, counts = run(layer, inp)
+        assert counts[3] == 13
+        assert_values(y, ref.y, f"int8gemv_groups {shape} flags={flags}")
+        layer.close()
