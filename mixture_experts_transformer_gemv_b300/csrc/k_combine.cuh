@@ -17,6 +17,7 @@ namespace moe {
 
 constexpr int kCombineThreads = 256;  // per token for large T; 1024 for T below the SM count
 constexpr int kCombineVec = 16;       // largest float4 count per thread kept in registers: d <= 16384
+constexpr int kDecMaxSplitCombine = 8;  // largest split of the decode path's down projection
 
 // kSplit = false: Y rows of the grouped GEMM path, Y[row] = p * o.
 // kSplit = true:  decode path, o split over `ksplit` reduction chunks:
@@ -55,18 +56,24 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(
     y1 = reinterpret_cast<const float4*>(y_rows + (size_t)r1 * d);
   }
   const int nv = d >> 2;
+  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d);
   float4 m[VEC];
+  uint2 xv[VEC];  // the residual row, read before the reduction (and before any aliasing write)
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < VEC; ++i) {
     const int c = threadIdx.x + i * THREADS;
     if (c < nv) {
+      xv[i] = xr[c];
       float4 a = y0[c], b = y1[c];
-      if (kSplit) {
-        for (int kc = 1; kc < ksplit; ++kc) {
-          const float4 a2 = y0[kc * kc_stride + c], b2 = y1[kc * kc_stride + c];
-          a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
-          b = make_float4(b.x + b2.x, b.y + b2.y, b.z + b2.z, b.w + b2.w);
+      if (kSplit) {  // unrolled to the largest split: every part's loads in flight at once
+#pragma unroll
+        for (int kc = 1; kc < kDecMaxSplitCombine; ++kc) {
+          if (kc < ksplit) {
+            const float4 a2 = y0[kc * kc_stride + c], b2 = y1[kc * kc_stride + c];
+            a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
+            b = make_float4(b.x + b2.x, b.y + b2.y, b.z + b2.z, b.w + b2.w);
+          }
         }
       }
       m[i] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
@@ -85,17 +92,15 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(
   for (int w = 0; w < THREADS / 32; ++w) tot += red[w];
   const float rr = 1.0f / sqrtf(tot / (float)d + eps);
 
-  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d);
   uint2* orow = reinterpret_cast<uint2*>(out + (size_t)t * d);
 #pragma unroll
   for (int i = 0; i < VEC; ++i) {
     const int c = threadIdx.x + i * THREADS;
     if (c < nv) {
       const float4 s = reinterpret_cast<const float4*>(s_post)[c];
-      const uint2 xv = xr[c];  // read before the (possibly aliasing) write below
       uint2 o;
-      o.x = pack_bf16x2(bf16_lo(xv.x) + m[i].x * rr * s.x, bf16_hi(xv.x) + m[i].y * rr * s.y);
-      o.y = pack_bf16x2(bf16_lo(xv.y) + m[i].z * rr * s.z, bf16_hi(xv.y) + m[i].w * rr * s.w);
+      o.x = pack_bf16x2(bf16_lo(xv[i].x) + m[i].x * rr * s.x, bf16_hi(xv[i].x) + m[i].y * rr * s.y);
+      o.y = pack_bf16x2(bf16_lo(xv[i].y) + m[i].z * rr * s.z, bf16_hi(xv[i].y) + m[i].w * rr * s.w);
       orow[c] = o;
     }
   }

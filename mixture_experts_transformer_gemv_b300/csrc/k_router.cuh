@@ -239,6 +239,13 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(
 // difference is latency: the lane issues the loads of all its chunks of x at
 // once, and the gate and s_pre arrive in shared memory by bulk copies (no
 // staging loop); the products s_pre_j G[e, j] are formed as they are used.
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 constexpr int kRouterSmallT = 16;
 constexpr int kRouterSmallK = 24;  // chunks per lane held in registers (d <= 6144)
 

@@ -45,6 +45,7 @@ using namespace moe_host;
 
 namespace {
 
+static_assert(kDecMaxSplitCombine == kDecMaxSplit, "the combine unrolls to the decode split");
 static_assert(kGemmBK == kDecBK && kGemmBK == kTmapBoxInner, "every bf16 GEMM operand box is 64 elements wide");
 
 // Row-major 2-D int8 tensor [rows, inner], box [box_rows, box_inner]: the staging
