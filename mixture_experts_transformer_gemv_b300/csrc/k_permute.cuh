@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_rows_kernel(
     bool sat = false;
 #pragma unroll 8
     for (int ch = lane; ch < nchunk; ch += 32) {
-      const uint4 xv = ld_nc_v4(src + (size_t)ch * 8);
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(src) + ch);  // (plain loads: the unrolled
+                                                                      // iterations' loads issue together)
       const float4 sa = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)ch * 8));
       const float4 sb = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)ch * 8 + 4));
       uint4 v;

@@ -232,73 +232,70 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(
   }
 }
 
-// Small batches (T <= kRouterSmallT, d <= 32 * 8 * kRouterSmallK): one warp
-// per token and CTA, with exactly the arithmetic of router_kernel (same chunks
-// per lane in the same order, the same products s_pre_j G[e, j], the same
-// butterfly), so a token routes the same to the last bit in any batch.  The
-// difference is latency: the lane issues the loads of all its chunks of x at
-// once, and the gate and s_pre arrive in shared memory by bulk copies (no
-// staging loop); the products s_pre_j G[e, j] are formed as they are used.
-// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
-// from global memory into this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
+// Small batches (T <= kRouterSmallT, d <= 32 * 8 * kRouterSmallK): each token
+// is split over kRouterSlices CTAs, with exactly the arithmetic of
+// router_kernel, so a token routes the same to the last bit in any batch.  In
+// router_kernel lane l of a warp sums the chunks c = l + 32 k of the token in
+// order (sum of squares and the 8 sums x_j (s_pre_j G[e, j])), then the warp's
+// xor butterfly adds the 32 lanes' sums.  Here "virtual lane" l is computed by
+// one thread of CTA (t, l / 4) over the same chunks in the same order, from
+// shared memory that its CTA filled with those chunks' G, s_pre and x (28.5 KB
+// instead of the whole 221 KB gate for one token on one SM); the 9 sums of
+// every virtual lane go to part[t][l], and the token's last CTA to finish
+// (a counter per token, reset by that CTA) loads the 32 sets into the lanes of
+// one warp and runs the same butterfly, softmax and top-2.
 constexpr int kRouterSmallT = 16;
-constexpr int kRouterSmallK = 24;  // chunks per lane held in registers (d <= 6144)
+constexpr int kRouterSlices = 8;                             // CTAs per token
+constexpr int kRouterSliceLanes = 32 / kRouterSlices;        // virtual lanes per CTA
+constexpr int kRouterSmallK = 24;                            // chunks per virtual lane (d <= 6144)
+constexpr int kRouterSplitThreads = kRouterSliceLanes * kRouterSmallK;  // one (lane, chunk) each to stage
+constexpr int kRouterPartFloats = 32 * (1 + kNumExperts);    // per token: 32 virtual lanes x 9 sums
 
-// Shared memory of router_small_kernel: G [8][d], s_pre [d] (fp32), one mbarrier.
-__host__ __device__ constexpr size_t router_small_smem(int d) { return (size_t)(kNumExperts + 1) * d * 4 + 16; }
-
-__global__ void __launch_bounds__(32, 1) router_small_kernel(
+__global__ void __launch_bounds__(kRouterSplitThreads) router_split_kernel(
     const __nv_bfloat16* __restrict__ x, int d, const float* __restrict__ gate, const float* __restrict__ gate_bias,
     const float* __restrict__ s_pre, float eps, float* __restrict__ rnorm_out, int32_t* __restrict__ idx_out,
     float* __restrict__ prob_out, int32_t* __restrict__ user_idx, float* __restrict__ user_prob,
-    float* __restrict__ p_part, uint32_t* __restrict__ err, uint64_t timeout_ns) {
-  extern __shared__ __align__(16) uint8_t router_smem[];
-  const float* gm = reinterpret_cast<const float*>(router_smem);   // G [8][d]
-  const float* sm = gm + (size_t)kNumExperts * d;                   // s_pre [d]
-  const uint32_t bar = smem_addr(router_smem + (size_t)(kNumExperts + 1) * d * 4);
-  const int lane = threadIdx.x;
-  const int t = blockIdx.x;
+    float* __restrict__ p_part, float* __restrict__ part, int32_t* __restrict__ done) {
+  __shared__ __align__(16) float gsl[kRouterSliceLanes][kRouterSmallK][kNumExperts][8];
+  __shared__ __align__(16) float ssl[kRouterSliceLanes][kRouterSmallK][8];
+  __shared__ __align__(16) uint4 xsl[kRouterSliceLanes][kRouterSmallK];
+  __shared__ int last;
+  const int t = blockIdx.x, slice = blockIdx.y, tid = threadIdx.x;
   const int nchunk = d >> 3;
-  if (lane == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  if (lane == 0) {
-    constexpr uint32_t kPiece = 16384;
-    const uint32_t gbytes = (uint32_t)kNumExperts * d * 4, sbytes = (uint32_t)d * 4;
-    mbar_arrive_expect_tx(bar, gbytes + sbytes);
-    for (uint32_t o = 0; o < gbytes; o += kPiece)
-      bulk_load(smem_addr(router_smem) + o, reinterpret_cast<const uint8_t*>(gate) + o, min(kPiece, gbytes - o), bar);
-    for (uint32_t o = 0; o < sbytes; o += kPiece)
-      bulk_load(smem_addr(router_smem) + gbytes + o, reinterpret_cast<const uint8_t*>(s_pre) + o,
-                min(kPiece, sbytes - o), bar);
-  }
-  uint4 xv[kRouterSmallK];
-#pragma unroll
-  for (int k = 0; k < kRouterSmallK; ++k) {
-    const int c = lane + 32 * k;
-    xv[k] = c < nchunk ? ld_nc_v4(x + (size_t)t * d + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
-  }
-  if (!__all_sync(0xffffffffu, wait_bounded(bar, 0, nullptr, timeout_ns))) {
-    if (lane == 0) atomicOr(err, kErrTimeout);
-    wait_bounded(bar, 0, nullptr, timeout_ns);  // the copies land before the CTA exits
-    return;
-  }
-  float ss = 0.f, lg[kNumExperts];
-#pragma unroll
-  for (int e = 0; e < kNumExperts; ++e) lg[e] = 0.f;
-#pragma unroll
-  for (int k = 0; k < kRouterSmallK; ++k) {
-    const int c = lane + 32 * k;
+  {  // stage chunk k of virtual lane v: G (8 experts), s_pre and x
+    const int v = tid / kRouterSmallK, k = tid % kRouterSmallK;
+    const int c = slice * kRouterSliceLanes + v + 32 * k;
     if (c < nchunk) {
+      float4 g[2 * kNumExperts];
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) {
+        g[2 * e] = __ldg(reinterpret_cast<const float4*>(gate + (size_t)e * d + (size_t)c * 8));
+        g[2 * e + 1] = __ldg(reinterpret_cast<const float4*>(gate + (size_t)e * d + (size_t)c * 8 + 4));
+      }
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)c * 8));
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)c * 8 + 4));
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + c);
+#pragma unroll
+      for (int e = 0; e < kNumExperts; ++e) {
+        reinterpret_cast<float4*>(gsl[v][k][e])[0] = g[2 * e];
+        reinterpret_cast<float4*>(gsl[v][k][e])[1] = g[2 * e + 1];
+      }
+      reinterpret_cast<float4*>(ssl[v][k])[0] = s0;
+      reinterpret_cast<float4*>(ssl[v][k])[1] = s1;
+      xsl[v][k] = xv;
+    }
+  }
+  __syncthreads();
+  if (tid < kRouterSliceLanes) {  // virtual lane l: its chunks in order, as a lane of router_kernel
+    const int l = slice * kRouterSliceLanes + tid;
+    float ss = 0.f, lg[kNumExperts];
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) lg[e] = 0.f;
+    for (int k = 0; k < kRouterSmallK; ++k) {
+      if (l + 32 * k >= nchunk) break;
+      const uint4 xv = xsl[tid][k];
+      const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
       float xf[8];
-      const uint32_t w[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         xf[2 * h] = bf16_lo(w[h]);
@@ -306,32 +303,37 @@ __global__ void __launch_bounds__(32, 1) router_small_kernel(
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) ss = fmaf(xf[j], xf[j], ss);
-      const float4 sa = *reinterpret_cast<const float4*>(sm + (size_t)c * 8);
-      const float4 sb = *reinterpret_cast<const float4*>(sm + (size_t)c * 8 + 4);
-      const float s8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-      float g[kNumExperts][8];
 #pragma unroll
-      for (int e = 0; e < kNumExperts; ++e) {
-        const float4 a = *reinterpret_cast<const float4*>(gm + (size_t)e * d + (size_t)c * 8);
-        const float4 b = *reinterpret_cast<const float4*>(gm + (size_t)e * d + (size_t)c * 8 + 4);
-        g[e][0] = a.x; g[e][1] = a.y; g[e][2] = a.z; g[e][3] = a.w;
-        g[e][4] = b.x; g[e][5] = b.y; g[e][6] = b.z; g[e][7] = b.w;
+      for (int j = 0; j < 8; ++j) {
+        const float sj = ssl[tid][k][j];
+#pragma unroll
+        for (int e = 0; e < kNumExperts; ++e) lg[e] = fmaf(xf[j], sj * gsl[tid][k][e][j], lg[e]);
       }
-      // element-major: the 8 experts' sums advance together (each sum still
-      // takes the elements in order), so consecutive FMAs are independent
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < kNumExperts; ++e) lg[e] = fmaf(xf[j], s8[j] * g[e][j], lg[e]);
     }
+    float* pl = part + (size_t)t * kRouterPartFloats + (size_t)l * (1 + kNumExperts);
+    pl[0] = ss;
+#pragma unroll
+    for (int e = 0; e < kNumExperts; ++e) pl[1 + e] = lg[e];
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(done + t, 1) == kRouterSlices - 1;
+  __syncthreads();
+  if (!last || tid >= 32) return;
+  __threadfence();
+  // the token's last CTA: virtual lane = lane, then router_kernel's butterfly
+  const float* pl = part + (size_t)t * kRouterPartFloats + (size_t)tid * (1 + kNumExperts);
+  float ss = __ldcg(pl), lg[kNumExperts];
+#pragma unroll
+  for (int e = 0; e < kNumExperts; ++e) lg[e] = __ldcg(pl + 1 + e);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
 #pragma unroll
   for (int e = 0; e < kNumExperts; ++e)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lg[e] += __shfl_xor_sync(0xffffffffu, lg[e], o);
-  if (lane == 0) {
+  if (tid == 0) {
+    done[t] = 0;  // for the next forward (stream order)
     const float r = 1.0f / sqrtf(ss / (float)d + eps);
     float l[kNumExperts], p[kNumExperts];
 #pragma unroll

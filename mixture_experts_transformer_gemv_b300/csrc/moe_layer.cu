@@ -110,7 +110,9 @@ struct moe_layer {
   uint32_t* err = nullptr;
   int ksplit = 1;         // decode path: chunks of the down-projection reduction
   bool router_gsmem = false;     // the router's scaled gate s_pre (.) G fits one CTA's shared memory
-  bool router_small = false;     // T <= kRouterSmallT: router_small_kernel (G and s_pre fit shared memory)
+  bool router_small = false;     // T <= kRouterSmallT and d <= 6144: router_split_kernel
+  float* router_part = nullptr;  // [kRouterSmallT][32][9] per-virtual-lane sums of router_split_kernel
+  int32_t* router_done = nullptr;  // [kRouterSmallT] its per-token counters (zero between forwards)
   bool pair_mblocks = false;     // F >= kPairMinF: forwards with T >= kPairMinT pair two m-blocks per tile
   int ksplit_i8 = 1;      // the same for the int8 decode kernel (128-wide k-blocks)
 
@@ -197,10 +199,9 @@ moe_status_t enqueue_forward(moe_layer* L, const void* hidden, void* out, int T,
   {
     const __nv_bfloat16* xh = static_cast<const __nv_bfloat16*>(hidden);
     if (L->router_small && T <= kRouterSmallT) {
-      router_small_kernel<<<T, 32, router_small_smem(d), st>>>(xh, d, L->w.gate, L->w.gate_bias,
-                                                              L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx,
-                                                              L->prob, topk_idx, topk_prob, L->p_part, L->err,
-                                                              kWaitLimitNs);
+      router_split_kernel<<<dim3(T, kRouterSlices), kRouterSplitThreads, 0, st>>>(
+          xh, d, L->w.gate, L->w.gate_bias, L->w.pre_norm_scale, L->cfg.eps, L->rnorm, L->idx, L->prob, topk_idx,
+          topk_prob, L->p_part, L->router_part, L->router_done);
     } else if (L->router_gsmem) {
       const int grid = std::min(L->num_sms, T);
       router_kernel<true><<<grid, kRouterThreads, (size_t)kNumExperts * d * 4, st>>>(
@@ -498,15 +499,16 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   // one workspace block, every buffer 1 KB aligned
   const int64_t kq = std::max(d, F);
   const bool i8 = c.weight_dtype == MOE_WEIGHT_INT8;
-  size_t offs[15], total = 0;
-  const size_t sizes[15] = {(size_t)(T * 4), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
+  size_t offs[16], total = 0;
+  const size_t sizes[16] = {(size_t)(T * 4), (size_t)(T * 2 * 4), (size_t)(T * 2 * 4), 256,
                             (size_t)(T * 2 * 4), (size_t)(R * 4),     (size_t)(R * 4),     (size_t)(R * d * 2),
                             (size_t)(R * F * 2), (size_t)(R * d * 4), 256,
                             (size_t)kDecMaxSplit * kNumExperts * kDecNS * d * 4,
                             (size_t)T * kNumExperts * 4,
                             i8 ? (size_t)kGv8QRows * kq * 2 : 0,
-                            i8 ? (size_t)(kq / kGv8BK) * kGv8QRows * 4 : 0};
-  for (int i = 0; i < 15; ++i) {
+                            i8 ? (size_t)(kq / kGv8BK) * kGv8QRows * 4 : 0,
+                            (size_t)kRouterSmallT * (kRouterPartFloats + 1) * 4};
+  for (int i = 0; i < 16; ++i) {
     offs[i] = total;
     total = align_up(total + sizes[i], 1024);
   }
@@ -532,6 +534,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   L->p_part = reinterpret_cast<float*>(b + offs[12]);
   L->xq = reinterpret_cast<int16_t*>(b + offs[13]);
   L->xqs = reinterpret_cast<float*>(b + offs[14]);
+  L->router_part = reinterpret_cast<float*>(b + offs[15]);
+  L->router_done = reinterpret_cast<int32_t*>(L->router_part + (size_t)kRouterSmallT * kRouterPartFloats);
   // decode-path split of the F reduction: up to kDecMaxSplit chunks of whole 64-wide blocks
   L->ksplit = kDecMaxSplit;
   while (L->ksplit > 1 && (F / kDecBK) % L->ksplit) L->ksplit /= 2;
@@ -574,17 +578,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w, m
   }
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_xn_perm16, L->xn_perm, d, R, kDecNS);
   if (s == MOE_OK) s = make_tmap_bf16(&L->tm_act16, L->act, F, R, kDecNS);
-  {
-    // small batches: G and s_pre (36 d bytes) bulk-copied into shared memory, d <= 6144
-    const size_t ssm = router_small_smem((int)d);
-    if (d <= 32 * 8 * kRouterSmallK && ssm <= (size_t)prop.sharedMemPerBlockOptin) {
-      if (cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm) ==
-          cudaSuccess)
-        L->router_small = true;
-      else
-        cudaGetLastError();
-    }
-  }
+  L->router_small = d <= 32 * 8 * kRouterSmallK;  // small batches: router_split_kernel
   {
     // the router keeps the scaled gate (32 d bytes) in shared memory where it fits
     const size_t gsm = (size_t)kNumExperts * d * 4;
