@@ -16,6 +16,7 @@
 // the gather, which forms the normed rows and puts them in expert order, runs
 // on all SMs.
 #pragma once
+#include <type_traits>
 #include "common.cuh"
 
 namespace moe {
@@ -261,18 +262,23 @@ __global__ void __launch_bounds__(kGroupThreads) group_rows_kernel(
     __syncthreads();
   }
 
-  // ---- 3. each token's normed row, written to both of its rows
+  // ---- 3. each token's normed row, written to both of its rows: one warp per
+  // token, or, with fewer tokens than warps in the CTA (small batches), every
+  // warp a share of each token's chunks (one warp's chunk loads were the
+  // latency of the step: 17-20 us at T = 8, 9-10 us shared)
   const int nchunk = d >> 3;
-  for (int t = t0 + warp; t < t1; t += kWarps) {
+  // one token's row: this lane's chunks c0, c0 + STEP, ... (STEP a compile-time
+  // constant, so the loop unrolls and its loads issue together)
+  auto row = [&](int t, int c0, auto step_tag) {
+    constexpr int STEP = decltype(step_tag)::value;
     const int ra = row_of_slot[2 * t], rb = row_of_slot[2 * t + 1];
     const bool wa = !(checks && ra >= rows_cap), wb = !(checks && rb >= rows_cap);
     const float r = rnorm[t];
     const __nv_bfloat16* src = x + (size_t)t * d;
     bool sat = false;
 #pragma unroll 8
-    for (int ch = lane; ch < nchunk; ch += 32) {
-      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(src) + ch);  // (plain loads: the unrolled
-                                                                      // iterations' loads issue together)
+    for (int ch = c0; ch < nchunk; ch += STEP) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(src) + ch);
       const float4 sa = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)ch * 8));
       const float4 sb = __ldg(reinterpret_cast<const float4*>(s_pre + (size_t)ch * 8 + 4));
       uint4 v;
@@ -297,6 +303,11 @@ __global__ void __launch_bounds__(kGroupThreads) group_rows_kernel(
       if (wb) reinterpret_cast<uint4*>(xn_perm + (size_t)rb * d)[ch] = v;
     }
     if (sat && err) atomicOr(err, kErrSaturate);
+  };
+  if (t1 - t0 < kWarps) {  // few tokens (small batches): every warp a share of each token's chunks
+    for (int t = t0; t < t1; ++t) row(t, lane + 32 * warp, std::integral_constant<int, 32 * kWarps>{});
+  } else {  // one warp per token
+    for (int t = t0 + warp; t < t1; t += kWarps) row(t, lane, std::integral_constant<int, 32>{});
   }
 
   // ---- 4. padding rows, row p of the padding handled by CTA p % G
