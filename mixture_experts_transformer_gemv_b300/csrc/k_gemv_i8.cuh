@@ -36,9 +36,9 @@
 // then reads its weights twice), so one TMA box brings the group's 8 rows of a
 // block and another their 8 scales.
 //
-// Data path per k-block of 128: TMA brings the int8 weight tile(s) (128 x 128,
-// 128-byte swizzle), the expert's 8 quantised rows (8 x 256 bytes) and their 8
-// scales into a ring of shared-memory stages; sixteen compute warps read the
+// Data path per k-block of 128: TMA brings two int8 weight tiles (128 x 128,
+// 128-byte swizzle), the slot group's 8 quantised rows (8 x 256 bytes) and their
+// 8 scales into a ring of shared-memory stages; sixteen compute warps read the
 // weights once each.  Compute lanes: lane = 8 g + c, c the 16-byte chunk (k in
 // [16 c, 16 c + 16)) and g a group of weight rows; the eight lanes of a group
 // hold the eight chunks of the same rows, so a 16-byte load per lane is

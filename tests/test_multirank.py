@@ -108,3 +108,27 @@ def test_attention_work_counts():
     assert w["qkv"] == ("tensor", 2.0 * 37 * 256 * (4 + 2 * 2) * 128)
     assert w["oproj"] == ("tensor", 2.0 * 37 * 4 * 128 * 256)
     assert bench.attn_compulsory_bytes(inp) == 4 * 37 * 128 * 2 + 2 * 2 * 37 * 128 * 2 + 37 * 4 * 128 * 2
+
+
+def test_bench_names_the_kernel_of_each_path():
+    """The kernel the bench's roofline names for each path of the layer: the
+    int8 GEMV kernels up to 16 tokens (grouped scales as the second template
+    argument), the bf16 weight-streaming kernels up to 16, the paired grouped
+    GEMMs from F = 16384 and T = 2048, and the same names ncu prints."""
+    import bench
+    import synth
+    i8 = synth.make_inputs(16, 256, 512, 3, name="n", weight_dtype="int8")
+    assert bench.kernel_function("up_geglu", i8)[0] == "gemv_i8_kernel<0, 0>"
+    assert bench.kernel_function("down", i8)[0] == "gemv_i8_kernel<1, 0>"
+    g8 = synth.make_inputs(8, 1024, 1024, 3, name="n", weight_dtype="int8", int8_scale_shape=(8, 8))
+    assert bench.kernel_function("down", g8)[0] == "gemv_i8_kernel<1, 1>"
+    assert bench.kernel_function("up_geglu", synth.make_inputs(17, 256, 512, 3, name="n", weight_dtype="int8"))[0] \
+        == "grouped_gemm_kernel<0, 1, 1>"
+    assert bench.kernel_function("up_geglu", synth.make_inputs(8, 256, 512, 3, name="n"))[0] == "decode_gemm_kernel<0>"
+    big = synth.MoeInputs(**{**synth.make_inputs(16, 256, 512, 3, name="n").__dict__, "T": 2048, "F": 16384})
+    assert bench.kernel_function("down", big)[0] == "grouped_gemm_kernel<1, 0, 2>"
+    for role in ("up_geglu", "down"):  # every named source file exists (the traffic record's hash)
+        for inp in (i8, g8, big):
+            bench.source_hash(bench.kernel_function(role, inp)[1])
+    assert bench.INT8_BAND_TOKENS == tuple(sorted(bench.INT8_BAND_TOKENS))
+    assert max(bench.INT8_BAND_TOKENS) <= bench.GEMV_I8_MAX_T == bench.DECODE_MAX_T
