@@ -84,7 +84,8 @@ typedef struct {
    * needs d and F to be multiples of 128 G.  With G == 1 the scale multiplies
    * the fp32 result of the reduction (exact); with G > 1 it multiplies each
    * weight as it is converted on chip, rounded once to bf16 (fp16 on the T <= 16
-   * path). */
+   * tensor-core path), or, on the T <= 16 CUDA-core GEMV path, each integer
+   * block sum in fp32. */
   int32_t scale_experts;
   int32_t scale_groups;
 } moe_config_t;
